@@ -1,0 +1,343 @@
+"""Seeded synthetic inputs for paged-KV decode attention.
+
+This module is shared by the tests, the benchmark and the oracle checks. It
+draws random numbers and lays them out; it holds none of the attention
+arithmetic. The workloads follow the statement of the problem on the ROCm
+blog page "Implementing a High-Performance Custom Diffusion Attention Kernel
+with FlyDSL" (introduction, item 1: paged KV caches plus scratch storage for
+speculatively generated draft tokens) and the MSLK pull request "[ROCm] Add
+FlyDSL paged-attention decode backend (dense + fp8) with benchmark" (Kernels:
+dense bf16 and native fp8 e4m3fn KV with a symmetric per-token scale).
+
+Layouts (all row-major, contiguous):
+    q            [B, T, Hq, D]           bf16
+    k/v cache    [num_pages, P, Hkv, D]  bf16, or e4m3fn codes as uint8
+    k/v scale    [num_pages, P, Hkv]     float32 (fp8 only)
+    block_tables [B, max_blocks]         int32, -1 where unused
+    context_lens [B]                     int32
+    k/v scratch  [B, T, Hkv, D]          bf16 (draft-block mode only)
+
+Random streams: every tensor has its own stream id, and large tensors are
+filled in chunks of whole pages, each chunk from its own generator seeded by
+(seed, stream id, chunk index). The data are therefore a pure function of
+the seed, independent of the number of threads used to make them.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+import os
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+E4M3FN_MAX = 448.0
+
+_STREAM_CTX = 1
+_STREAM_PERM = 2
+_STREAM_Q = 3
+_STREAM_K = 4
+_STREAM_V = 5
+_STREAM_KS = 6
+_STREAM_VS = 7
+
+# Elements per generator chunk (whole pages are kept together).
+_CHUNK_ELEMS = 1 << 22
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeSpec:
+    """Shape and value recipe of one decode workload."""
+
+    name: str
+    batch: int
+    q_tokens: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    # Either explicit context lengths, or an inclusive uniform range.
+    context_lens: Optional[Sequence[int]] = None
+    ctx_range: Optional[tuple] = None
+    kv_format: str = "bf16"  # "bf16" or "fp8"
+    draft_scratch: bool = False  # TiDAR draft block: contiguous scratch KV
+    pool_pages: Optional[int] = None  # None: exactly the pages in use
+    max_blocks_per_seq: Optional[int] = None  # None: from the largest context
+    seed: int = 0
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+# The five workloads of the decode engine (sizes from the problem statement).
+SPECS = {
+    "tiny": DecodeSpec("tiny", batch=2, q_tokens=1, num_q_heads=4, num_kv_heads=1,
+                       head_dim=64, page_size=16, context_lens=(37, 100),
+                       pool_pages=16, seed=0),
+    "gqa": DecodeSpec("gqa", batch=32, q_tokens=1, num_q_heads=32, num_kv_heads=8,
+                      head_dim=128, page_size=16, ctx_range=(512, 8192),
+                      max_blocks_per_seq=8192 // 16, seed=1),
+    "long": DecodeSpec("long", batch=4, q_tokens=1, num_q_heads=64, num_kv_heads=8,
+                       head_dim=128, page_size=64, context_lens=(131072,) * 4, seed=2),
+    "fp8": DecodeSpec("fp8", batch=64, q_tokens=1, num_q_heads=32, num_kv_heads=2,
+                      head_dim=256, page_size=16, ctx_range=(1024, 16384),
+                      kv_format="fp8", max_blocks_per_seq=16384 // 16, seed=3),
+    "tidar": DecodeSpec("tidar", batch=16, q_tokens=8, num_q_heads=32, num_kv_heads=8,
+                        head_dim=128, page_size=16, ctx_range=(2048, 8192),
+                        draft_scratch=True, max_blocks_per_seq=8192 // 16, seed=4),
+}
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    """Host (CPU) tensors of one decode problem."""
+
+    spec: DecodeSpec
+    q: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor
+    context_lens: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+    k_scratch: Optional[torch.Tensor] = None
+    v_scratch: Optional[torch.Tensor] = None
+
+    @property
+    def scale(self) -> float:
+        return self.spec.scale
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    def tensors(self):
+        names = ["q", "k_cache", "v_cache", "block_tables", "context_lens",
+                 "k_scale", "v_scale", "k_scratch", "v_scratch"]
+        return {n: getattr(self, n) for n in names if getattr(self, n) is not None}
+
+    def to(self, device, non_blocking: bool = False) -> "DecodeInputs":
+        moved = {n: t.to(device, non_blocking=non_blocking) for n, t in self.tensors().items()}
+        return dataclasses.replace(self, **moved)
+
+    def pin_memory(self) -> "DecodeInputs":
+        return dataclasses.replace(self, **{n: t.pin_memory() for n, t in self.tensors().items()})
+
+    # Raw-bit numpy views for the oracle (bf16 as uint16, fp8 as uint8).
+    def numpy_bits(self):
+        def bits(t):
+            if t is None:
+                return None
+            if t.dtype == torch.bfloat16:
+                return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+            return t.contiguous().numpy()
+        return {n: bits(t) for n, t in self.tensors().items()}
+
+
+def _rng(seed: int, stream: int, chunk: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, stream, chunk])))
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def _parallel(fn, n: int) -> None:
+    """Run fn(i) for i in range(n) on a few threads (numpy releases the GIL)."""
+    nt = min(_threads(), n)
+    if nt <= 1:
+        for i in range(n):
+            fn(i)
+        return
+    err = []
+
+    def worker(w):
+        try:
+            for i in range(w, n, nt):
+                fn(i)
+        except BaseException as e:  # surfaced below
+            err.append(e)
+
+    ths = [threading.Thread(target=worker, args=(w,)) for w in range(nt)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    if err:
+        raise err[0]
+
+
+def _normal_bf16(shape, seed: int, stream: int, rows_per_chunk: int) -> torch.Tensor:
+    """N(0,1) float32 draws rounded to bf16 (round to nearest even), chunked on dim 0."""
+    out = torch.empty(shape, dtype=torch.bfloat16)
+    n0 = shape[0]
+    nchunks = max(1, -(-n0 // rows_per_chunk))
+    row_elems = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+
+    def fill(c):
+        r0, r1 = c * rows_per_chunk, min(n0, (c + 1) * rows_per_chunk)
+        buf = np.empty((r1 - r0) * row_elems, dtype=np.float32)
+        _rng(seed, stream, c).standard_normal(out=buf, dtype=np.float32)
+        out[r0:r1] = torch.from_numpy(buf).view((r1 - r0,) + tuple(shape[1:])).to(torch.bfloat16)
+
+    _parallel(fill, nchunks)
+    return out
+
+
+def _normal_fp8(shape, seed: int, stream: int, rows_per_chunk: int):
+    """N(0,1) float32 draws quantised to e4m3fn with a symmetric scale per
+    (page, token, kv head): scale = amax over D / 448 (fp32), code = RNE of
+    clamp(x / scale, -448, 448). An all-zero vector gets scale 1."""
+    codes = torch.empty(shape, dtype=torch.uint8)
+    scales = torch.empty(shape[:-1], dtype=torch.float32)
+    n0 = shape[0]
+    nchunks = max(1, -(-n0 // rows_per_chunk))
+    row_elems = int(np.prod(shape[1:]))
+
+    def fill(c):
+        r0, r1 = c * rows_per_chunk, min(n0, (c + 1) * rows_per_chunk)
+        buf = np.empty((r1 - r0) * row_elems, dtype=np.float32)
+        _rng(seed, stream, c).standard_normal(out=buf, dtype=np.float32)
+        x = torch.from_numpy(buf).view((r1 - r0,) + tuple(shape[1:]))
+        amax = x.abs().amax(dim=-1)
+        s = torch.where(amax > 0, amax / E4M3FN_MAX, torch.ones_like(amax))
+        y = torch.clamp(x / s.unsqueeze(-1), -E4M3FN_MAX, E4M3FN_MAX)
+        codes[r0:r1] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+        scales[r0:r1] = s
+
+    _parallel(fill, nchunks)
+    return codes, scales
+
+
+def draw_context_lens(spec: DecodeSpec) -> np.ndarray:
+    if spec.context_lens is not None:
+        lens = np.asarray(spec.context_lens, dtype=np.int64)
+        assert lens.shape == (spec.batch,)
+        return lens
+    lo, hi = spec.ctx_range
+    return _rng(spec.seed, _STREAM_CTX).integers(lo, hi, size=spec.batch, endpoint=True)
+
+
+def make_inputs(spec: DecodeSpec, poison: bool = False) -> DecodeInputs:
+    """Build the host tensors of one decode problem.
+
+    Pages are drawn from a pool through a seeded random permutation: the
+    sequences take consecutive slices of the permuted page ids, in batch
+    order. With poison=True every value that must never be read is set to
+    NaN (unused pool pages, and slots past the context end inside the last
+    page of each sequence, including their fp8 scales) and unused
+    block-table entries are set to INT32_MAX instead of -1.
+    """
+    B, T, Hq, Hkv, D, P = (spec.batch, spec.q_tokens, spec.num_q_heads,
+                           spec.num_kv_heads, spec.head_dim, spec.page_size)
+    assert Hq % Hkv == 0
+    lens = draw_context_lens(spec)
+    npages = [(int(c) + P - 1) // P for c in lens]
+    used = int(sum(npages))
+    pool = spec.pool_pages if spec.pool_pages is not None else max(used, 1)
+    assert pool >= used, "page pool smaller than the pages in use"
+    max_blocks = spec.max_blocks_per_seq if spec.max_blocks_per_seq is not None else max(1, max(npages))
+    assert max_blocks >= max(npages)
+
+    perm = _rng(spec.seed, _STREAM_PERM).permutation(pool).astype(np.int64)
+    bt = np.full((B, max_blocks), np.iinfo(np.int32).max if poison else -1, dtype=np.int64)
+    off = 0
+    for b in range(B):
+        bt[b, :npages[b]] = perm[off:off + npages[b]]
+        off += npages[b]
+
+    page_elems = P * Hkv * D
+    rows_per_chunk = max(1, _CHUNK_ELEMS // page_elems)
+    q = _normal_bf16((B, T, Hq, D), spec.seed, _STREAM_Q, max(1, _CHUNK_ELEMS // (T * Hq * D)))
+    k_scale = v_scale = None
+    if spec.kv_format == "bf16":
+        k = _normal_bf16((pool, P, Hkv, D), spec.seed, _STREAM_K, rows_per_chunk)
+        v = _normal_bf16((pool, P, Hkv, D), spec.seed, _STREAM_V, rows_per_chunk)
+    elif spec.kv_format == "fp8":
+        k, k_scale = _normal_fp8((pool, P, Hkv, D), spec.seed, _STREAM_K, rows_per_chunk)
+        v, v_scale = _normal_fp8((pool, P, Hkv, D), spec.seed, _STREAM_V, rows_per_chunk)
+    else:
+        raise ValueError(f"unknown kv_format {spec.kv_format!r}")
+
+    k_scr = v_scr = None
+    if spec.draft_scratch:
+        k_scr = _normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_KS, B)
+        v_scr = _normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_VS, B)
+
+    if poison:
+        _poison(k, v, k_scale, v_scale, bt, lens, npages, pool, P)
+
+    return DecodeInputs(
+        spec=spec, q=q, k_cache=k, v_cache=v,
+        block_tables=torch.from_numpy(bt.astype(np.int32)),
+        context_lens=torch.from_numpy(np.asarray(lens, dtype=np.int32)),
+        k_scale=k_scale, v_scale=v_scale, k_scratch=k_scr, v_scratch=v_scr)
+
+
+def _poison(k, v, k_scale, v_scale, bt, lens, npages, pool, P):
+    in_use = np.zeros(pool, dtype=bool)
+    for b in range(len(lens)):
+        in_use[bt[b, :npages[b]]] = True
+    unused = torch.from_numpy(np.nonzero(~in_use)[0])
+
+    def nan_fill(t, idx, slot0=None):
+        if t.dtype == torch.bfloat16:
+            val = float("nan")
+        elif t.dtype == torch.uint8:
+            val = 0x7F  # e4m3fn NaN
+        else:
+            val = float("nan")
+        if slot0 is None:
+            t[idx] = val
+        else:
+            t[idx, slot0:] = val
+
+    for t in (k, v, k_scale, v_scale):
+        if t is not None and len(unused):
+            nan_fill(t, unused)
+    for b in range(len(lens)):
+        c = int(lens[b])
+        if npages[b] and c % P:
+            last = int(bt[b, npages[b] - 1])
+            for t in (k, v, k_scale, v_scale):
+                if t is not None:
+                    nan_fill(t, last, c % P)
+
+
+def custom_spec(name="custom", **kw) -> DecodeSpec:
+    """A DecodeSpec for ad-hoc shapes (tests)."""
+    return DecodeSpec(name=name, **kw)
+
+
+def algorithmic_bytes(inp: DecodeInputs) -> int:
+    """Bytes a decode call must move at minimum: the KV rows of valid tokens,
+    their fp8 scales, the block-table entries in use, q, out, lse,
+    context_lens and the draft-block scratch KV. Split-K scratch traffic is
+    not counted."""
+    s = inp.spec
+    lens = inp.context_lens.to(torch.int64)
+    tokens = int(lens.sum())
+    pages = int(((lens + s.page_size - 1) // s.page_size).sum())
+    kv_elem = 1 if s.kv_format == "fp8" else 2
+    nbytes = 2 * tokens * s.num_kv_heads * s.head_dim * kv_elem
+    if s.kv_format == "fp8":
+        nbytes += 2 * tokens * s.num_kv_heads * 4
+    nbytes += pages * 4
+    rows = s.batch * s.q_tokens * s.num_q_heads
+    nbytes += rows * s.head_dim * 2 * 2  # q in, out
+    nbytes += rows * 4 + s.batch * 4  # lse, context_lens
+    if s.draft_scratch:
+        nbytes += 2 * s.batch * s.q_tokens * s.num_kv_heads * s.head_dim * 2
+    return nbytes
