@@ -1,0 +1,160 @@
+/*
+ * pa_decode.h - C ABI of the GB300 (sm_103a) paged-KV decode attention engine.
+ *
+ * The operation: softmax attention of a few query tokens per sequence over a
+ * KV cache stored in fixed-size physical pages and addressed through a
+ * per-sequence block table, with grouped query heads, split-K partials
+ * combined by their log-sum-exp, an fp8 e4m3fn cache with per-token scales,
+ * and a draft-block (TiDAR) mode with extra contiguous scratch KV.
+ * Sources: ROCm blog "Implementing a High-Performance Custom Diffusion
+ * Attention Kernel with FlyDSL" (introduction, items 1-3: paged KV caches,
+ * scratch storage for speculatively generated tokens, FlashAttention and
+ * split-K; section Graph Capture: runtime versus fixed parameters) and the
+ * MSLK pull request "[ROCm] Add FlyDSL paged-attention decode backend
+ * (dense + fp8) with benchmark" (section Kernels: dense decode, native fp8
+ * decode with symmetric per-token scale, split-K reduce, stream threaded
+ * through compute and reduce launches so the calls can be graph-captured).
+ *
+ * Definition computed, for every sequence b < B, query token t < T and query
+ * head h < Hq, with kv head g = h / G and G = Hq / Hkv:
+ *   keys j < C_b = context_lens[b]; key j lives in physical page
+ *   block_tables[b][j / P], slot j % P, kv head g;
+ *   s_j = scale * <q[b][t][h], k_j>;  out = sum_j softmax(s)_j v_j;
+ *   lse = ln sum_j exp(s_j)   (natural log, scale included).
+ * An empty key set gives out = 0 and lse = -inf.
+ *
+ * Common conventions
+ *  - Every pointer argument is a DEVICE pointer on the current CUDA device,
+ *    16-byte aligned; every tensor is dense row-major (contiguous).
+ *  - Layouts: q, out [B, T, Hq, D] bf16; k_cache, v_cache
+ *    [num_pages, P, Hkv, D] (bf16, or e4m3fn bytes); k_scale, v_scale
+ *    [num_pages, P, Hkv] fp32; block_tables [B, max_blocks_per_seq] int32;
+ *    context_lens [B] int32; lse [B, T, Hq] fp32; k_scratch, v_scratch
+ *    [B, T, Hkv, D] bf16.
+ *  - context_lens[b] is clamped on the device to [0, max_blocks_per_seq * P];
+ *    only the first ceil(C_b / P) block-table entries of a row are read.
+ *    A page id outside [0, num_pages) reads zeros (the copy engine fills
+ *    out-of-range boxes); it never faults.
+ *  - Ownership: the caller owns every buffer, including the workspace. The
+ *    library allocates nothing, keeps no pointer after return, performs no
+ *    host<->device copy and no synchronisation. Work is enqueued on `stream`
+ *    and completes asynchronously. Calls may be captured into a CUDA graph;
+ *    the first call on a device does one-time set-up (device attribute
+ *    queries, kernel attributes), so make it before capturing.
+ *  - Errors: argument and shape problems are reported BEFORE any launch
+ *    (out, lse and the workspace are untouched). PA_ERR_CUDA reports a
+ *    launch failure (cudaGetLastError). Nothing aborts or throws across the
+ *    ABI. A device-side wait that runs out of time (a bug, never expected)
+ *    makes the kernel stop early and set a flag read by
+ *    pa_decode_device_error().
+ *
+ * Supported: D in {64, 128, 256} (fp8: {128, 256}); P in {16, 32, 64, 128,
+ * 256}; M = G * T <= 32 query rows per kv head; fp8 needs Hkv <= 8.
+ * Anything else returns PA_ERR_UNSUPPORTED.
+ *
+ * num_splits:
+ *   0   auto. The flattened list of (sequence, kv head, page) work is cut into
+ *       equal contiguous shares, one per CTA of a grid that fills the SMs, so
+ *       sequences of any length mix are balanced. Needs the workspace of
+ *       pa_decode_workspace_size(shape, 0) (its layout is private).
+ *   1   one CTA per (sequence, kv head) writes out/lse directly; no workspace.
+ *   S>1 split s of sequence b covers pages [s*pps, min((s+1)*pps, n_b)),
+ *       pps = ceil(n_b / S), n_b = ceil(C_b / P); draft-block scratch tokens
+ *       belong to split S-1. The workspace holds, at byte 0, part_out
+ *       float [B][T][Hq][S][D] (each split normalised over its own keys) and,
+ *       at byte align256(B*T*Hq*S*D*4), part_lse float [B][T][Hq][S]
+ *       (-inf for an empty split); pa_decode_reduce() then combines them.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. NULL = legacy stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad shape, bad scale */
+  PA_ERR_UNSUPPORTED = 2, /* valid but outside the compiled kernel set */
+  PA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  PA_ERR_CUDA = 4         /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef struct pa_shape {
+  int32_t batch;              /* B >= 0 (0: nothing to do) */
+  int32_t q_tokens;           /* T >= 1: 1 for decode, the draft length for TiDAR */
+  int32_t num_q_heads;        /* Hq >= 1, a multiple of num_kv_heads */
+  int32_t num_kv_heads;       /* Hkv >= 1 */
+  int32_t head_dim;           /* D */
+  int32_t page_size;          /* P, tokens per physical page */
+  int32_t num_pages;          /* physical pages in each cache tensor, >= 1 */
+  int32_t max_blocks_per_seq; /* columns of block_tables, >= 1 */
+} pa_shape;
+
+/* Bytes of workspace pa_decode* needs for this shape and num_splits (0 for
+ * num_splits == 1). For num_splits == 0 the size depends on the current
+ * device's SM count. Returns 0 as well for an invalid shape. */
+size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits);
+
+/* Dense bf16 paged decode (the MSLK page's dense decode kernel).
+ * q, k_cache, v_cache, out: bf16 as above. lse may be NULL. scale: the
+ * softmax scale (finite), e.g. 1/sqrt(D). */
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens,
+                    const pa_shape* shape, float scale, void* out, float* lse,
+                    int32_t num_splits, void* workspace, size_t workspace_bytes,
+                    pa_stream_t stream);
+
+/* Native fp8 paged decode (the MSLK page's fp8 kernel: OCP e4m3fn codes with
+ * a symmetric per-token, per-kv-head fp32 scale; value = code * scale).
+ * q is bf16 and is not quantised. The codes are converted exactly in
+ * registers; the products run in f16 with fp32 accumulation, so |q| must be
+ * below 65504. Otherwise as pa_decode. */
+pa_status pa_decode_fp8(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                        const float* k_scale, const float* v_scale,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        const pa_shape* shape, float scale, void* out, float* lse,
+                        int32_t num_splits, void* workspace, size_t workspace_bytes,
+                        pa_stream_t stream);
+
+/* Draft-block (TiDAR) decode: as pa_decode, plus the T scratch tokens of each
+ * sequence (k_scratch, v_scratch [B, T, Hkv, D] bf16, contiguous) as extra
+ * keys after the paged prefix. Every draft token attends to the whole prefix
+ * and to all T scratch tokens (no mask inside the draft block); C_b counts
+ * the paged prefix only. (ROCm blog, introduction item 1.) */
+pa_status pa_decode_tidar(const void* q, const void* k_cache, const void* v_cache,
+                          const void* k_scratch, const void* v_scratch,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          const pa_shape* shape, float scale, void* out, float* lse,
+                          int32_t num_splits, void* workspace, size_t workspace_bytes,
+                          pa_stream_t stream);
+
+/* Split-K combine (the MSLK page's pa_decode_reduce): for every (b, t, h),
+ * M = max_s lse_s, w_s = exp(lse_s - M), out = sum_s w_s part_out_s / sum_s w_s,
+ * lse = M + ln sum_s w_s; all splits empty gives out = 0, lse = -inf.
+ * part_out float [B][T][Hq][num_splits][D], part_lse float [B][T][Hq][num_splits]
+ * (the layout pa_decode writes for num_splits > 1). out bf16 [B][T][Hq][D];
+ * lse may be NULL. num_splits >= 1. Only batch, q_tokens, num_q_heads and
+ * head_dim of shape are used (head_dim a multiple of 4, <= 1024). */
+pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t num_splits,
+                           const pa_shape* shape, void* out, float* lse, pa_stream_t stream);
+
+/* A static description of a status code (never NULL). */
+const char* pa_status_string(pa_status status);
+
+/* Reads and clears the current device's error flags set by the kernels
+ * (bit 0: a pipeline wait in the split kernel ran out of time). Synchronous;
+ * for diagnostics only, never inside stream capture. */
+pa_status pa_decode_device_error(int32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

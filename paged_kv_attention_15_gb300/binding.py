@@ -1,0 +1,197 @@
+"""ctypes binding of libpadecode.so (include/pa_decode.h).
+
+Argument marshalling only: torch supplies device memory and the current
+stream; every step of the computation runs in the library's CUDA kernels.
+The library is loaded on first use; if it is missing the call raises, there
+is no other implementation to fall back to.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpadecode.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "pa_decode.h")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+
+
+class PaShape(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("q_tokens", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+    ]
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_DECODE_TAIL = [ctypes.POINTER(PaShape), ctypes.c_float, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]
+_SIGNATURES = {
+    "pa_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(PaShape), ctypes.c_int32]),
+    "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _P] + _DECODE_TAIL),
+    "pa_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
+    "pa_decode_tidar": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
+    "pa_decode_reduce": (ctypes.c_int, [_P, _P, ctypes.c_int32, ctypes.POINTER(PaShape), _P, _P, _P]),
+    "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pa_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32)]),
+}
+
+
+def header_functions() -> list:
+    """Names of the functions include/pa_decode.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with paged_kv_attention_15_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor) -> PaShape:
+    B, T, Hq, D = q.shape
+    num_pages, P, Hkv, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("q and k_cache head_dim differ")
+    return PaShape(B, T, Hq, Hkv, D, P, num_pages, block_tables.shape[1])
+
+
+def workspace_size(shape: PaShape, num_splits: int) -> int:
+    return int(lib().pa_decode_workspace_size(ctypes.byref(shape), int(num_splits)))
+
+
+def _need_contig(**tensors):
+    for name, t in tensors.items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+           context_lens: torch.Tensor, scale: float, *, k_scale: Optional[torch.Tensor] = None,
+           v_scale: Optional[torch.Tensor] = None, k_scratch: Optional[torch.Tensor] = None,
+           v_scratch: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+           want_lse: bool = True, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Paged decode through pa_decode / pa_decode_fp8 / pa_decode_tidar.
+
+    The fp8 entry point is used when k_cache is uint8 (e4m3fn codes, with
+    k_scale/v_scale); the draft-block entry point when k_scratch is given.
+    out, lse and the workspace are allocated here when not passed in."""
+    _need_contig(q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables, context_lens=context_lens,
+                 k_scale=k_scale, v_scale=v_scale, k_scratch=k_scratch, v_scratch=v_scratch, out=out, lse=lse)
+    shape = make_shape(q, k_cache, block_tables)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    need = workspace_size(shape, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    L = lib()
+    tail = (ctypes.byref(shape), float(scale), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), ws_bytes,
+            _stream(stream))
+    if k_cache.dtype == torch.uint8:
+        st = L.pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                             _ptr(block_tables), _ptr(context_lens), *tail)
+        _check(st, "pa_decode_fp8")
+    elif k_scratch is not None:
+        st = L.pa_decode_tidar(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scratch), _ptr(v_scratch),
+                               _ptr(block_tables), _ptr(context_lens), *tail)
+        _check(st, "pa_decode_tidar")
+    else:
+        st = L.pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), *tail)
+        _check(st, "pa_decode")
+    return out, lse
+
+
+def decode_inputs(inp, **kw):
+    """decode() on a DecodeInputs bundle already on the device."""
+    return decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale,
+                  k_scale=inp.k_scale, v_scale=inp.v_scale, k_scratch=inp.k_scratch, v_scratch=inp.v_scratch,
+                  **kw)
+
+
+def split_workspace_views(workspace: torch.Tensor, B: int, T: int, Hq: int, S: int, D: int):
+    """part_out [B,T,Hq,S,D] and part_lse [B,T,Hq,S] inside an explicit-split workspace."""
+    rows = B * T * Hq * S
+    off = (rows * D * 4 + 255) // 256 * 256
+    flat = workspace.view(torch.uint8)
+    part_out = flat[: rows * D * 4].view(torch.float32).view(B, T, Hq, S, D)
+    part_lse = flat[off: off + rows * 4].view(torch.float32).view(B, T, Hq, S)
+    return part_out, part_lse
+
+
+def decode_reduce(part_out: torch.Tensor, part_lse: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                  lse: Optional[torch.Tensor] = None, stream=None):
+    """pa_decode_reduce: combine part_out [B,T,Hq,S,D] by part_lse [B,T,Hq,S]."""
+    _need_contig(part_out=part_out, part_lse=part_lse)
+    B, T, Hq, S, D = part_out.shape
+    shape = PaShape(B, T, Hq, 1, D, 16, 1, 1)
+    if out is None:
+        out = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=part_out.device)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=part_out.device)
+    st = lib().pa_decode_reduce(_ptr(part_out), _ptr(part_lse), S, ctypes.byref(shape), _ptr(out), _ptr(lse),
+                                _stream(stream))
+    _check(st, "pa_decode_reduce")
+    return out, lse
+
+
+def device_error() -> int:
+    """Reads and clears the kernels' error flags on the current device (synchronous)."""
+    v = ctypes.c_int32(0)
+    _check(lib().pa_decode_device_error(ctypes.byref(v)), "pa_decode_device_error")
+    return int(v.value)

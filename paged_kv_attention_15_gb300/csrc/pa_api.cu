@@ -1,0 +1,438 @@
+// C ABI of the paged-KV decode engine: argument checks, work scheduling,
+// TMA descriptor encoding and kernel launches. See include/pa_decode.h.
+#include "pa_decode.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pa_launch.h"
+#include "pa_reduce.cuh"
+
+namespace {
+
+using pa::ReduceParams;
+using pa::SplitKernel;
+using pa::SplitParams;
+
+// Error flags written by the kernels (one word per device: each device has
+// its own copy of a module-scope __device__ variable).
+__device__ int g_pa_err_flags;
+
+constexpr int kMaxDevices = 64;
+constexpr int kKernelSlots = 16;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int smem_optin = 0;
+  int* err_flags = nullptr;
+  const void* smem_set[kKernelSlots] = {};
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+enum class Kind { kBf16, kFp8, kTidar };
+
+pa_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d.ready) {
+      if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PA_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_pa_err_flags) != cudaSuccess) return PA_ERR_CUDA;
+      d.err_flags = static_cast<int*>(ptr);
+      d.ready = true;
+    }
+  }
+  *out = &d;
+  return PA_OK;
+}
+
+// Raises the kernel's dynamic shared-memory limit once per device.
+pa_status ensure_smem_attr(DeviceState* d, const void* fn) {
+  for (int i = 0; i < kKernelSlots; ++i)
+    if (d->smem_set[i] == fn) return PA_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < kKernelSlots; ++i) {
+    if (d->smem_set[i] == fn) return PA_OK;
+    if (d->smem_set[i] == nullptr) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
+        return PA_ERR_CUDA;
+      d->smem_set[i] = fn;
+      return PA_OK;
+    }
+  }
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D map, dims innermost first, strides in bytes for dims 1..3, 128-byte swizzle.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims[4],
+              const uint64_t strides[3], const uint32_t box[4]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, dt, 4, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool pow2_in(int x, int lo, int hi) { return x >= lo && x <= hi && (x & (x - 1)) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Shape checks shared by every entry point.
+pa_status check_shape(const pa_shape* s, Kind kind) {
+  if (!s) return PA_ERR_INVALID_ARG;
+  if (s->batch < 0 || s->q_tokens < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->head_dim < 1 ||
+      s->page_size < 1 || s->num_pages < 1 || s->max_blocks_per_seq < 1)
+    return PA_ERR_INVALID_ARG;
+  if (s->num_q_heads % s->num_kv_heads) return PA_ERR_INVALID_ARG;
+  if ((int64_t)s->max_blocks_per_seq * s->page_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+  const int D = s->head_dim;
+  if (kind == Kind::kFp8) {
+    if (D != 128 && D != 256) return PA_ERR_UNSUPPORTED;
+    if (s->num_kv_heads > pa::kMaxHkvFp8) return PA_ERR_UNSUPPORTED;
+  } else if (D != 64 && D != 128 && D != 256) {
+    return PA_ERR_UNSUPPORTED;
+  }
+  if (!pow2_in(s->page_size, 16, 256)) return PA_ERR_UNSUPPORTED;
+  const int64_t M = (int64_t)(s->num_q_heads / s->num_kv_heads) * s->q_tokens;
+  if (M > 32) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+SplitKernel pick_kernel(Kind kind, int D, int MT) {
+  return kind == Kind::kFp8 ? pa::split_kernel_fp8(D, MT) : pa::split_kernel_bf16(D, MT);
+}
+
+int row_tiles(const pa_shape* s) {
+  const int M = (s->num_q_heads / s->num_kv_heads) * s->q_tokens;
+  return (M + 15) / 16;
+}
+
+// The launch plan of a call: mode, grid and workspace.
+struct Plan {
+  bool balanced = false;  // equal shares of the flattened pages, one CTA per SM
+  int splits = 1;         // explicit mode
+  int grid = 0;           // balanced mode CTAs
+  size_t smem = 0;
+  size_t ws_bytes = 0;
+  size_t part_lse_off = 0;
+};
+
+pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d, Plan* plan) {
+  const SplitKernel k = pick_kernel(kind, s->head_dim, row_tiles(s));
+  if (!k.fn) return PA_ERR_UNSUPPORTED;
+  const int B = s->batch, T = s->q_tokens, Hq = s->num_q_heads, Hkv = s->num_kv_heads, D = s->head_dim;
+  const int M = (Hq / Hkv) * T;
+  Plan p;
+  if (num_splits == 0) {
+    const size_t smem = (size_t)k.smem_fixed + (size_t)(2 * B + 1) * 4;
+    if (smem <= (size_t)d->smem_optin) {
+      p.balanced = true;
+      p.grid = d->sms;
+      p.smem = smem;
+      const size_t slots = (size_t)B * Hkv + p.grid;
+      p.part_lse_off = align256(slots * M * D * sizeof(float));
+      p.ws_bytes = p.part_lse_off + align256(slots * M * sizeof(float));
+      *plan = p;
+      return PA_OK;
+    }
+    // Too many sequences for the on-chip table: explicit splits that give
+    // every SM about two CTAs.
+    const int units = B * Hkv;
+    int S = (2 * d->sms + units - 1) / units;
+    S = S < 1 ? 1 : (S > s->max_blocks_per_seq ? s->max_blocks_per_seq : S);
+    num_splits = S;
+  }
+  if (num_splits > 65535) return PA_ERR_UNSUPPORTED;
+  p.splits = num_splits;
+  p.smem = (size_t)k.smem_fixed;
+  if (p.smem > (size_t)d->smem_optin) return PA_ERR_UNSUPPORTED;
+  if (num_splits > 1) {
+    const size_t rows = (size_t)B * T * Hq * num_splits;
+    p.part_lse_off = align256(rows * D * sizeof(float));
+    p.ws_bytes = p.part_lse_off + align256(rows * sizeof(float));
+  }
+  *plan = p;
+  return PA_OK;
+}
+
+struct CallArgs {
+  Kind kind;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const void* k_scratch;
+  const void* v_scratch;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const pa_shape* shape;
+  float scale;
+  void* out;
+  float* lse;
+  int32_t num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+pa_status run_decode(const CallArgs& a) {
+  pa_status st = check_shape(a.shape, a.kind);
+  if (st != PA_OK) return st;
+  const pa_shape& s = *a.shape;
+  if (!std::isfinite(a.scale) || a.num_splits < 0) return PA_ERR_INVALID_ARG;
+  if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.out) return PA_ERR_INVALID_ARG;
+  if (!aligned(a.q, 16) || !aligned(a.k_cache, 16) || !aligned(a.v_cache, 16) || !aligned(a.out, 16) ||
+      !aligned(a.block_tables, 4) || !aligned(a.context_lens, 4) || (a.lse && !aligned(a.lse, 4)))
+    return PA_ERR_INVALID_ARG;
+  if (a.kind == Kind::kFp8 &&
+      (!a.k_scale || !a.v_scale || !aligned(a.k_scale, 16) || !aligned(a.v_scale, 16)))
+    return PA_ERR_INVALID_ARG;
+  if (a.kind == Kind::kTidar &&
+      (!a.k_scratch || !a.v_scratch || !aligned(a.k_scratch, 16) || !aligned(a.v_scratch, 16)))
+    return PA_ERR_INVALID_ARG;
+  if (s.batch == 0) return PA_OK;
+
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;
+  Plan plan;
+  if ((st = make_plan(a.shape, a.kind, a.num_splits, d, &plan)) != PA_OK) return st;
+  if (plan.ws_bytes) {
+    if (!a.workspace || a.workspace_bytes < plan.ws_bytes || !aligned(a.workspace, 256)) return PA_ERR_WORKSPACE;
+  }
+
+  const int B = s.batch, T = s.q_tokens, Hq = s.num_q_heads, Hkv = s.num_kv_heads, D = s.head_dim;
+  const int P = s.page_size, G = Hq / Hkv, M = G * T;
+  const bool fp8 = a.kind == Kind::kFp8;
+  const uint64_t e = fp8 ? 1 : 2;
+
+  static_assert(sizeof(SplitParams) % 64 == 0, "params must keep the descriptors aligned");
+  SplitParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2, (uint64_t)T * Hq * D * 2};
+    const uint32_t box[4] = {64u, (uint32_t)G, (uint32_t)T, 1u};
+    if (!make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, dims, str, box)) return PA_ERR_INVALID_ARG;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)P, (uint64_t)s.num_pages};
+    const uint64_t str[3] = {(uint64_t)D * e, (uint64_t)Hkv * D * e, (uint64_t)P * Hkv * D * e};
+    const uint32_t box[4] = {(uint32_t)(128 / e), 1u, (uint32_t)(P < pa::kTS ? P : pa::kTS), 1u};
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map(&p.tm_k, dt, a.k_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
+    if (!make_map(&p.tm_v, dt, a.v_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
+  }
+  if (a.kind == Kind::kTidar) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2, (uint64_t)T * Hkv * D * 2};
+    const uint32_t box[4] = {64u, 1u, (uint32_t)T, 1u};
+    if (!make_map(&p.tm_ks, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k_scratch, dims, str, box) ||
+        !make_map(&p.tm_vs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v_scratch, dims, str, box))
+      return PA_ERR_INVALID_ARG;
+  }
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.err_flags = d->err_flags;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.M = M;
+  p.P = P;
+  p.max_blocks = s.max_blocks_per_seq;
+  p.num_pages = s.num_pages;
+  p.num_splits = plan.balanced ? 0 : plan.splits;
+  p.tidar = a.kind == Kind::kTidar ? 1 : 0;
+  p.grid = plan.grid;
+  p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+  if (plan.ws_bytes) {
+    p.part_o = static_cast<float*>(a.workspace);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + plan.part_lse_off);
+  }
+
+  const SplitKernel k = pick_kernel(a.kind, D, row_tiles(a.shape));
+  if ((st = ensure_smem_attr(d, k.fn)) != PA_OK) return st;
+  const dim3 grid = plan.balanced ? dim3(plan.grid) : dim3(B * Hkv, plan.splits);
+  void* args[] = {&p};
+  if (cudaLaunchKernel(k.fn, grid, dim3(pa::kThreads), args, plan.smem, a.stream) != cudaSuccess)
+    return PA_ERR_CUDA;
+
+  if (plan.balanced || plan.splits > 1) {
+    ReduceParams r;
+    std::memset(&r, 0, sizeof(r));
+    r.part_o = p.part_o;
+    r.part_lse = p.part_lse;
+    r.out = p.out;
+    r.lse = p.lse;
+    r.context_lens = p.context_lens;
+    r.B = B;
+    r.T = T;
+    r.Hq = Hq;
+    r.Hkv = Hkv;
+    r.G = G;
+    r.M = M;
+    r.D = D;
+    r.P = P;
+    r.max_blocks = s.max_blocks_per_seq;
+    r.tidar = p.tidar;
+    r.num_splits = plan.balanced ? 0 : plan.splits;
+    r.grid = plan.grid;
+    void* rargs[] = {&r};
+    cudaError_t err;
+    if (plan.balanced)
+      err = cudaLaunchKernel(reinterpret_cast<const void*>(&pa::pa_reduce_balanced_kernel), dim3(B * Hkv),
+                             dim3(128), rargs, 0, a.stream);
+    else
+      err = cudaLaunchKernel(reinterpret_cast<const void*>(&pa::pa_reduce_splits_kernel),
+                             dim3((unsigned)(((size_t)B * T * Hq + 3) / 4)), dim3(128), rargs, 0, a.stream);
+    if (err != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits) {
+  if (check_shape(shape, Kind::kBf16) != PA_OK && check_shape(shape, Kind::kFp8) != PA_OK) return 0;
+  if (num_splits < 0) return 0;
+  if (num_splits == 1) return 0;
+  if (num_splits > 1) {
+    const size_t rows = (size_t)shape->batch * shape->q_tokens * shape->num_q_heads * num_splits;
+    return align256(rows * shape->head_dim * sizeof(float)) + align256(rows * sizeof(float));
+  }
+  DeviceState* d = nullptr;
+  if (device_state(&d) != PA_OK) return 0;
+  // The balanced plan does not depend on the KV format beyond the instance's
+  // fixed shared memory; take the larger of the two plans.
+  size_t best = 0;
+  for (Kind kind : {Kind::kBf16, Kind::kFp8}) {
+    if (check_shape(shape, kind) != PA_OK) continue;
+    Plan plan;
+    if (make_plan(shape, kind, 0, d, &plan) == PA_OK && plan.ws_bytes > best) best = plan.ws_bytes;
+  }
+  return best;
+}
+
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                    const int32_t* context_lens, const pa_shape* shape, float scale, void* out, float* lse,
+                    int32_t num_splits, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  CallArgs a{Kind::kBf16, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, block_tables, context_lens,
+             shape, scale, out, lse, num_splits, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)};
+  return run_decode(a);
+}
+
+pa_status pa_decode_fp8(const void* q, const uint8_t* k_cache, const uint8_t* v_cache, const float* k_scale,
+                        const float* v_scale, const int32_t* block_tables, const int32_t* context_lens,
+                        const pa_shape* shape, float scale, void* out, float* lse, int32_t num_splits,
+                        void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  CallArgs a{Kind::kFp8, q, k_cache, v_cache, k_scale, v_scale, nullptr, nullptr, block_tables, context_lens,
+             shape, scale, out, lse, num_splits, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)};
+  return run_decode(a);
+}
+
+pa_status pa_decode_tidar(const void* q, const void* k_cache, const void* v_cache, const void* k_scratch,
+                          const void* v_scratch, const int32_t* block_tables, const int32_t* context_lens,
+                          const pa_shape* shape, float scale, void* out, float* lse, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  CallArgs a{Kind::kTidar, q, k_cache, v_cache, nullptr, nullptr, k_scratch, v_scratch, block_tables,
+             context_lens, shape, scale, out, lse, num_splits, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream)};
+  return run_decode(a);
+}
+
+pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t num_splits, const pa_shape* shape,
+                           void* out, float* lse, pa_stream_t stream) {
+  if (!shape || !part_out || !part_lse || !out || num_splits < 1) return PA_ERR_INVALID_ARG;
+  if (shape->batch < 0 || shape->q_tokens < 1 || shape->num_q_heads < 1 || shape->head_dim < 4 ||
+      shape->head_dim % 4 || shape->head_dim > 1024)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(part_out, 16) || !aligned(part_lse, 4) || !aligned(out, 8) || (lse && !aligned(lse, 4)))
+    return PA_ERR_INVALID_ARG;
+  if (shape->batch == 0) return PA_OK;
+  ReduceParams r;
+  std::memset(&r, 0, sizeof(r));
+  r.part_o = part_out;
+  r.part_lse = part_lse;
+  r.out = static_cast<__nv_bfloat16*>(out);
+  r.lse = lse;
+  r.B = shape->batch;
+  r.T = shape->q_tokens;
+  r.Hq = shape->num_q_heads;
+  r.D = shape->head_dim;
+  r.num_splits = num_splits;
+  const size_t rows = (size_t)r.B * r.T * r.Hq;
+  void* rargs[] = {&r};
+  if (cudaLaunchKernel(reinterpret_cast<const void*>(&pa::pa_reduce_splits_kernel), dim3((unsigned)((rows + 3) / 4)),
+                       dim3(128), rargs, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+pa_status pa_decode_device_error(int32_t* flags) {
+  if (!flags) return PA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  pa_status st = device_state(&d);
+  if (st != PA_OK) return st;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_pa_err_flags, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_pa_err_flags, &zero, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+  *flags = v;
+  return PA_OK;
+}
+
+}  // extern "C"

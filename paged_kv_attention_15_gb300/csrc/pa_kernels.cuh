@@ -1,0 +1,753 @@
+// Paged-KV decode attention kernels for sm_103a.
+//
+// The split kernel computes softmax attention of the M = G * T query rows
+// that share one kv head (head packing: the GQA group times the draft
+// tokens form the MMA M dimension) over a contiguous range of that
+// sequence's paged keys, FlashAttention style: online max and sum in base 2,
+// rescaled accumulator, and a log-sum-exp per row. The reduce kernel merges
+// split-K partials by their log-sum-exp.
+// Sources: ROCm blog "Implementing a High-Performance Custom Diffusion
+// Attention Kernel with FlyDSL" (introduction items 1-3; "Match MFMA Operands
+// to the Desired Fragment Layout": the score fragment feeds the P x V
+// product without a trip through shared memory; "Prefetch Data"; "Address
+// LDS Bank Conflicts") and the MSLK pull request "[ROCm] Add FlyDSL
+// paged-attention decode backend (dense + fp8) with benchmark" (Kernels:
+// head-packed matrix-core decode with double-buffered loads, native fp8
+// e4m3fn KV with symmetric per-token scale, split-K partial combine).
+//
+// GB300 design. One CTA per SM (persistent) or per (sequence, kv head,
+// split). Warp 4 is the producer: it walks the block table and issues TMA
+// box copies of whole pages (K, V, and for fp8 the per-token scales) into
+// a ring of NS shared-memory stages of 64 tokens, each guarded by a pair of
+// mbarriers (full: bytes landed; empty: consumers done). Warps 0-3 consume:
+// QK^T and PV run as mma.sync m16n8k16 with fp32 accumulators; the score
+// fragment becomes the P operand in registers; K is read with ldmatrix and
+// V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). Stages
+// are dealt round-robin to NG = 4 / MT groups of MT warps (MT = m16 tiles of
+// query rows); at the end of a work item the groups merge through shared
+// memory. Every wait is bounded in time, so a protocol error cannot hang
+// the GPU.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kTS = 64;  // tokens per pipeline stage
+constexpr int kMaxHkvFp8 = 8;
+constexpr int kSmemBudget = 220 * 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kErrWaitTimeout = 1;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
+constexpr int clamp_int(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+struct SplitParams {
+  CUtensorMap tm_q;   // q       (D, Hq, T, B)          box (64, G, T, 1)
+  CUtensorMap tm_k;   // k_cache (D, Hkv, P, num_pages) box (128 B, 1, min(P,64), 1)
+  CUtensorMap tm_v;   // v_cache likewise
+  CUtensorMap tm_ks;  // k_scratch (D, Hkv, T, B)       box (64, 1, T, 1)
+  CUtensorMap tm_vs;  // v_scratch likewise
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const float* k_scale;
+  const float* v_scale;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int* err_flags;
+  int B, T, Hq, Hkv, G, M, P, max_blocks, num_pages;
+  int num_splits;  // >= 1: explicit splits (grid = units x splits); 0: balanced (grid = CTAs)
+  int tidar;       // 1: each sequence also attends to its T scratch tokens
+  int grid;        // CTAs of a balanced launch
+  float scale_log2;
+};
+
+struct ReduceParams {
+  const float* part_o;
+  const float* part_lse;
+  __nv_bfloat16* out;
+  float* lse;
+  const int32_t* context_lens;
+  int B, T, Hq, Hkv, G, M, D, P, max_blocks, tidar;
+  int num_splits;  // >= 1: explicit layout [B][T][Hq][S]; 0: balanced-launch slots
+  int grid;        // CTAs of the balanced split launch
+};
+
+// Shared-memory plan of one kernel instance.
+template <int D, int MT, bool FP8>
+struct Cfg {
+  static constexpr int ELEM = FP8 ? 1 : 2;
+  static constexpr int CE = 128 / ELEM;         // elements per 128-byte row chunk
+  static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
+  static constexpr int CHUNK = kTS * 128;       // bytes of one chunk column of a stage tile
+  static constexpr int TILE = kTS * D * ELEM;   // bytes of the K (or V) tile of a stage
+  static constexpr int SCALE = FP8 ? kTS * kMaxHkvFp8 * 4 : 0;
+  static constexpr int STAGE = round_up(2 * TILE + 2 * SCALE, 1024);
+  static constexpr int ROWS = 16 * MT;
+  static constexpr int QCH = D / 64;
+  static constexpr int QCHUNK = ROWS * 128;
+  static constexpr int QSLOT = QCH * QCHUNK;
+  static constexpr int NG = kConsumerWarps / MT;  // stage groups
+  static constexpr int RSTR = D + 8;              // floats per row of the merge buffer
+  static constexpr int RED = (NG - 1) * ROWS * RSTR * 4;
+  static constexpr int REDML = (NG - 1) * ROWS * 2 * 4;
+  static constexpr int BARS = 256;
+  static constexpr int FIXED = 2 * QSLOT + round_up(RED + REDML, 1024) + BARS;
+  static constexpr int NS = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
+  static constexpr int OFF_Q = NS * STAGE;
+  static constexpr int OFF_RED = OFF_Q + 2 * QSLOT;
+  static constexpr int OFF_REDML = OFF_RED + RED;
+  static constexpr int OFF_BAR = round_up(OFF_REDML + REDML, 1024);
+  static constexpr int OFF_PREFIX = OFF_BAR + BARS;
+  static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1024 to align the dynamic base
+  static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
+  static_assert(MT == 1 || MT == 2, "unsupported row tiles");
+};
+
+// ----------------------------------------------------------------- schedule
+struct Item {
+  int b, g;
+  int tok0, tok_end;  // paged tokens [tok0, tok_end) of sequence b
+  int scratch;        // 1: the T draft-block scratch tokens follow (last stage)
+  int nst;            // pipeline stages
+  int part;           // -1: write the final out/lse; else the partial index
+};
+
+struct Cursor {
+  long long f, f0, f1;  // balanced mode: this CTA's share of the flattened pages
+  int done;             // explicit mode: the single item was handed out
+};
+
+__device__ __forceinline__ int clamp_ctx(const SplitParams& p, int c) {
+  const int cap = p.max_blocks * p.P;
+  return c < 0 ? 0 : (c > cap ? cap : c);
+}
+
+__device__ __forceinline__ void cursor_init(const SplitParams& p, const int* s_start, Cursor& cur) {
+  cur.done = 0;
+  if (p.num_splits == 0) {
+    const long long N = (long long)p.Hkv * s_start[p.B];
+    cur.f0 = N * blockIdx.x / p.grid;
+    cur.f1 = N * (blockIdx.x + 1) / p.grid;
+    cur.f = cur.f0;
+  }
+}
+
+// The next work item of this CTA; identical on every thread that calls it.
+__device__ __forceinline__ bool next_item(const SplitParams& p, const int* s_ctx, const int* s_start,
+                                          Cursor& cur, Item& it) {
+  const int P = p.P;
+  if (p.num_splits > 0) {
+    if (cur.done) return false;
+    cur.done = 1;
+    const int S = p.num_splits;
+    const int s = blockIdx.y;
+    const int u = blockIdx.x;
+    it.b = u / p.Hkv;
+    it.g = u % p.Hkv;
+    const int ctx = clamp_ctx(p, __ldg(p.context_lens + it.b));
+    const int n = (ctx + P - 1) / P;
+    const int pps = (n + S - 1) / S;
+    const int p0 = min(n, s * pps);
+    const int p1 = min(n, p0 + pps);
+    it.tok0 = p0 * P;
+    it.tok_end = max(it.tok0, min(p1 * P, ctx));
+    it.scratch = (p.tidar && s == S - 1) ? 1 : 0;
+    it.part = S == 1 ? -1 : s;
+  } else {
+    if (cur.f >= cur.f1) return false;
+    const long long f = cur.f;
+    const int Hkv = p.Hkv;
+    int lo = 0, hi = p.B - 1;  // largest b with Hkv * start[b] <= f (a non-empty sequence)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)Hkv * s_start[mid] <= f) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int nv = s_start[b + 1] - s_start[b];
+    const long long ub = (long long)Hkv * s_start[b];
+    const int g = (int)((f - ub) / nv);
+    const long long us = ub + (long long)g * nv;
+    const long long ue = us + nv;
+    const long long end = ue < cur.f1 ? ue : cur.f1;
+    const int vp0 = (int)(f - us);
+    const int vp1 = (int)(end - us);
+    const int ctx = s_ctx[b];
+    const int n = (ctx + P - 1) / P;
+    it.b = b;
+    it.g = g;
+    it.tok0 = vp0 * P;
+    it.tok_end = max(it.tok0, min(min(vp1, n) * P, ctx));
+    it.scratch = (p.tidar && vp1 == nv) ? 1 : 0;  // the scratch is the unit's last virtual page
+    it.part = (us >= cur.f0 && ue <= cur.f1) ? -1 : (b * Hkv + g + (int)blockIdx.x);
+    cur.f = end;
+  }
+  it.nst = (it.tok_end - it.tok0 + kTS - 1) / kTS + it.scratch;
+  return true;
+}
+
+// Swizzled byte offset of 16-byte unit `unit` in row `row` of a 128-byte-row tile.
+__device__ __forceinline__ uint32_t swz(int row, int unit) {
+  return (uint32_t)(row * 128 + (((unit) ^ (row & 7)) << 4));
+}
+
+// After an abandoned wait: let the copies that may still be in flight land
+// before this CTA's shared memory can be reused (each wait is bounded too).
+template <int NS>
+__device__ __forceinline__ void drain_copies(uint32_t bar_full, uint32_t bar_qfull, int stages, int qloads) {
+  const int zero = 0;
+  const volatile int* no_abort = &zero;
+  for (int st = stages - NS > 0 ? stages - NS : 0; st < stages; ++st)
+    mbar_wait(bar_full + 8 * (st % NS), (st / NS) & 1, kWaitLimitNs, no_abort);
+  for (int q = qloads - 2 > 0 ? qloads - 2 : 0; q < qloads; ++q)
+    mbar_wait(bar_qfull + 8 * (q & 1), (q >> 1) & 1, kWaitLimitNs, no_abort);
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* s_abort, int* err_flags) {
+  *s_abort = 1;
+  atomicOr(err_flags, kErrWaitTimeout);
+}
+
+// ------------------------------------------------------------ split kernel
+template <int D, int MT, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_constant__ SplitParams p) {
+  using C = Cfg<D, MT, FP8>;
+  constexpr int NS = C::NS;
+  constexpr int NG = C::NG;
+  constexpr int NT8 = D / 8;  // n8 tiles of the output row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t bar_full = smem_u32(bars);
+  const uint32_t bar_empty = bar_full + 8 * NS;
+  const uint32_t bar_qfull = bar_full + 16 * NS;
+  const uint32_t bar_qempty = bar_qfull + 16;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 2 * NS + 4);
+  int* s_ctx = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
+  int* s_start = s_ctx + (p.num_splits == 0 ? p.B : 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, MT);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(bar_qfull + 8 * q, 1);
+      mbar_init(bar_qempty + 8 * q, kConsumerWarps);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  // Query rows past M read as zero: clear both Q slots once.
+  {
+    uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q);
+    for (int i = tid; i < 2 * C::QSLOT / 16; i += kThreads) q4[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (p.num_splits == 0) {
+    for (int i = tid; i < p.B; i += kThreads) s_ctx[i] = clamp_ctx(p, __ldg(p.context_lens + i));
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix sum of virtual pages per sequence
+      int carry = 0;
+      if (lane == 0) s_start[0] = 0;
+      for (int base = 0; base < p.B; base += 32) {
+        const int i = base + lane;
+        int v = i < p.B ? (s_ctx[i] + p.P - 1) / p.P + p.tidar : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += n;
+        }
+        if (i < p.B) s_start[i + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  const int P = p.P;
+  if (warp == kConsumerWarps) {
+    // ================================================================ producer
+    const uint64_t pol_kv = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_q);
+      prefetch_tensormap(&p.tm_k);
+      prefetch_tensormap(&p.tm_v);
+    }
+    Cursor cur;
+    cursor_init(p, s_start, cur);
+    Item it;
+    int stage = 0, qn = 0;
+    bool ok = true;
+    while (ok && next_item(p, s_ctx, s_start, cur, it)) {
+      if (it.nst == 0) continue;
+      const int qs = qn & 1;
+      if (qn >= 2) ok = mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort);
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t qdst = sbase + C::OFF_Q + qs * C::QSLOT;
+        mbar_arrive_expect_tx(bar_qfull + 8 * qs, C::QCH * p.M * 128);
+#pragma unroll
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load_4d(qdst + c * C::QCHUNK, &p.tm_q, bar_qfull + 8 * qs, c * 64, it.g * p.G, 0, it.b, pol_q);
+      }
+      ++qn;
+
+      const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
+      const int pbase = it.tok0 / P;
+      const int npages = it.tok_end > it.tok0 ? (it.tok_end - 1) / P + 1 - pbase : 0;
+      int ibase = 0;
+      int ids = lane < npages ? __ldg(bt_row + pbase + lane) : 0;
+      int ids_next = 32 + lane < npages ? __ldg(bt_row + pbase + 32 + lane) : 0;
+      for (int j = 0; j < it.nst; ++j, ++stage) {
+        const int slot = stage % NS;
+        if (stage >= NS) {
+          ok = mbar_wait(bar_empty + 8 * slot, ((stage / NS) - 1) & 1, kWaitLimitNs, s_abort);
+          if (!ok) break;
+        }
+        const uint32_t full = bar_full + 8 * slot;
+        const uint32_t kdst = sbase + slot * C::STAGE;
+        const uint32_t vdst = kdst + C::TILE;
+        const uint32_t ksd = kdst + 2 * C::TILE;
+        const uint32_t vsd = ksd + C::SCALE;
+        if (it.scratch && j == it.nst - 1) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full, 2 * C::NCH * p.T * 128);
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c) {
+              tma_load_4d(kdst + c * C::CHUNK, &p.tm_ks, full, c * C::CE, it.g, 0, it.b, pol_kv);
+              tma_load_4d(vdst + c * C::CHUNK, &p.tm_vs, full, c * C::CE, it.g, 0, it.b, pol_kv);
+            }
+          }
+          continue;
+        }
+        const int t_first = it.tok0 + j * kTS;
+        const int valid = min(kTS, it.tok_end - t_first);
+        const int pidx0 = t_first / P - pbase;  // page of the stage, relative to the item
+        while (pidx0 >= ibase + 32) {           // advance the block-table window
+          ibase += 32;
+          ids = ids_next;
+          ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
+        }
+        if (P < kTS) {
+          const int npg = (valid + P - 1) / P;
+          if (lane == 0)
+            mbar_arrive_expect_tx(full, 2 * npg * P * (C::NCH * 128 + (FP8 ? p.Hkv * 4 : 0)));
+          for (int i = 0; i < npg; ++i) {
+            const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase + i);
+            if (lane == 0) {
+#pragma unroll
+              for (int c = 0; c < C::NCH; ++c) {
+                tma_load_4d(kdst + c * C::CHUNK + i * P * 128, &p.tm_k, full, c * C::CE, it.g, 0, page, pol_kv);
+                tma_load_4d(vdst + c * C::CHUNK + i * P * 128, &p.tm_v, full, c * C::CE, it.g, 0, page, pol_kv);
+              }
+              if (FP8) {
+                const uint32_t sb = P * p.Hkv * 4;
+                const size_t off = (size_t)page * P * p.Hkv;
+                bulk_load(ksd + i * sb, p.k_scale + off, sb, full, pol_kv);
+                bulk_load(vsd + i * sb, p.v_scale + off, sb, full, pol_kv);
+              }
+            }
+          }
+        } else {
+          const int row0 = t_first % P;
+          const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full, 2 * kTS * (C::NCH * 128 + (FP8 ? p.Hkv * 4 : 0)));
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c) {
+              tma_load_4d(kdst + c * C::CHUNK, &p.tm_k, full, c * C::CE, it.g, row0, page, pol_kv);
+              tma_load_4d(vdst + c * C::CHUNK, &p.tm_v, full, c * C::CE, it.g, row0, page, pol_kv);
+            }
+            if (FP8) {
+              const uint32_t sb = kTS * p.Hkv * 4;
+              const size_t off = ((size_t)page * P + row0) * p.Hkv;
+              bulk_load(ksd, p.k_scale + off, sb, full, pol_kv);
+              bulk_load(vsd, p.v_scale + off, sb, full, pol_kv);
+            }
+          }
+        }
+      }
+    }
+    if (!ok || *s_abort) {
+      // Stop the consumers, then let the copies already issued land.
+      if (lane == 0) raise_abort(s_abort, p.err_flags);
+      drain_copies<NS>(bar_full, bar_qfull, stage, qn);
+    }
+    return;
+  }
+
+  // ================================================================ consumers
+  const int mt = warp % MT;
+  const int grp = warp / MT;
+  const int r = lane >> 2;
+  const int c4 = lane & 3;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  float* redml = reinterpret_cast<float*>(smem + C::OFF_REDML);
+
+  Cursor cur;
+  cursor_init(p, s_start, cur);
+  Item it;
+  int stage = 0, qn = 0;
+  bool ok = true;
+  float acc[NT8][4];
+
+  while (next_item(p, s_ctx, s_start, cur, it)) {
+    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+    if (it.nst > 0) {
+      const int qs = qn & 1;
+      const uint32_t qbase = sbase + C::OFF_Q + qs * C::QSLOT;
+      if (ok) {
+        ok = mbar_wait(bar_qfull + 8 * qs, (qn >> 1) & 1, kWaitLimitNs, s_abort);
+        if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
+      }
+      if (FP8) {
+        // Rewrite this item's Q rows, in place, as f16 A fragments whose k
+        // order matches the fp8 K fragments: in k-step s, thread c4 holds
+        // d = 16 s + 4 c4 .. +3. The fragments of k-steps 4q..4q+3 of row
+        // tile mt take exactly the 2 KB that the tile's rows occupy in
+        // column chunk q, so each chunk is converted by its own warp.
+        if (grp == 0) {
+          uint8_t* qs_ptr = smem + C::OFF_Q + qs * C::QSLOT;
+          uint4* dst = reinterpret_cast<uint4*>(qs_ptr);
+#pragma unroll
+          for (int q = 0; q < D / 64; ++q) {
+            uint32_t fr[4][4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int d = 16 * (4 * q + e) + 4 * c4;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {  // rows r and r + 8
+                const int row = mt * 16 + r + 8 * h;
+                uint2 v = make_uint2(0, 0);
+                if (row < p.M)
+                  v = *reinterpret_cast<const uint2*>(qs_ptr + q * C::QCHUNK + swz(row, (d % 64) / 8) + (d % 8) * 2);
+                fr[e][h] = bf16x2_to_f16x2(v.x);
+                fr[e][2 + h] = bf16x2_to_f16x2(v.y);
+              }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[(q * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane] = make_uint4(fr[e][0], fr[e][1], fr[e][2], fr[e][3]);
+            __syncwarp();
+          }
+        }
+        named_barrier_sync(1, 32 * kConsumerWarps);
+      }
+#pragma unroll
+      for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+      for (int j = grp; j < it.nst; j += NG) {
+        const int st = stage + j;
+        const int slot = st % NS;
+        if (ok) {
+          ok = mbar_wait(bar_full + 8 * slot, (st / NS) & 1, kWaitLimitNs, s_abort);
+          if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
+        }
+        if (ok) {
+          const bool scr = it.scratch && j == it.nst - 1;
+          const int valid = scr ? p.T : min(kTS, it.tok_end - (it.tok0 + j * kTS));
+          const uint32_t kb_ = sbase + slot * C::STAGE;
+          const uint32_t vb_ = kb_ + C::TILE;
+          const float* ksc = reinterpret_cast<const float*>(smem + slot * C::STAGE + 2 * C::TILE);
+          const float* vsc = ksc + C::SCALE / 4;
+
+          // ---- S = Q K^T for the 64 tokens of the stage (16 rows x 64 tokens)
+          float s[8][4];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+          if (!FP8) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              uint32_t qa[4];
+              {
+                const int row = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int d = kk * 16 + (lane >> 4) * 8;
+                ldsm_x4(qbase + (d / 64) * C::QCHUNK + swz(row, (d % 64) / 8), qa[0], qa[1], qa[2], qa[3]);
+              }
+#pragma unroll
+              for (int nb = 0; nb < 4; ++nb) {
+                const int tok = nb * 16 + (lane >> 4) * 8 + (lane & 7);
+                const int d = kk * 16 + ((lane >> 3) & 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                mma_bf16(s[2 * nb], qa, b0, b1);
+                mma_bf16(s[2 * nb + 1], qa, b2, b3);
+              }
+            }
+          } else {
+            const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
+#pragma unroll
+            for (int kq = 0; kq < D / 64; ++kq) {
+              uint32_t qa[4][4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
+                qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
+              }
+#pragma unroll
+              for (int nt = 0; nt < 8; ++nt) {
+                const int tok = nt * 8 + (lane & 7);
+                const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
+                uint32_t kr[4];
+                ldsm_x4(kb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), kr[0], kr[1], kr[2], kr[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
+              }
+            }
+          }
+
+          // ---- scale (and per-token K scale), mask, online softmax in base 2
+          const float sl = p.scale_log2;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = i * 8 + 2 * c4 + (e & 1);
+              float f = s[i][e] * sl;
+              if (FP8) f *= ksc[tok * p.Hkv + it.g];
+              s[i][e] = tok < valid ? f : NEG_INF;
+            }
+          }
+          float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[i][2], s[i][3]));
+          }
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
+          const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
+          const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+          m0 = mn0;
+          m1 = mn1;
+          float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            s[i][0] = ex2(s[i][0] - mu0);
+            s[i][1] = ex2(s[i][1] - mu0);
+            s[i][2] = ex2(s[i][2] - mu1);
+            s[i][3] = ex2(s[i][3] - mu1);
+            ls0 += s[i][0] + s[i][1];
+            ls1 += s[i][2] + s[i][3];
+          }
+          l0 = l0 * al0 + ls0;
+          l1 = l1 * al1 + ls1;
+#pragma unroll
+          for (int i = 0; i < NT8; ++i) {
+            acc[i][0] *= al0;
+            acc[i][1] *= al0;
+            acc[i][2] *= al1;
+            acc[i][3] *= al1;
+          }
+
+          // ---- O += P V: the score fragments are the A operand as they are
+          const bool partial = valid < kTS;
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            const int t0 = kb * 16 + 2 * c4;  // tokens of the lo fragment; +8 for the hi one
+            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+            if (partial) {
+              vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+              vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+            }
+            uint32_t pa[4];
+            if (!FP8) {
+              pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
+              pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
+              pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
+              pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
+#pragma unroll
+              for (int nd = 0; nd < D / 16; ++nd) {
+                const int tok = kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int d = nd * 16 + (lane >> 4) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                if (partial) {
+                  b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
+                }
+                mma_bf16(acc[2 * nd], pa, b0, b1);
+                mma_bf16(acc[2 * nd + 1], pa, b2, b3);
+              }
+            } else {
+              // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
+              float vs[4];
+              vs[0] = t0 < valid ? vsc[t0 * p.Hkv + it.g] : 0.f;
+              vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + it.g] : 0.f;
+              vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + it.g] : 0.f;
+              vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + it.g] : 0.f;
+              pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
+              pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
+              pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
+              pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
+#pragma unroll
+              for (int uu = 0; uu < D / 32; ++uu) {
+                const int tok = kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int unit = 2 * uu + (lane >> 4);
+                uint32_t R[4];
+                ldsm_x4_trans(vb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), R[0], R[1], R[2], R[3]);
+                if (partial) {
+                  R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  // bytes (tok 2c d 2r, tok 2c d 2r+1, tok 2c+1 d 2r, tok 2c+1 d 2r+1)
+                  const uint32_t x = prmt(R[2 * k], 0, 0x3120);
+                  const uint32_t y = prmt(R[2 * k + 1], 0, 0x3120);
+                  const int nt = 2 * (2 * uu + k);
+                  mma_f16(acc[nt], pa, e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(y));
+                  mma_f16(acc[nt + 1], pa, e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y >> 16));
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+      }
+      stage += it.nst;
+      if (FP8) fence_proxy_async_smem();  // the slot was rewritten through the generic proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qempty + 8 * qs);
+      ++qn;
+    } else {
+#pragma unroll
+      for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    }
+
+    // ---- merge the NG groups' partial results, then write
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int rho0 = mt * 16 + r, rho1 = rho0 + 8;
+    if (NG > 1) {
+      named_barrier_sync(1, 32 * kConsumerWarps);
+      if (grp > 0) {
+        float* rb = red + (size_t)(grp - 1) * C::ROWS * C::RSTR;
+#pragma unroll
+        for (int i = 0; i < NT8; ++i) {
+          *reinterpret_cast<float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][0], acc[i][1]);
+          *reinterpret_cast<float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][2], acc[i][3]);
+        }
+        if (c4 == 0) {
+          float* ml = redml + (size_t)(grp - 1) * C::ROWS * 2;
+          ml[2 * rho0] = m0;
+          ml[2 * rho0 + 1] = l0;
+          ml[2 * rho1] = m1;
+          ml[2 * rho1 + 1] = l1;
+        }
+      }
+      named_barrier_sync(1, 32 * kConsumerWarps);
+    }
+    if (grp != 0) continue;
+
+    float M0 = m0, M1 = m1;
+#pragma unroll
+    for (int q = 0; q < NG - 1; ++q) {
+      M0 = fmaxf(M0, redml[(q * C::ROWS + rho0) * 2]);
+      M1 = fmaxf(M1, redml[(q * C::ROWS + rho1) * 2]);
+    }
+    const float Mu0 = M0 == NEG_INF ? 0.f : M0;
+    const float Mu1 = M1 == NEG_INF ? 0.f : M1;
+    const float w00 = ex2(m0 - Mu0), w01 = ex2(m1 - Mu1);
+    float L0 = w00 * l0, L1 = w01 * l1;
+    float wq0[NG > 1 ? NG - 1 : 1], wq1[NG > 1 ? NG - 1 : 1];
+#pragma unroll
+    for (int q = 0; q < NG - 1; ++q) {
+      wq0[q] = ex2(redml[(q * C::ROWS + rho0) * 2] - Mu0);
+      wq1[q] = ex2(redml[(q * C::ROWS + rho1) * 2] - Mu1);
+      L0 += wq0[q] * redml[(q * C::ROWS + rho0) * 2 + 1];
+      L1 += wq1[q] * redml[(q * C::ROWS + rho1) * 2 + 1];
+    }
+    const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
+    const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+#pragma unroll
+    for (int i = 0; i < NT8; ++i) {
+      float a0 = acc[i][0] * w00, a1 = acc[i][1] * w00, a2 = acc[i][2] * w01, a3 = acc[i][3] * w01;
+#pragma unroll
+      for (int q = 0; q < NG - 1; ++q) {
+        const float* rb = red + (size_t)q * C::ROWS * C::RSTR;
+        const float2 x = *reinterpret_cast<const float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4);
+        const float2 y = *reinterpret_cast<const float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4);
+        a0 += wq0[q] * x.x;
+        a1 += wq0[q] * x.y;
+        a2 += wq1[q] * y.x;
+        a3 += wq1[q] * y.y;
+      }
+      acc[i][0] = a0 * inv0;
+      acc[i][1] = a1 * inv0;
+      acc[i][2] = a2 * inv1;
+      acc[i][3] = a3 * inv1;
+    }
+    const float lse0 = L0 > 0.f ? (M0 + lg2(L0)) * kLn2 : NEG_INF;
+    const float lse1 = L1 > 0.f ? (M1 + lg2(L1)) * kLn2 : NEG_INF;
+
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int rho = h2 ? rho1 : rho0;
+      if (rho >= p.M) continue;
+      const int t = rho / p.G;
+      const int h = it.g * p.G + rho % p.G;
+      const size_t row = ((size_t)it.b * p.T + t) * p.Hq + h;
+      const float lsev = h2 ? lse1 : lse0;
+      if (it.part < 0) {
+        __nv_bfloat16* o = p.out + row * D;
+        if (!FP8) {
+#pragma unroll
+          for (int i = 0; i < NT8; ++i)
+            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * c4) = pack_bf16x2(acc[i][2 * h2], acc[i][2 * h2 + 1]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < D / 16; ++u)
+            *reinterpret_cast<uint2*>(o + 16 * u + 4 * c4) =
+                make_uint2(pack_bf16x2(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2]),
+                           pack_bf16x2(acc[2 * u][2 * h2 + 1], acc[2 * u + 1][2 * h2 + 1]));
+        }
+        if (c4 == 0 && p.lse) p.lse[row] = lsev;
+      } else {
+        const size_t prow = p.num_splits > 0 ? row * p.num_splits + it.part : (size_t)it.part * p.M + rho;
+        float* o = p.part_o + prow * D;
+        if (!FP8) {
+#pragma unroll
+          for (int i = 0; i < NT8; ++i)
+            *reinterpret_cast<float2*>(o + i * 8 + 2 * c4) = make_float2(acc[i][2 * h2], acc[i][2 * h2 + 1]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < D / 16; ++u)
+            *reinterpret_cast<float4*>(o + 16 * u + 4 * c4) =
+                make_float4(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2], acc[2 * u][2 * h2 + 1],
+                            acc[2 * u + 1][2 * h2 + 1]);
+        }
+        if (c4 == 0) p.part_lse[prow] = lsev;
+      }
+    }
+  }
+  if (warp == 0 && *s_abort) drain_copies<NS>(bar_full, bar_qfull, stage, qn);
+}
+
+}  // namespace pa

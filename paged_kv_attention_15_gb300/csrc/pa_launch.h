@@ -1,0 +1,20 @@
+// Internal interface between the C-ABI host code and the kernel instances.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "pa_kernels.cuh"
+
+namespace pa {
+
+struct SplitKernel {
+  const void* fn;   // __global__ function, launched with cudaLaunchKernel
+  int smem_fixed;   // dynamic shared memory without the per-sequence table
+  int stages;       // pipeline depth of the instance
+};
+
+// Kernel instance for (head_dim, row tiles, fp8); fn == nullptr if not built.
+SplitKernel split_kernel_bf16(int head_dim, int row_tiles);
+SplitKernel split_kernel_fp8(int head_dim, int row_tiles);
+
+}  // namespace pa

@@ -1,0 +1,112 @@
+"""The C-ABI library: it builds, loads, exports every function the header
+declares, and rejects bad arguments before touching the GPU."""
+
+import ctypes
+import os
+
+import pytest
+
+from paged_kv_attention_15_gb300 import binding as pb
+from paged_kv_attention_15_gb300 import build as pbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(pb.LIB_PATH):
+        pbuild.build()
+    return pb.lib()
+
+
+def shape(**kw):
+    base = dict(batch=2, q_tokens=1, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                num_pages=64, max_blocks_per_seq=8)
+    base.update(kw)
+    return pb.PaShape(*[base[f] for f, _ in pb.PaShape._fields_])
+
+
+FAKE = 1 << 20  # an aligned, never dereferenced address
+
+
+def call_decode(lib, s, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, scale=0.1, out=FAKE, lse=None, splits=1, ws=None, wsb=0)
+    a.update(kw)
+    return lib.pa_decode(a["q"], a["k"], a["v"], a["bt"], a["cl"], ctypes.byref(s), a["scale"], a["out"],
+                         a["lse"], a["splits"], a["ws"], a["wsb"], None)
+
+
+def test_exports_every_declared_function(lib):
+    names = pb.header_functions()
+    assert {"pa_decode", "pa_decode_fp8", "pa_decode_reduce", "pa_decode_tidar"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pb._SIGNATURES) == set(names)
+
+
+def test_status_strings(lib):
+    for st in range(5):
+        assert pb.status_string(st)
+    assert pb.status_string(99) == "unknown status"
+
+
+def test_shape_validation_before_any_launch(lib):
+    assert call_decode(lib, shape(num_q_heads=6, num_kv_heads=4)) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, shape(head_dim=96)) == pb.PA_ERR_UNSUPPORTED
+    assert call_decode(lib, shape(page_size=8)) == pb.PA_ERR_UNSUPPORTED
+    assert call_decode(lib, shape(page_size=48)) == pb.PA_ERR_UNSUPPORTED
+    assert call_decode(lib, shape(num_q_heads=64, num_kv_heads=1)) == pb.PA_ERR_UNSUPPORTED  # 64 rows
+    assert call_decode(lib, shape(q_tokens=0)) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, shape(num_pages=0)) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, shape(batch=-1)) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, shape(max_blocks_per_seq=1 << 28, page_size=256)) == pb.PA_ERR_INVALID_ARG
+    assert lib.pa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, None, 0.1, FAKE, None, 1, None, 0, None) == pb.PA_ERR_INVALID_ARG
+
+
+def test_pointer_and_argument_validation(lib):
+    s = shape()
+    assert call_decode(lib, s, q=None) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, s, out=None) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, s, k=FAKE + 8) == pb.PA_ERR_INVALID_ARG  # not 16-byte aligned
+    assert call_decode(lib, s, scale=float("nan")) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, s, scale=float("inf")) == pb.PA_ERR_INVALID_ARG
+    assert call_decode(lib, s, splits=-1) == pb.PA_ERR_INVALID_ARG
+    # Nothing to do: OK without touching the device.
+    assert call_decode(lib, shape(batch=0)) == pb.PA_OK
+
+
+def test_fp8_and_tidar_validation(lib):
+    s = shape()
+    assert lib.pa_decode_fp8(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, None, 1,
+                             None, 0, None) == pb.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(shape(head_dim=64)), 0.1,
+                             FAKE, None, 1, None, 0, None) == pb.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             ctypes.byref(shape(num_q_heads=16, num_kv_heads=16)), 0.1, FAKE, None, 1, None, 0,
+                             None) == pb.PA_ERR_UNSUPPORTED  # > 8 kv heads
+    assert lib.pa_decode_tidar(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, None, 1,
+                               None, 0, None) == pb.PA_ERR_INVALID_ARG
+
+
+def test_reduce_validation(lib):
+    s = shape()
+    assert lib.pa_decode_reduce(None, FAKE, 3, ctypes.byref(s), FAKE, None, None) == pb.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_reduce(FAKE, FAKE, 0, ctypes.byref(s), FAKE, None, None) == pb.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_reduce(FAKE, FAKE, 3, ctypes.byref(shape(head_dim=6)), FAKE, None,
+                                None) == pb.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_reduce(FAKE, FAKE, 3, ctypes.byref(shape(batch=0)), FAKE, None, None) == pb.PA_OK
+
+
+def test_explicit_split_workspace_size(lib):
+    s = shape(batch=3, q_tokens=2, num_q_heads=8, head_dim=64)
+    assert lib.pa_decode_workspace_size(ctypes.byref(s), 1) == 0
+    rows = 3 * 2 * 8 * 5
+    expect = (rows * 64 * 4 + 255) // 256 * 256 + (rows * 4 + 255) // 256 * 256
+    assert lib.pa_decode_workspace_size(ctypes.byref(s), 5) == expect
+    assert lib.pa_decode_workspace_size(ctypes.byref(shape(head_dim=96)), 5) == 0
+    assert lib.pa_decode_workspace_size(ctypes.byref(s), -2) == 0
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(pb, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(pb, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        pb.lib()

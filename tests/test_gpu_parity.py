@@ -1,0 +1,264 @@
+"""GPU path (through the C ABI) against the fp64 oracle.
+
+Bar: |gpu - oracle| <= tol + tol * |oracle| elementwise on out, with
+tol = 1e-2 for bf16 KV and 2e-2 for fp8 KV, and |lse_gpu - lse_oracle| <= 1e-3
+(lse = -inf exactly where the oracle's is). Inputs are the seeded synthetic
+workloads; the full-size ones are checked on sampled rows the oracle
+computes one by one, in the launch configuration the benchmark times
+(num_splits = 0).
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_15_gb300 import binding as pb
+from paged_kv_attention_15_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+LSE_TOL = 1e-3
+
+
+def tol_of(spec):
+    return 2e-2 if spec.kv_format == "fp8" else 1e-2
+
+
+def ora_inputs(inp):
+    return oracle.as_oracle_inputs(inp.numpy_bits(), inp.spec.kv_format)
+
+
+def gpu_decode(inp, num_splits=0, dev=None, **kw):
+    dev = dev if dev is not None else inp.to("cuda")
+    out, lse = pb.decode_inputs(dev, num_splits=num_splits, **kw)
+    torch.cuda.synchronize()
+    assert pb.device_error() == 0
+    return out, lse
+
+
+def to_np(out, lse):
+    return out.float().cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+def assert_match(out, lse, ref_out, ref_lse, tol, rows=None):
+    if rows is not None:
+        idx = tuple(np.array(rows).T)
+        out, lse, ref_out, ref_lse = out[idx], lse[idx], ref_out[idx], ref_lse[idx]
+    assert np.all(np.isfinite(out)), "non-finite output"
+    excess = np.abs(out - ref_out) - (tol + tol * np.abs(ref_out))
+    assert excess.max() <= 0, f"out mismatch: max excess {excess.max():.3g}, max abs err {np.abs(out - ref_out).max():.3g}"
+    inf = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), inf), "lse -inf pattern differs"
+    d = np.abs(lse[~inf] - ref_lse[~inf])
+    assert d.size == 0 or d.max() <= LSE_TOL, f"lse mismatch: {d.max():.3g}"
+
+
+def check_full(inp, num_splits):
+    ref_out, ref_lse = oracle.decode(ora_inputs(inp), inp.scale)
+    out, lse = to_np(*gpu_decode(inp, num_splits))
+    assert_match(out, lse, ref_out, ref_lse, tol_of(inp.spec))
+
+
+# --------------------------------------------------------------------- tiny
+@pytest.mark.parametrize("num_splits", [1, 3, 0])
+def test_tiny_workload(num_splits):
+    check_full(gen.make_inputs(gen.SPECS["tiny"]), num_splits)
+
+
+# ------------------------------------------------------------ shape sweeps
+def spec(**kw):
+    base = dict(batch=4, q_tokens=1, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                context_lens=(1, 100, 16, 333), seed=21)
+    base.update(kw)
+    return gen.custom_spec(**base)
+
+
+SWEEP = [
+    dict(),
+    dict(head_dim=64),
+    dict(head_dim=256),
+    dict(page_size=32),
+    dict(page_size=64, context_lens=(64, 65, 200, 1)),
+    dict(page_size=128, context_lens=(300, 127, 128, 129)),
+    dict(page_size=256, context_lens=(600, 255, 1, 257)),
+    dict(num_q_heads=16, num_kv_heads=1),                       # G 16: one full row tile
+    dict(num_q_heads=32, num_kv_heads=1, head_dim=64),          # G 32: two row tiles
+    dict(num_q_heads=4, num_kv_heads=4),                        # MHA
+    dict(q_tokens=4, num_q_heads=8, num_kv_heads=2),            # 16 rows
+    dict(q_tokens=3, num_q_heads=10, num_kv_heads=2),           # 15 rows, odd group
+    dict(context_lens=(0, 37, 0, 500)),                         # empty sequences
+    dict(batch=9, ctx_range=(1, 700), context_lens=None, pool_pages=400),
+]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=[str(i) for i in range(len(SWEEP))])
+@pytest.mark.parametrize("num_splits", [0, 1, 3, 17])
+def test_bf16_sweep(case, num_splits):
+    check_full(gen.make_inputs(spec(**case)), num_splits)
+
+
+FP8_SWEEP = [
+    dict(kv_format="fp8"),
+    dict(kv_format="fp8", head_dim=256, num_q_heads=16, num_kv_heads=1),
+    dict(kv_format="fp8", head_dim=256, num_q_heads=32, num_kv_heads=2, page_size=64, context_lens=(64, 1, 700, 65)),
+    dict(kv_format="fp8", num_q_heads=24, num_kv_heads=1),       # two row tiles
+    dict(kv_format="fp8", num_q_heads=16, num_kv_heads=8, context_lens=(0, 5, 900, 31)),
+]
+
+
+@pytest.mark.parametrize("case", FP8_SWEEP, ids=[str(i) for i in range(len(FP8_SWEEP))])
+@pytest.mark.parametrize("num_splits", [0, 1, 4])
+def test_fp8_sweep(case, num_splits):
+    check_full(gen.make_inputs(spec(**case)), num_splits)
+
+
+TIDAR_SWEEP = [
+    dict(draft_scratch=True, q_tokens=8, num_q_heads=8, num_kv_heads=2),
+    dict(draft_scratch=True, q_tokens=4, num_q_heads=4, num_kv_heads=1, context_lens=(0, 16, 17, 250)),
+    dict(draft_scratch=True, q_tokens=2, num_q_heads=16, num_kv_heads=2, head_dim=64, page_size=64,
+         context_lens=(63, 64, 1, 400)),
+]
+
+
+@pytest.mark.parametrize("case", TIDAR_SWEEP, ids=[str(i) for i in range(len(TIDAR_SWEEP))])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_tidar_sweep(case, num_splits):
+    check_full(gen.make_inputs(spec(**case)), num_splits)
+
+
+# --------------------------------------------------------------- robustness
+@pytest.mark.parametrize("kv_format", ["bf16", "fp8"])
+@pytest.mark.parametrize("num_splits", [0, 2])
+def test_unread_values_are_never_read(kv_format, num_splits):
+    """NaN in unused pages, in slots past the context end and in their fp8
+    scales, and INT32_MAX in unused block-table entries change nothing."""
+    s = spec(kv_format=kv_format, context_lens=(5, 100, 33, 250), pool_pages=60)
+    clean = gen.make_inputs(s)
+    dirty = gen.make_inputs(s, poison=True)
+    a = gpu_decode(clean, num_splits)
+    b = gpu_decode(dirty, num_splits)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    check_full(dirty, num_splits)
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_page_relabelling_is_bit_exact(num_splits):
+    inp = gen.make_inputs(spec(pool_pages=80, context_lens=(300, 7, 129, 64)))
+    perm = torch.randperm(80, generator=torch.Generator().manual_seed(5))
+    moved = dataclasses.replace(inp)
+    moved.k_cache = torch.empty_like(inp.k_cache)
+    moved.v_cache = torch.empty_like(inp.v_cache)
+    moved.k_cache[perm] = inp.k_cache
+    moved.v_cache[perm] = inp.v_cache
+    bt = inp.block_tables.clone()
+    valid = bt >= 0
+    bt[valid] = perm[bt[valid].long()].to(torch.int32)
+    moved.block_tables = bt
+    a = gpu_decode(inp, num_splits)
+    b = gpu_decode(moved, num_splits)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("S", [2, 5, 40])
+def test_explicit_split_partials_match_oracle(S):
+    """The per-split partials (an intermediate the pages suggest checking:
+    the log-sum-exp) against the oracle's split variant."""
+    inp = gen.make_inputs(spec(context_lens=(1, 100, 16, 333)))
+    dev = inp.to("cuda")
+    shp = pb.make_shape(dev.q, dev.k_cache, dev.block_tables)
+    ws = torch.zeros(pb.workspace_size(shp, S), dtype=torch.uint8, device="cuda")
+    gpu_decode(inp, S, dev=dev, workspace=ws)
+    B, T, Hq, D = inp.q.shape
+    po, pl = pb.split_workspace_views(ws, B, T, Hq, S, D)
+    ref_po, ref_pl = oracle.decode_split(ora_inputs(inp), inp.scale, S)
+    pl = pl.double().cpu().numpy()
+    po = po.double().cpu().numpy()
+    inf = np.isneginf(ref_pl)
+    assert np.array_equal(np.isneginf(pl), inf)
+    assert np.abs(pl[~inf] - ref_pl[~inf]).max() <= LSE_TOL
+    fin = ~inf
+    assert np.abs(po[fin] - ref_po[fin]).max() <= 1e-2 * (1 + np.abs(ref_po[fin]).max())
+
+
+def test_reduce_entry_point_against_oracle_combine():
+    rng = np.random.default_rng(9)
+    B, T, Hq, S, D = 3, 2, 4, 7, 128
+    po = rng.standard_normal((B, T, Hq, S, D)).astype(np.float32)
+    pl = (rng.standard_normal((B, T, Hq, S)) * 3).astype(np.float32)
+    pl[0, 0, 0, :] = -np.inf          # all splits empty
+    pl[1, 1, 2, ::2] = -np.inf        # some empty
+    ref_o, ref_l = oracle.combine(po.astype(np.float64), pl.astype(np.float64))
+    out, lse = pb.decode_reduce(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda())
+    torch.cuda.synchronize()
+    o, l = to_np(out, lse)
+    assert_match(o, l, ref_o, ref_l, 1e-2)
+
+
+def test_split_counts_beyond_pages_and_single_page():
+    inp = gen.make_inputs(spec(context_lens=(16, 1, 17, 40)))
+    for S in (1, 2, 3, 4, 9, 100):
+        check_full(inp, S)
+
+
+# ----------------------------------------------------- full-size workloads
+def sample_rows(inp, n, seed):
+    s = inp.spec
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0, 0), (s.batch - 1, s.q_tokens - 1, s.num_q_heads - 1)}
+    # every query token of one whole kv-head group
+    b = int(rng.integers(s.batch))
+    g = int(rng.integers(s.num_kv_heads))
+    for t in range(s.q_tokens):
+        for h in range(g * s.group, (g + 1) * s.group):
+            rows.add((b, t, h))
+    while len(rows) < n:
+        rows.add((int(rng.integers(s.batch)), int(rng.integers(s.q_tokens)), int(rng.integers(s.num_q_heads))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["gqa", "long", "fp8", "tidar"])
+def test_full_size_workload_sampled(name):
+    inp = gen.make_inputs(gen.SPECS[name])
+    out, lse = gpu_decode(inp, 0)
+    out_np, lse_np = to_np(out, lse)
+    assert np.all(np.isfinite(out_np)) and np.all(np.isfinite(lse_np))
+    rows = sample_rows(inp, 48, seed=len(name))
+    ref_out, ref_lse = oracle.decode(ora_inputs(inp), inp.scale, rows=rows)
+    assert_match(out_np, lse_np, ref_out, ref_lse, tol_of(inp.spec), rows=rows)
+    # Explicit splits agree with the balanced launch at full size as well.
+    out2, lse2 = to_np(*gpu_decode(inp, 7))
+    assert np.abs(lse2 - lse_np).max() <= LSE_TOL
+    assert np.abs(out2 - out_np).max() <= 2 * tol_of(inp.spec)
+
+
+# ------------------------------------------------------------ graph capture
+def test_graph_capture_replays_like_eager():
+    """Captured into a CUDA graph, then inputs rewritten in place and the
+    graph replayed: identical bits to an eager call on the new inputs."""
+    common = dict(batch=6, ctx_range=(1, 900), context_lens=None, pool_pages=500, max_blocks_per_seq=57)
+    inp = gen.make_inputs(spec(**common))
+    other = gen.make_inputs(spec(**common, seed=99))
+    dev = inp.to("cuda")
+    shp = pb.make_shape(dev.q, dev.k_cache, dev.block_tables)
+    ws = torch.empty(pb.workspace_size(shp, 0), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev.q)
+    lse = torch.empty(dev.q.shape[:3], dtype=torch.float32, device="cuda")
+    pb.decode_inputs(dev, out=out, lse=lse, workspace=ws)  # first call outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            pb.decode_inputs(dev, out=out, lse=lse, workspace=ws)
+    for name, t in other.tensors().items():
+        getattr(dev, name).copy_(t)
+    g.replay()
+    torch.cuda.synchronize()
+    got = (out.clone(), lse.clone())
+    eager = gpu_decode(other, 0)
+    assert torch.equal(got[0], eager[0]) and torch.equal(got[1], eager[1])
+    ref_out, ref_lse = oracle.decode(ora_inputs(other), other.scale)
+    assert_match(*to_np(*got), ref_out, ref_lse, 1e-2)
