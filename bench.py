@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 paged-KV decode engine.
+
+One step = one decode call (split kernel + split-K reduce) over the whole
+batch of the workload, inputs resident in HBM. Two device copies of the
+inputs are alternated so that no step finds its KV in the 129 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gqa|long|fp8|tidar]
+                    [--impl ours|reference]
+
+Prints one JSON line on rank 0. `value` is the achieved algorithmic HBM
+bandwidth in GB/s (bytes a decode must move, see algorithmic_bytes, over
+the device time of a call), summed over ranks; `ms_per_step` is the time
+of one call. `--impl reference` times the fp64 CPU oracle on host cores on
+a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_kv_attention_15_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "paged decode µs/call and achieved HBM GB/s (fraction of 8 TB/s) on 1 GB300"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_CONFIG = "gqa"
+
+WORKLOADS = {
+    "tiny": "tiny paged decode: B2 T1 Hq4 Hkv1 D64 P16 ctx {37,100} bf16",
+    "gqa": "GQA decode: B32 T1 Hq32 Hkv8 D128 P16 ctx U[512,8192] bf16",
+    "long": "long-context split-K decode: B4 T1 Hq64 Hkv8 D128 P64 ctx 131072 bf16",
+    "fp8": "native fp8 KV decode: B64 T1 Hq32 Hkv2 D256 P16 ctx U[1024,16384] e4m3fn KV + fp32 per-token scale",
+    "tidar": "TiDAR draft-block decode: B16 T8 Hq32 Hkv8 D128 P16 ctx U[2048,8192] + scratch KV [16,8,8,128] bf16",
+}
+SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# --------------------------------------------------------------------------- bytes
+def algorithmic_bytes(inp) -> int:
+    """Bytes a decode call must move at minimum: KV rows of the valid tokens,
+    their fp8 scales, the block-table entries in use, q, out, lse,
+    context_lens and the draft-block scratch. Split-K partials excluded."""
+    s = inp.spec
+    lens = inp.context_lens.to(torch.int64)
+    tokens = int(lens.sum())
+    pages = int(((lens + s.page_size - 1) // s.page_size).sum())
+    kv_elem = 1 if s.kv_format == "fp8" else 2
+    nbytes = 2 * tokens * s.num_kv_heads * s.head_dim * kv_elem
+    if s.kv_format == "fp8":
+        nbytes += 2 * tokens * s.num_kv_heads * 4
+    nbytes += pages * 4
+    rows = s.batch * s.q_tokens * s.num_q_heads
+    nbytes += rows * s.head_dim * 2 * 2 + rows * 4 + s.batch * 4
+    if s.draft_scratch:
+        nbytes += 2 * s.batch * s.q_tokens * s.num_kv_heads * s.head_dim * 2
+    return nbytes
+
+
+def unit_bytes(spec, ctx: int) -> int:
+    """Algorithmic bytes of one (sequence, kv head) unit with ctx keys."""
+    kv_elem = 1 if spec.kv_format == "fp8" else 2
+    n = 2 * ctx * spec.head_dim * kv_elem + (2 * ctx * 4 if spec.kv_format == "fp8" else 0)
+    rows = spec.group * spec.q_tokens
+    n += rows * spec.head_dim * 2 * 2 + rows * 4 + ((ctx + spec.page_size - 1) // spec.page_size) * 4
+    if spec.draft_scratch:
+        n += 2 * spec.q_tokens * spec.head_dim * 2
+    return n
+
+
+# --------------------------------------------------------------------------- peaks
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "of measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for name in SPLIT_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_attention_15_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(config: str):
+    """DRAM bytes per split-kernel launch from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(config)
+        if rec and rec.get("kernel_sha") == kernel_sha():
+            return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------- clocks
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+            0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read only)
+    every few milliseconds on a background thread."""
+
+    def __init__(self, device_index: int = 0, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(handle)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.nvml, self.handle = nv, handle
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._reasons_fn = fn
+        except Exception:
+            self.nvml = None
+
+    def _run(self):
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(int(mhz.value))
+            if self._reasons_fn(self.handle, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(self.period)
+
+    def start(self):
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self):
+        if self.nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        names = [n for bit, n in _REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------- ranks
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_throughput(bytes_per_step: int, steps: int, max_elapsed_s: float, world: int) -> float:
+    """Whole-job GB/s: every rank ran `steps` steps of `bytes_per_step`."""
+    return world * bytes_per_step * steps / max_elapsed_s / 1e9
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_sample_run(inp, budget_s: float, start_unit: int = 0):
+    """Runs the oracle, as it stands, on whole (sequence, kv head) units (a
+    context prefix for the first unit when one unit alone exceeds the
+    budget). Returns (seconds, algorithmic bytes, description)."""
+    import oracle
+
+    spec = inp.spec
+    bits = oracle.as_oracle_inputs(inp.numpy_bits(), spec.kv_format)
+    ctx = bits["context_lens"].astype(np.int64)
+    units = [(b, g) for b in range(spec.batch) for g in range(spec.num_kv_heads)]
+    rows_of = lambda b, g: [(b, t, h) for t in range(spec.q_tokens)
+                            for h in range(g * spec.group, (g + 1) * spec.group)]
+    # calibrate on a prefix of the first unit
+    b0, g0 = units[start_unit % len(units)]
+    probe = min(int(ctx[b0]), 4096)
+    trial = dict(bits)
+    trial["context_lens"] = bits["context_lens"].copy()
+    trial["context_lens"][b0] = probe
+    t = time.perf_counter()
+    oracle.decode(trial, spec.scale, rows=rows_of(b0, g0))
+    per_token = max((time.perf_counter() - t) / max(probe, 1), 1e-9)
+    done_s, done_bytes, n_units, prefix = 0.0, 0, 0, None
+    i = start_unit
+    while done_s < budget_s and n_units < len(units):
+        b, g = units[i % len(units)]
+        c = int(ctx[b])
+        run = dict(bits)
+        if per_token * c > budget_s - done_s and n_units == 0:
+            c = max(1, int((budget_s - done_s) / per_token))
+            run["context_lens"] = bits["context_lens"].copy()
+            run["context_lens"][b] = c
+            prefix = c
+        elif per_token * c > 2 * (budget_s - done_s) and n_units > 0:
+            break
+        t = time.perf_counter()
+        oracle.decode(run, spec.scale, rows=rows_of(b, g))
+        done_s += time.perf_counter() - t
+        done_bytes += unit_bytes(spec, c)
+        n_units += 1
+        i += 1
+    desc = f"{n_units} (sequence, kv head) unit(s) of the {spec.name} workload"
+    if prefix is not None:
+        desc += f", the first one cut to its first {prefix} keys"
+    return done_s, done_bytes, desc
+
+
+# --------------------------------------------------------------------------- arms
+def run_ours(args, world, rank, local):
+    from paged_kv_attention_15_gb300 import binding as pb
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = gen.SPECS[args.config]
+    host = gen.make_inputs(spec)
+    pb.lib()
+    sets = [host.to(dev), host.to(dev)]  # alternated: each step reads KV not in L2
+    shape = pb.make_shape(sets[0].q, sets[0].k_cache, sets[0].block_tables)
+    ws_bytes = pb.workspace_size(shape, args.num_splits)
+    wss = [torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) for _ in sets]
+    outs = [torch.empty_like(s.q) for s in sets]
+    lses = [torch.empty(s.q.shape[:3], dtype=torch.float32, device=dev) for s in sets]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i & 1
+        pb.decode_inputs(sets[j], out=outs[j], lse=lses[j], workspace=wss[j], num_splits=args.num_splits,
+                         stream=stream)
+
+    nbytes = algorithmic_bytes(host)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert pb.device_error() == 0
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0.record(stream)
+    for i in range(args.steps):
+        pb.arm_profile_events(ev[i][0], ev[i][1])
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    split_ms = [a.elapsed_time(b) for a, b in ev]
+    assert pb.device_error() == 0
+
+    max_ms = max_over_ranks(elapsed_ms, world, dev)
+    ms_per_step = max_ms / args.steps
+    value = aggregate_throughput(nbytes, args.steps, max_ms / 1e3, world)
+    split_mean_ms = sum(split_ms) / len(split_ms)
+    peak, peak_src = load_peak()
+    achieved = nbytes / (split_mean_ms / 1e3) / 1e9
+
+    # Graph replay of the same calls, for reference (launch overhead removed).
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(dev)
+        with torch.cuda.stream(s2):
+            with torch.cuda.graph(g, stream=s2):
+                for i in range(2):
+                    pb.decode_inputs(sets[i], out=outs[i], lse=lses[i], workspace=wss[i],
+                                     num_splits=args.num_splits)
+        reps = max(3, min(200, args.steps // 2))
+        g.replay()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s2)
+        for _ in range(reps):
+            g.replay()
+        b.record(s2)
+        torch.cuda.synchronize(dev)
+        graph_us = a.elapsed_time(b) * 1e3 / (2 * reps)
+    except Exception as e:  # reported, not fatal
+        graph_us = f"graph capture failed: {e}"
+
+    e2e = run_e2e(args, host, dev, pb, nbytes, world)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8" if spec.kv_format == "fp8" else "bf16", "data": "synthetic",
+        "config": {
+            "workload": WORKLOADS[args.config], "batch": spec.batch, "q_tokens": spec.q_tokens,
+            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+            "page_size": spec.page_size, "num_splits": args.num_splits, "seed": spec.seed,
+            "algorithmic_bytes_per_step": nbytes,
+            "l2": f"inputs larger than L2: two device copies of {nbytes / 1e6:.0f} MB alternated",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "us_per_call": ms_per_step * 1e3,
+        "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
+        "kernels_us": {"split": split_mean_ms * 1e3, "reduce_and_gaps": (ms_per_step - split_mean_ms) * 1e3,
+                       "graph_replay_per_call": graph_us},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": load_traffic(args.config), "peak_source": peak_src,
+                     "kernel": "pa_split_kernel"},
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps if (args.num_splits != 1) else args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, b, desc = oracle_sample_run(host, args.cpu_budget)
+        result["cpu_baseline"] = {"value": b / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": desc, "seconds": secs}
+    return result
+
+
+def run_e2e(args, host, dev, pb, nbytes, world):
+    """Same metric through the public call with host buffers: every step
+    copies its inputs from pinned host memory and reads out + lse back."""
+    pinned = host.pin_memory()
+    devset = host.to(dev)
+    shape = pb.make_shape(devset.q, devset.k_cache, devset.block_tables)
+    ws = torch.empty(max(pb.workspace_size(shape, args.num_splits), 1), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(devset.q)
+    lse = torch.empty(devset.q.shape[:3], dtype=torch.float32, device=dev)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.tensors().values())
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for name, t in pinned.tensors().items():
+            getattr(devset, name).copy_(t, non_blocking=True)
+        pb.decode_inputs(devset, out=out, lse=lse, workspace=ws, num_splits=args.num_splits, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize(dev)
+    k = max(1, min(args.steps, args.e2e_steps))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record(stream)
+    for _ in range(k):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": aggregate_throughput(nbytes, k, ms / 1e3, world), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": ms / k}
+
+
+def run_reference(args):
+    """The fp64 CPU oracle, as it stands, on host cores: each step is a
+    bounded sample of the workload sized so the whole run takes minutes."""
+    spec = gen.SPECS[args.config]
+    host = gen.make_inputs(spec)
+    budget = max(0.002, args.reference_seconds / (args.steps + args.warmup))
+    for w in range(args.warmup):
+        oracle_sample_run(host, budget, start_unit=w)
+    secs, nbytes, desc = 0.0, 0, None
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s, b, d = oracle_sample_run(host, budget, start_unit=args.warmup + i)
+        secs += s
+        nbytes += b
+        desc = desc or d
+    wall = time.perf_counter() - t0
+    value = nbytes / secs / 1e9
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOADS[args.config], "num_splits": args.num_splits},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"per step: {desc}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    result = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -148,6 +148,14 @@ pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t
 /* A static description of a status code (never NULL). */
 const char* pa_status_string(pa_status status);
 
+/* Benchmark hook. Arms the calling thread's NEXT pa_decode, pa_decode_fp8 or
+ * pa_decode_tidar call to record `start_event` on its stream just before the
+ * split kernel's launch and `split_done_event` just after it (both are
+ * cudaEvent_t handles owned by the caller; NULL disarms). The arming is
+ * consumed by that call whatever its outcome, so the split kernel alone can
+ * be timed with cudaEventElapsedTime. Pure host bookkeeping; no device work. */
+pa_status pa_decode_profile_events(void* start_event, void* split_done_event);
+
 /* Reads and clears the current device's error flags set by the kernels
  * (bit 0: a pipeline wait in the split kernel ran out of time). Synchronous;
  * for diagnostics only, never inside stream capture. */

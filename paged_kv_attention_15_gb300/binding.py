@@ -53,6 +53,7 @@ _SIGNATURES = {
     "pa_decode_reduce": (ctypes.c_int, [_P, _P, ctypes.c_int32, ctypes.POINTER(PaShape), _P, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32)]),
+    "pa_decode_profile_events": (ctypes.c_int, [_P, _P]),
 }
 
 
@@ -188,6 +189,13 @@ def decode_reduce(part_out: torch.Tensor, part_lse: torch.Tensor, *, out: Option
                                 _stream(stream))
     _check(st, "pa_decode_reduce")
     return out, lse
+
+
+def arm_profile_events(start_event, split_done_event) -> None:
+    """Record the two torch.cuda.Event objects around the split kernel of the
+    calling thread's next decode call (see pa_decode_profile_events)."""
+    _check(lib().pa_decode_profile_events(start_event.cuda_event, split_done_event.cuda_event),
+           "pa_decode_profile_events")
 
 
 def device_error() -> int:

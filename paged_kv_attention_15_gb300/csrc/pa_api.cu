@@ -38,6 +38,10 @@ struct DeviceState {
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 
+// One-shot events armed by pa_decode_profile_events for this thread's next call.
+thread_local cudaEvent_t t_ev_start = nullptr;
+thread_local cudaEvent_t t_ev_split = nullptr;
+
 enum class Kind { kBf16, kFp8, kTidar };
 
 pa_status device_state(DeviceState** out) {
@@ -211,7 +215,15 @@ struct CallArgs {
   cudaStream_t stream;
 };
 
+pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t ev_split);
+
 pa_status run_decode(const CallArgs& a) {
+  cudaEvent_t ev_start = t_ev_start, ev_split = t_ev_split;
+  t_ev_start = t_ev_split = nullptr;
+  return run_decode_impl(a, ev_start, ev_split);
+}
+
+pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t ev_split) {
   pa_status st = check_shape(a.shape, a.kind);
   if (st != PA_OK) return st;
   const pa_shape& s = *a.shape;
@@ -295,8 +307,10 @@ pa_status run_decode(const CallArgs& a) {
   if ((st = ensure_smem_attr(d, k.fn)) != PA_OK) return st;
   const dim3 grid = plan.balanced ? dim3(plan.grid) : dim3(B * Hkv, plan.splits);
   void* args[] = {&p};
+  if (ev_start && cudaEventRecord(ev_start, a.stream) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaLaunchKernel(k.fn, grid, dim3(pa::kThreads), args, plan.smem, a.stream) != cudaSuccess)
     return PA_ERR_CUDA;
+  if (ev_split && cudaEventRecord(ev_split, a.stream) != cudaSuccess) return PA_ERR_CUDA;
 
   if (plan.balanced || plan.splits > 1) {
     ReduceParams r;
@@ -420,6 +434,12 @@ const char* pa_status_string(pa_status status) {
     case PA_ERR_CUDA: return "CUDA error";
   }
   return "unknown status";
+}
+
+pa_status pa_decode_profile_events(void* start_event, void* split_done_event) {
+  t_ev_start = static_cast<cudaEvent_t>(start_event);
+  t_ev_split = static_cast<cudaEvent_t>(split_done_event);
+  return PA_OK;
 }
 
 pa_status pa_decode_device_error(int32_t* flags) {

@@ -319,25 +319,3 @@ def _poison(k, v, k_scale, v_scale, bt, lens, npages, pool, P):
 def custom_spec(name="custom", **kw) -> DecodeSpec:
     """A DecodeSpec for ad-hoc shapes (tests)."""
     return DecodeSpec(name=name, **kw)
-
-
-def algorithmic_bytes(inp: DecodeInputs) -> int:
-    """Bytes a decode call must move at minimum: the KV rows of valid tokens,
-    their fp8 scales, the block-table entries in use, q, out, lse,
-    context_lens and the draft-block scratch KV. Split-K scratch traffic is
-    not counted."""
-    s = inp.spec
-    lens = inp.context_lens.to(torch.int64)
-    tokens = int(lens.sum())
-    pages = int(((lens + s.page_size - 1) // s.page_size).sum())
-    kv_elem = 1 if s.kv_format == "fp8" else 2
-    nbytes = 2 * tokens * s.num_kv_heads * s.head_dim * kv_elem
-    if s.kv_format == "fp8":
-        nbytes += 2 * tokens * s.num_kv_heads * 4
-    nbytes += pages * 4
-    rows = s.batch * s.q_tokens * s.num_q_heads
-    nbytes += rows * s.head_dim * 2 * 2  # q in, out
-    nbytes += rows * 4 + s.batch * 4  # lse, context_lens
-    if s.draft_scratch:
-        nbytes += 2 * s.batch * s.q_tokens * s.num_kv_heads * s.head_dim * 2
-    return nbytes
