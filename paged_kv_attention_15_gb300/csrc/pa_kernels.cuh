@@ -23,9 +23,9 @@
 // QK^T and PV run as mma.sync m16n8k16 with fp32 accumulators; the score
 // fragment becomes the P operand in registers; K is read with ldmatrix and
 // V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). Stages
-// are dealt round-robin to NG = 4 / MT groups of MT warps (MT = m16 tiles of
-// query rows); at the end of a work item the groups merge through shared
-// memory. Every wait is bounded in time, so a protocol error cannot hang
+// are dealt round-robin to stage groups of MT warps (MT = m16 tiles of
+// query rows), each group owning its own ring slots; at the end of a work
+// item the groups merge through shared memory. Every wait is bounded in time, so a protocol error cannot hang
 // the GPU.
 #pragma once
 
@@ -96,13 +96,18 @@ struct Cfg {
   static constexpr int QCH = D / 64;
   static constexpr int QCHUNK = ROWS * 128;
   static constexpr int QSLOT = QCH * QCHUNK;
-  static constexpr int NG = kConsumerWarps / MT;  // stage groups
-  static constexpr int RSTR = D + 8;              // floats per row of the merge buffer
-  static constexpr int RED = (NG - 1) * ROWS * RSTR * 4;
-  static constexpr int REDML = (NG - 1) * ROWS * 2 * 4;
+  static constexpr int NGW = kConsumerWarps / MT;  // warp groups (each holds a partial result)
+  static constexpr int RSTR = D + 8;               // floats per row of the merge buffer
+  static constexpr int RED = (NGW - 1) * ROWS * RSTR * 4;
+  static constexpr int REDML = (NGW - 1) * ROWS * 2 * 4;
   static constexpr int BARS = 256;
   static constexpr int FIXED = 2 * QSLOT + round_up(RED + REDML, 1024) + BARS;
-  static constexpr int NS = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
+  static constexpr int NS_FIT = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
+  // Stage groups: each owns SPG ring slots and walks them in order, so a
+  // waiter is never more than one mbarrier phase ahead of its slot.
+  static constexpr int NG = NGW < NS_FIT ? NGW : NS_FIT;
+  static constexpr int SPG = NS_FIT / NG;
+  static constexpr int NS = NG * SPG;
   static constexpr int OFF_Q = NS * STAGE;
   static constexpr int OFF_RED = OFF_Q + 2 * QSLOT;
   static constexpr int OFF_REDML = OFF_RED + RED;
@@ -200,14 +205,16 @@ __device__ __forceinline__ uint32_t swz(int row, int unit) {
   return (uint32_t)(row * 128 + (((unit) ^ (row & 7)) << 4));
 }
 
-// After an abandoned wait: let the copies that may still be in flight land
-// before this CTA's shared memory can be reused (each wait is bounded too).
-template <int NS>
-__device__ __forceinline__ void drain_copies(uint32_t bar_full, uint32_t bar_qfull, int stages, int qloads) {
+// Waits (bounded, ignoring the abort flag) for the last fill of every ring
+// slot and Q slot this producer issued, so that no copy is still in flight
+// when the CTA exits. `filled` has bit s set if slot s was ever filled, and
+// `parity` holds the phase parity of its last fill.
+__device__ __forceinline__ void drain_copies(uint32_t bar_full, uint32_t bar_qfull, int ns, uint32_t filled,
+                                             uint32_t parity, int qloads) {
   const int zero = 0;
   const volatile int* no_abort = &zero;
-  for (int st = stages - NS > 0 ? stages - NS : 0; st < stages; ++st)
-    mbar_wait(bar_full + 8 * (st % NS), (st / NS) & 1, kWaitLimitNs, no_abort);
+  for (int s = 0; s < ns; ++s)
+    if (filled >> s & 1) mbar_wait(bar_full + 8 * s, parity >> s & 1, kWaitLimitNs, no_abort);
   for (int q = qloads - 2 > 0 ? qloads - 2 : 0; q < qloads; ++q)
     mbar_wait(bar_qfull + 8 * (q & 1), (q >> 1) & 1, kWaitLimitNs, no_abort);
 }
@@ -222,8 +229,10 @@ template <int D, int MT, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_constant__ SplitParams p) {
   using C = Cfg<D, MT, FP8>;
   constexpr int NS = C::NS;
-  constexpr int NG = C::NG;
-  constexpr int NT8 = D / 8;  // n8 tiles of the output row
+  constexpr int NG = C::NG;    // stage groups (each owns SPG ring slots)
+  constexpr int NGW = C::NGW;  // warp groups holding partial results
+  constexpr int SPG = C::SPG;
+  constexpr int NT8 = D / 8;   // n8 tiles of the output row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -293,7 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     Cursor cur;
     cursor_init(p, s_start, cur);
     Item it;
-    int stage = 0, qn = 0;
+    int qn = 0;
+    int gcnt[NG];  // stages dealt to each stage group so far
+#pragma unroll
+    for (int q = 0; q < NG; ++q) gcnt[q] = 0;
+    uint32_t filled = 0, fill_parity = 0;
     bool ok = true;
     while (ok && next_item(p, s_ctx, s_start, cur, it)) {
       if (it.nst == 0) continue;
@@ -315,12 +328,19 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       int ibase = 0;
       int ids = lane < npages ? __ldg(bt_row + pbase + lane) : 0;
       int ids_next = 32 + lane < npages ? __ldg(bt_row + pbase + 32 + lane) : 0;
-      for (int j = 0; j < it.nst; ++j, ++stage) {
-        const int slot = stage % NS;
-        if (stage >= NS) {
-          ok = mbar_wait(bar_empty + 8 * slot, ((stage / NS) - 1) & 1, kWaitLimitNs, s_abort);
+      for (int j = 0; j < it.nst; ++j) {
+        const int grp_j = j % NG;  // stage j of an item goes to stage group j % NG
+        int cj = j / NG;
+#pragma unroll
+        for (int q = 0; q < NG; ++q)
+          if (q == grp_j) cj += gcnt[q];
+        const int slot = grp_j * SPG + cj % SPG;
+        if (cj >= SPG) {
+          ok = mbar_wait(bar_empty + 8 * slot, ((cj / SPG) - 1) & 1, kWaitLimitNs, s_abort);
           if (!ok) break;
         }
+        filled |= 1u << slot;
+        fill_parity = (fill_parity & ~(1u << slot)) | (uint32_t((cj / SPG) & 1) << slot);
         const uint32_t full = bar_full + 8 * slot;
         const uint32_t kdst = sbase + slot * C::STAGE;
         const uint32_t vdst = kdst + C::TILE;
@@ -384,12 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           }
         }
       }
+#pragma unroll
+      for (int q = 0; q < NG; ++q) gcnt[q] += it.nst > q ? (it.nst - q + NG - 1) / NG : 0;
     }
-    if (!ok || *s_abort) {
-      // Stop the consumers, then let the copies already issued land.
-      if (lane == 0) raise_abort(s_abort, p.err_flags);
-      drain_copies<NS>(bar_full, bar_qfull, stage, qn);
-    }
+    if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
+    // Let every copy this warp issued land before the CTA can exit.
+    drain_copies(bar_full, bar_qfull, NS, filled, fill_parity, qn);
     return;
   }
 
@@ -405,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   Cursor cur;
   cursor_init(p, s_start, cur);
   Item it;
-  int stage = 0, qn = 0;
+  int qn = 0;
+  int mycnt = 0;  // stages this warp's stage group has consumed so far
   bool ok = true;
   float acc[NT8][4];
 
@@ -456,11 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
 #pragma unroll
       for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-      for (int j = grp; j < it.nst; j += NG) {
-        const int st = stage + j;
-        const int slot = st % NS;
+      for (int j = grp; grp < NG && j < it.nst; j += NG) {
+        const int cj = mycnt + (j - grp) / NG;
+        const int slot = grp * SPG + cj % SPG;
         if (ok) {
-          ok = mbar_wait(bar_full + 8 * slot, (st / NS) & 1, kWaitLimitNs, s_abort);
+          ok = mbar_wait(bar_full + 8 * slot, (cj / SPG) & 1, kWaitLimitNs, s_abort);
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
         if (ok) {
@@ -629,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
       }
-      stage += it.nst;
+      if (grp < NG && it.nst > grp) mycnt += (it.nst - grp + NG - 1) / NG;
       if (FP8) fence_proxy_async_smem();  // the slot was rewritten through the generic proxy
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_qempty + 8 * qs);
@@ -639,13 +660,13 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
 
-    // ---- merge the NG groups' partial results, then write
+    // ---- merge the NGW warp groups' partial results, then write
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const int rho0 = mt * 16 + r, rho1 = rho0 + 8;
-    if (NG > 1) {
+    if (NGW > 1) {
       named_barrier_sync(1, 32 * kConsumerWarps);
       if (grp > 0) {
         float* rb = red + (size_t)(grp - 1) * C::ROWS * C::RSTR;
@@ -668,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
 
     float M0 = m0, M1 = m1;
 #pragma unroll
-    for (int q = 0; q < NG - 1; ++q) {
+    for (int q = 0; q < NGW - 1; ++q) {
       M0 = fmaxf(M0, redml[(q * C::ROWS + rho0) * 2]);
       M1 = fmaxf(M1, redml[(q * C::ROWS + rho1) * 2]);
     }
@@ -676,9 +697,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     const float Mu1 = M1 == NEG_INF ? 0.f : M1;
     const float w00 = ex2(m0 - Mu0), w01 = ex2(m1 - Mu1);
     float L0 = w00 * l0, L1 = w01 * l1;
-    float wq0[NG > 1 ? NG - 1 : 1], wq1[NG > 1 ? NG - 1 : 1];
+    float wq0[NGW > 1 ? NGW - 1 : 1], wq1[NGW > 1 ? NGW - 1 : 1];
 #pragma unroll
-    for (int q = 0; q < NG - 1; ++q) {
+    for (int q = 0; q < NGW - 1; ++q) {
       wq0[q] = ex2(redml[(q * C::ROWS + rho0) * 2] - Mu0);
       wq1[q] = ex2(redml[(q * C::ROWS + rho1) * 2] - Mu1);
       L0 += wq0[q] * redml[(q * C::ROWS + rho0) * 2 + 1];
@@ -690,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     for (int i = 0; i < NT8; ++i) {
       float a0 = acc[i][0] * w00, a1 = acc[i][1] * w00, a2 = acc[i][2] * w01, a3 = acc[i][3] * w01;
 #pragma unroll
-      for (int q = 0; q < NG - 1; ++q) {
+      for (int q = 0; q < NGW - 1; ++q) {
         const float* rb = red + (size_t)q * C::ROWS * C::RSTR;
         const float2 x = *reinterpret_cast<const float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4);
         const float2 y = *reinterpret_cast<const float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4);
@@ -747,7 +768,6 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       }
     }
   }
-  if (warp == 0 && *s_abort) drain_copies<NS>(bar_full, bar_qfull, stage, qn);
 }
 
 }  // namespace pa
