@@ -293,6 +293,9 @@ def run_ours(args, world, rank, local):
     assert pb.device_error() == 0
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:  # torch creates the CUDA event handles on first record
+        a.record(stream)
+        b.record(stream)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier(world)
