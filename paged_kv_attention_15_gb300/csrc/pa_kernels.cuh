@@ -233,6 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   constexpr int NGW = C::NGW;  // warp groups holding partial results
   constexpr int SPG = C::SPG;
   constexpr int NT8 = D / 8;   // n8 tiles of the output row
+  constexpr int TSUB = D >= 256 ? 32 : 64;  // tokens per softmax sub-block
+  constexpr int NTS = TSUB / 8;            // n8 tiles of a sub-block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -492,156 +494,161 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           const float* ksc = reinterpret_cast<const float*>(smem + slot * C::STAGE + 2 * C::TILE);
           const float* vsc = ksc + C::SCALE / 4;
 
-          // ---- S = Q K^T for the 64 tokens of the stage (16 rows x 64 tokens)
-          float s[8][4];
+          // The stage is processed in sub-blocks of TSUB tokens (32 when D = 256,
+          // which keeps the score tile and the accumulator in registers).
+#pragma unroll 1
+          for (int tb = 0; tb < kTS && tb < valid; tb += TSUB) {
+            // ---- S = Q K^T for TSUB tokens of the stage (16 rows x TSUB tokens)
+            float s[NTS][4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-          if (!FP8) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              uint32_t qa[4];
-              {
-                const int row = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int d = kk * 16 + (lane >> 4) * 8;
-                ldsm_x4(qbase + (d / 64) * C::QCHUNK + swz(row, (d % 64) / 8), qa[0], qa[1], qa[2], qa[3]);
-              }
-#pragma unroll
-              for (int nb = 0; nb < 4; ++nb) {
-                const int tok = nb * 16 + (lane >> 4) * 8 + (lane & 7);
-                const int d = kk * 16 + ((lane >> 3) & 1) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
-                mma_bf16(s[2 * nb], qa, b0, b1);
-                mma_bf16(s[2 * nb + 1], qa, b2, b3);
-              }
-            }
-          } else {
-            const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
-#pragma unroll
-            for (int kq = 0; kq < D / 64; ++kq) {
-              uint32_t qa[4][4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
-                qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
-              }
-#pragma unroll
-              for (int nt = 0; nt < 8; ++nt) {
-                const int tok = nt * 8 + (lane & 7);
-                const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
-                uint32_t kr[4];
-                ldsm_x4(kb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), kr[0], kr[1], kr[2], kr[3]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
-              }
-            }
-          }
-
-          // ---- scale (and per-token K scale), mask, online softmax in base 2
-          const float sl = p.scale_log2;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = i * 8 + 2 * c4 + (e & 1);
-              float f = s[i][e] * sl;
-              if (FP8) f *= ksc[tok * p.Hkv + it.g];
-              s[i][e] = tok < valid ? f : NEG_INF;
-            }
-          }
-          float mx0 = NEG_INF, mx1 = NEG_INF;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][1]));
-            mx1 = fmaxf(mx1, fmaxf(s[i][2], s[i][3]));
-          }
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-          const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
-          const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
-          const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
-          m0 = mn0;
-          m1 = mn1;
-          float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            s[i][0] = ex2(s[i][0] - mu0);
-            s[i][1] = ex2(s[i][1] - mu0);
-            s[i][2] = ex2(s[i][2] - mu1);
-            s[i][3] = ex2(s[i][3] - mu1);
-            ls0 += s[i][0] + s[i][1];
-            ls1 += s[i][2] + s[i][3];
-          }
-          l0 = l0 * al0 + ls0;
-          l1 = l1 * al1 + ls1;
-#pragma unroll
-          for (int i = 0; i < NT8; ++i) {
-            acc[i][0] *= al0;
-            acc[i][1] *= al0;
-            acc[i][2] *= al1;
-            acc[i][3] *= al1;
-          }
-
-          // ---- O += P V: the score fragments are the A operand as they are
-          const bool partial = valid < kTS;
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            const int t0 = kb * 16 + 2 * c4;  // tokens of the lo fragment; +8 for the hi one
-            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-            if (partial) {
-              vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-              vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-            }
-            uint32_t pa[4];
+            for (int i = 0; i < NTS; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
             if (!FP8) {
-              pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
-              pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
-              pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
-              pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
 #pragma unroll
-              for (int nd = 0; nd < D / 16; ++nd) {
-                const int tok = kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int d = nd * 16 + (lane >> 4) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
-                if (partial) {
-                  b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
+              for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t qa[4];
+                {
+                  const int row = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                  const int d = kk * 16 + (lane >> 4) * 8;
+                  ldsm_x4(qbase + (d / 64) * C::QCHUNK + swz(row, (d % 64) / 8), qa[0], qa[1], qa[2], qa[3]);
                 }
-                mma_bf16(acc[2 * nd], pa, b0, b1);
-                mma_bf16(acc[2 * nd + 1], pa, b2, b3);
+#pragma unroll
+                for (int nb = 0; nb < NTS / 2; ++nb) {
+                  const int tok = tb + nb * 16 + (lane >> 4) * 8 + (lane & 7);
+                  const int d = kk * 16 + ((lane >> 3) & 1) * 8;
+                  uint32_t b0, b1, b2, b3;
+                  ldsm_x4(kb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                  mma_bf16(s[2 * nb], qa, b0, b1);
+                  mma_bf16(s[2 * nb + 1], qa, b2, b3);
+                }
               }
             } else {
-              // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
-              float vs[4];
-              vs[0] = t0 < valid ? vsc[t0 * p.Hkv + it.g] : 0.f;
-              vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + it.g] : 0.f;
-              vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + it.g] : 0.f;
-              vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + it.g] : 0.f;
-              pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
-              pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
-              pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
-              pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
+              const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
 #pragma unroll
-              for (int uu = 0; uu < D / 32; ++uu) {
-                const int tok = kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int unit = 2 * uu + (lane >> 4);
-                uint32_t R[4];
-                ldsm_x4_trans(vb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), R[0], R[1], R[2], R[3]);
-                if (partial) {
-                  R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
+              for (int kq = 0; kq < D / 64; ++kq) {
+                uint32_t qa[4][4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
+                  qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
                 }
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  // bytes (tok 2c d 2r, tok 2c d 2r+1, tok 2c+1 d 2r, tok 2c+1 d 2r+1)
-                  const uint32_t x = prmt(R[2 * k], 0, 0x3120);
-                  const uint32_t y = prmt(R[2 * k + 1], 0, 0x3120);
-                  const int nt = 2 * (2 * uu + k);
-                  mma_f16(acc[nt], pa, e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(y));
-                  mma_f16(acc[nt + 1], pa, e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y >> 16));
+                for (int nt = 0; nt < NTS; ++nt) {
+                  const int tok = tb + nt * 8 + (lane & 7);
+                  const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
+                  uint32_t kr[4];
+                  ldsm_x4(kb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), kr[0], kr[1], kr[2], kr[3]);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
+                }
+              }
+            }
+
+            // ---- scale (and per-token K scale), mask, online softmax in base 2
+            const float sl = p.scale_log2;
+#pragma unroll
+            for (int i = 0; i < NTS; ++i) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int tok = tb + i * 8 + 2 * c4 + (e & 1);
+                float f = s[i][e] * sl;
+                if (FP8) f *= ksc[tok * p.Hkv + it.g];
+                s[i][e] = tok < valid ? f : NEG_INF;
+              }
+            }
+            float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+            for (int i = 0; i < NTS; ++i) {
+              mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][1]));
+              mx1 = fmaxf(mx1, fmaxf(s[i][2], s[i][3]));
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
+            const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
+            const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+            m0 = mn0;
+            m1 = mn1;
+            float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < NTS; ++i) {
+              s[i][0] = ex2(s[i][0] - mu0);
+              s[i][1] = ex2(s[i][1] - mu0);
+              s[i][2] = ex2(s[i][2] - mu1);
+              s[i][3] = ex2(s[i][3] - mu1);
+              ls0 += s[i][0] + s[i][1];
+              ls1 += s[i][2] + s[i][3];
+            }
+            l0 = l0 * al0 + ls0;
+            l1 = l1 * al1 + ls1;
+#pragma unroll
+            for (int i = 0; i < NT8; ++i) {
+              acc[i][0] *= al0;
+              acc[i][1] *= al0;
+              acc[i][2] *= al1;
+              acc[i][3] *= al1;
+            }
+
+            // ---- O += P V: the score fragments are the A operand as they are
+            const bool partial = valid < tb + TSUB;
+#pragma unroll
+            for (int kb = 0; kb < NTS / 2; ++kb) {
+              const int t0 = tb + kb * 16 + 2 * c4;  // tokens of the lo fragment; +8 for the hi one
+              uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+              if (partial) {
+                vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+                vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+              }
+              uint32_t pa[4];
+              if (!FP8) {
+                pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
+                pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
+                pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
+                pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
+#pragma unroll
+                for (int nd = 0; nd < D / 16; ++nd) {
+                  const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                  const int d = nd * 16 + (lane >> 4) * 8;
+                  uint32_t b0, b1, b2, b3;
+                  ldsm_x4_trans(vb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                  if (partial) {
+                    b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
+                  }
+                  mma_bf16(acc[2 * nd], pa, b0, b1);
+                  mma_bf16(acc[2 * nd + 1], pa, b2, b3);
+                }
+              } else {
+                // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
+                float vs[4];
+                vs[0] = t0 < valid ? vsc[t0 * p.Hkv + it.g] : 0.f;
+                vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + it.g] : 0.f;
+                vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + it.g] : 0.f;
+                vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + it.g] : 0.f;
+                pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
+                pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
+                pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
+                pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
+#pragma unroll
+                for (int uu = 0; uu < D / 32; ++uu) {
+                  const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                  const int unit = 2 * uu + (lane >> 4);
+                  uint32_t R[4];
+                  ldsm_x4_trans(vb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), R[0], R[1], R[2], R[3]);
+                  if (partial) {
+                    R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
+                  }
+#pragma unroll
+                  for (int k = 0; k < 2; ++k) {
+                    // bytes (tok 2c d 2r, tok 2c d 2r+1, tok 2c+1 d 2r, tok 2c+1 d 2r+1)
+                    const uint32_t x = prmt(R[2 * k], 0, 0x3120);
+                    const uint32_t y = prmt(R[2 * k + 1], 0, 0x3120);
+                    const int nt = 2 * (2 * uu + k);
+                    mma_f16(acc[nt], pa, e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(y));
+                    mma_f16(acc[nt + 1], pa, e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y >> 16));
+                  }
                 }
               }
             }
