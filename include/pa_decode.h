@@ -145,6 +145,32 @@ pa_status pa_decode_tidar(const void* q, const void* k_cache, const void* v_cach
 pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t num_splits,
                            const pa_shape* shape, void* out, float* lse, pa_stream_t stream);
 
+/* pa_decode without a caller-provided workspace (the papers have no
+ * counterpart; this is a convenience of this library). Some callers cannot
+ * allocate device memory at the point where they decode: a plug-in that is
+ * handed only the input and output pointers by a host framework whose own
+ * memory pool has reserved the device, or a latency-critical path that must
+ * not call cudaMalloc because it can block and synchronise the device. This
+ * entry point takes the same arguments as pa_decode minus the workspace and
+ * keeps the split-K partials in a fixed scratch array that the library
+ * reserves statically on every GPU that loads it (held until the process
+ * exits): PA_NOALLOC_SCRATCH_BYTES bytes. It allocates nothing.
+ *  - Calls whose partials need more than that (pa_decode_workspace_size()
+ *    above the limit) return PA_ERR_WORKSPACE before any launch.
+ *  - The first call on a device looks up the scratch array's device address
+ *    (once per device, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents; nothing in it needs to start at zero (every partial is
+ *    written before it is read within a call). Calls whose work overlaps on
+ *    the GPU (several streams, or several host threads) race on it: order
+ *    them on one stream. */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            const pa_shape* shape, float scale, void* out, float* lse,
+                            int32_t num_splits, pa_stream_t stream);
+
 /* A static description of a status code (never NULL). */
 const char* pa_status_string(pa_status status);
 

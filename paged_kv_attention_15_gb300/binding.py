@@ -54,6 +54,8 @@ _SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32)]),
     "pa_decode_profile_events": (ctypes.c_int, [_P, _P]),
+    "pa_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float, _P, _P,
+                                         ctypes.c_int32, _P]),
 }
 
 
@@ -173,6 +175,25 @@ def split_workspace_views(workspace: torch.Tensor, B: int, T: int, Hq: int, S: i
     part_out = flat[: rows * D * 4].view(torch.float32).view(B, T, Hq, S, D)
     part_lse = flat[off: off + rows * 4].view(torch.float32).view(B, T, Hq, S)
     return part_out, part_lse
+
+
+def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                   context_lens: torch.Tensor, scale: float, *, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, num_splits: int = 0, stream=None):
+    """pa_decode_noalloc: bf16 paged decode whose split-K scratch is the
+    library's static device array (no workspace argument)."""
+    _need_contig(q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables, context_lens=context_lens,
+                 out=out, lse=lse)
+    shape = make_shape(q, k_cache, block_tables)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    st = lib().pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+                                 ctypes.byref(shape), float(scale), _ptr(out), _ptr(lse), int(num_splits),
+                                 _stream(stream))
+    _check(st, "pa_decode_noalloc")
+    return out, lse
 
 
 def decode_reduce(part_out: torch.Tensor, part_lse: torch.Tensor, *, out: Optional[torch.Tensor] = None,

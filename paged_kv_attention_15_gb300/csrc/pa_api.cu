@@ -436,6 +436,54 @@ const char* pa_status_string(pa_status status) {
   return "unknown status";
 }
 
+// Split-K scratch for pa_decode_noalloc: reserved statically in every
+// device's copy of this module, so the entry point never allocates.
+static __device__ __align__(256) unsigned char g_pa_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+static void* g_noalloc_ptr[kMaxDevices];
+static bool g_noalloc_ready[kMaxDevices];
+
+// Device address of this device's scratch array. In host code the array's
+// name stands for a host-side shadow, so the address must come from the
+// runtime; looked up once per device, with that device current.
+static pa_status noalloc_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  if (!g_noalloc_ready[dev]) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_noalloc_ready[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_pa_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+      g_noalloc_ptr[dev] = p;
+      g_noalloc_ready[dev] = true;
+    }
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return PA_OK;
+}
+
+pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            const int32_t* context_lens, const pa_shape* shape, float scale, void* out,
+                            float* lse, int32_t num_splits, pa_stream_t stream) {
+  pa_status st = check_shape(shape, Kind::kBf16);
+  if (st != PA_OK) return st;
+  if (num_splits < 0) return PA_ERR_INVALID_ARG;
+  size_t need = 0;
+  if (shape->batch > 0) {
+    DeviceState* d = nullptr;
+    if ((st = device_state(&d)) != PA_OK) return st;
+    Plan plan;
+    if ((st = make_plan(shape, Kind::kBf16, num_splits, d, &plan)) != PA_OK) return st;
+    need = plan.ws_bytes;
+  }
+  if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if (need > 0 && (st = noalloc_scratch(&ws)) != PA_OK) return st;
+  return pa_decode(q, k_cache, v_cache, block_tables, context_lens, shape, scale, out, lse, num_splits, ws, need,
+                   stream);
+}
+
 pa_status pa_decode_profile_events(void* start_event, void* split_done_event) {
   t_ev_start = static_cast<cudaEvent_t>(start_event);
   t_ev_split = static_cast<cudaEvent_t>(split_done_event);
