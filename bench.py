@@ -24,6 +24,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import math
@@ -265,12 +266,21 @@ def oracle_sample_run(inp, budget_s: float, start_unit: int = 0):
 
 
 # --------------------------------------------------------------------------- arms
+def workload_spec(args):
+    """The workload's spec; --batch shrinks it (profiling captures only)."""
+    spec = gen.SPECS[args.config]
+    if args.batch:
+        lens = spec.context_lens[: args.batch] if spec.context_lens is not None else None
+        spec = dataclasses.replace(spec, batch=args.batch, context_lens=lens)
+    return spec
+
+
 def run_ours(args, world, rank, local):
     from paged_kv_attention_15_gb300 import binding as pb
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    spec = gen.SPECS[args.config]
+    spec = workload_spec(args)
     host = gen.make_inputs(spec)
     pb.lib()
     sets = [host.to(dev), host.to(dev)]  # alternated: each step reads KV not in L2
@@ -351,7 +361,8 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8" if spec.kv_format == "fp8" else "bf16", "data": "synthetic",
         "config": {
-            "workload": WORKLOADS[args.config], "batch": spec.batch, "q_tokens": spec.q_tokens,
+            "workload": WORKLOADS[args.config] + (f" (batch cut to {spec.batch})" if args.batch else ""),
+            "batch": spec.batch, "q_tokens": spec.q_tokens,
             "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
             "page_size": spec.page_size, "num_splits": args.num_splits, "seed": spec.seed,
             "algorithmic_bytes_per_step": nbytes,
@@ -417,7 +428,7 @@ def run_e2e(args, host, dev, pb, nbytes, world):
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, on host cores: each step is a
     bounded sample of the workload sized so the whole run takes minutes."""
-    spec = gen.SPECS[args.config]
+    spec = workload_spec(args)
     host = gen.make_inputs(spec)
     budget = max(0.002, args.reference_seconds / (args.steps + args.warmup))
     for w in range(args.warmup):
@@ -449,6 +460,7 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--reference-seconds", type=float, default=120.0)
