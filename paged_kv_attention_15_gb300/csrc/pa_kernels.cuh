@@ -23,9 +23,10 @@
 // QK^T and PV run as mma.sync m16n8k16 with fp32 accumulators; the score
 // fragment becomes the P operand in registers; K is read with ldmatrix and
 // V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). Stages
-// are dealt round-robin to stage groups of MT warps (MT = m16 tiles of
-// query rows), each group owning its own ring slots; at the end of a work
-// item the groups merge through shared memory. Every wait is bounded in time, so a protocol error cannot hang
+// are consumed in order by all four consumer warps: warp w takes row tile
+// w % MT (MT = m16 tiles of query rows) and a token slice of every stage,
+// keeping its own online-softmax state; at the end of a work item the
+// slices merge through shared memory. Every wait is bounded in time, so a protocol error cannot hang
 // the GPU.
 #pragma once
 
@@ -102,12 +103,7 @@ struct Cfg {
   static constexpr int REDML = (NGW - 1) * ROWS * 2 * 4;
   static constexpr int BARS = 256;
   static constexpr int FIXED = 2 * QSLOT + round_up(RED + REDML, 1024) + BARS;
-  static constexpr int NS_FIT = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
-  // Stage groups: each owns SPG ring slots and walks them in order, so a
-  // waiter is never more than one mbarrier phase ahead of its slot.
-  static constexpr int NG = NGW < NS_FIT ? NGW : NS_FIT;
-  static constexpr int SPG = NS_FIT / NG;
-  static constexpr int NS = NG * SPG;
+  static constexpr int NS = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
   static constexpr int OFF_Q = NS * STAGE;
   static constexpr int OFF_RED = OFF_Q + 2 * QSLOT;
   static constexpr int OFF_REDML = OFF_RED + RED;
@@ -229,12 +225,10 @@ template <int D, int MT, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_constant__ SplitParams p) {
   using C = Cfg<D, MT, FP8>;
   constexpr int NS = C::NS;
-  constexpr int NG = C::NG;    // stage groups (each owns SPG ring slots)
-  constexpr int NGW = C::NGW;  // warp groups holding partial results
-  constexpr int SPG = C::SPG;
-  constexpr int NT8 = D / 8;   // n8 tiles of the output row
-  constexpr int TSUB = D >= 256 ? 32 : 64;  // tokens per softmax sub-block
-  constexpr int NTS = TSUB / 8;            // n8 tiles of a sub-block
+  constexpr int NGW = C::NGW;          // token groups, each holding a partial result
+  constexpr int TSL = kTS / NGW;       // tokens of a stage per warp
+  constexpr int NTS = TSL / 8;         // n8 tiles of a warp's slice
+  constexpr int NT8 = D / 8;           // n8 tiles of the output row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -255,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, MT);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(bar_qfull + 8 * q, 1);
@@ -304,10 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     Cursor cur;
     cursor_init(p, s_start, cur);
     Item it;
-    int qn = 0;
-    int gcnt[NG];  // stages dealt to each stage group so far
-#pragma unroll
-    for (int q = 0; q < NG; ++q) gcnt[q] = 0;
+    int stage = 0, qn = 0;
     uint32_t filled = 0, fill_parity = 0;
     bool ok = true;
     while (ok && next_item(p, s_ctx, s_start, cur, it)) {
@@ -330,19 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       int ibase = 0;
       int ids = lane < npages ? __ldg(bt_row + pbase + lane) : 0;
       int ids_next = 32 + lane < npages ? __ldg(bt_row + pbase + 32 + lane) : 0;
-      for (int j = 0; j < it.nst; ++j) {
-        const int grp_j = j % NG;  // stage j of an item goes to stage group j % NG
-        int cj = j / NG;
-#pragma unroll
-        for (int q = 0; q < NG; ++q)
-          if (q == grp_j) cj += gcnt[q];
-        const int slot = grp_j * SPG + cj % SPG;
-        if (cj >= SPG) {
-          ok = mbar_wait(bar_empty + 8 * slot, ((cj / SPG) - 1) & 1, kWaitLimitNs, s_abort);
+      for (int j = 0; j < it.nst; ++j, ++stage) {
+        const int slot = stage % NS;
+        if (stage >= NS) {
+          ok = mbar_wait(bar_empty + 8 * slot, ((stage / NS) - 1) & 1, kWaitLimitNs, s_abort);
           if (!ok) break;
         }
         filled |= 1u << slot;
-        fill_parity = (fill_parity & ~(1u << slot)) | (uint32_t((cj / SPG) & 1) << slot);
+        fill_parity = (fill_parity & ~(1u << slot)) | (uint32_t((stage / NS) & 1) << slot);
         const uint32_t full = bar_full + 8 * slot;
         const uint32_t kdst = sbase + slot * C::STAGE;
         const uint32_t vdst = kdst + C::TILE;
@@ -406,8 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           }
         }
       }
-#pragma unroll
-      for (int q = 0; q < NG; ++q) gcnt[q] += it.nst > q ? (it.nst - q + NG - 1) / NG : 0;
     }
     if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
     // Let every copy this warp issued land before the CTA can exit.
@@ -416,8 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   }
 
   // ================================================================ consumers
+  // Warp w owns row tile mt = w % MT and the token slice tg = w / MT of every
+  // stage (TSL tokens); all consumer warps read every stage, so the ring is
+  // consumed strictly in order and NS - 1 stages stay in flight.
   const int mt = warp % MT;
-  const int grp = warp / MT;
+  const int tg = warp / MT;
   const int r = lane >> 2;
   const int c4 = lane & 3;
   const float NEG_INF = -__int_as_float(0x7f800000);
@@ -427,8 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   Cursor cur;
   cursor_init(p, s_start, cur);
   Item it;
-  int qn = 0;
-  int mycnt = 0;  // stages this warp's stage group has consumed so far
+  int stage = 0, qn = 0;
   bool ok = true;
   float acc[NT8][4];
 
@@ -448,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         // d = 16 s + 4 c4 .. +3. The fragments of k-steps 4q..4q+3 of row
         // tile mt take exactly the 2 KB that the tile's rows occupy in
         // column chunk q, so each chunk is converted by its own warp.
-        if (grp == 0) {
+        if (tg == 0) {
           uint8_t* qs_ptr = smem + C::OFF_Q + qs * C::QSLOT;
           uint4* dst = reinterpret_cast<uint4*>(qs_ptr);
 #pragma unroll
@@ -479,111 +465,111 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
 #pragma unroll
       for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-      for (int j = grp; grp < NG && j < it.nst; j += NG) {
-        const int cj = mycnt + (j - grp) / NG;
-        const int slot = grp * SPG + cj % SPG;
+      for (int j = 0; j < it.nst; ++j) {
+        const int st = stage + j;
+        const int slot = st % NS;
         if (ok) {
-          ok = mbar_wait(bar_full + 8 * slot, (cj / SPG) & 1, kWaitLimitNs, s_abort);
+          ok = mbar_wait(bar_full + 8 * slot, (st / NS) & 1, kWaitLimitNs, s_abort);
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
-        if (ok) {
-          const bool scr = it.scratch && j == it.nst - 1;
-          const int valid = scr ? p.T : min(kTS, it.tok_end - (it.tok0 + j * kTS));
+        const bool scr = it.scratch && j == it.nst - 1;
+        const int valid = scr ? p.T : min(kTS, it.tok_end - (it.tok0 + j * kTS));
+        const int tb = tg * TSL;  // first token of this warp's slice
+        if (ok && tb < valid) {
           const uint32_t kb_ = sbase + slot * C::STAGE;
           const uint32_t vb_ = kb_ + C::TILE;
           const float* ksc = reinterpret_cast<const float*>(smem + slot * C::STAGE + 2 * C::TILE);
           const float* vsc = ksc + C::SCALE / 4;
 
-          // The stage is processed in sub-blocks of TSUB tokens (32 when D = 256,
-          // which keeps the score tile and the accumulator in registers).
-#pragma unroll 1
-          for (int tb = 0; tb < kTS && tb < valid; tb += TSUB) {
-            // ---- S = Q K^T for TSUB tokens of the stage (16 rows x TSUB tokens)
-            float s[NTS][4];
+          // ---- S = Q K^T: 16 rows x TSL tokens
+          float s[NTS][4];
 #pragma unroll
-            for (int i = 0; i < NTS; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-            if (!FP8) {
+          for (int i = 0; i < NTS; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+          if (!FP8) {
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t qa[4];
-                {
-                  const int row = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                  const int d = kk * 16 + (lane >> 4) * 8;
-                  ldsm_x4(qbase + (d / 64) * C::QCHUNK + swz(row, (d % 64) / 8), qa[0], qa[1], qa[2], qa[3]);
-                }
-#pragma unroll
-                for (int nb = 0; nb < NTS / 2; ++nb) {
-                  const int tok = tb + nb * 16 + (lane >> 4) * 8 + (lane & 7);
-                  const int d = kk * 16 + ((lane >> 3) & 1) * 8;
-                  uint32_t b0, b1, b2, b3;
-                  ldsm_x4(kb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
-                  mma_bf16(s[2 * nb], qa, b0, b1);
-                  mma_bf16(s[2 * nb + 1], qa, b2, b3);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+              uint32_t qa[4];
+              {
+                const int row = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int d = kk * 16 + (lane >> 4) * 8;
+                ldsm_x4(qbase + (d / 64) * C::QCHUNK + swz(row, (d % 64) / 8), qa[0], qa[1], qa[2], qa[3]);
               }
-            } else {
-              const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
 #pragma unroll
-              for (int kq = 0; kq < D / 64; ++kq) {
-                uint32_t qa[4][4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
-                  qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
-                }
-#pragma unroll
-                for (int nt = 0; nt < NTS; ++nt) {
-                  const int tok = tb + nt * 8 + (lane & 7);
-                  const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
-                  uint32_t kr[4];
-                  ldsm_x4(kb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), kr[0], kr[1], kr[2], kr[3]);
-#pragma unroll
-                  for (int e = 0; e < 4; ++e)
-                    mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
-                }
+              for (int nb = 0; nb < NTS / 2; ++nb) {
+                const int tok = tb + nb * 16 + (lane >> 4) * 8 + (lane & 7);
+                const int d = kk * 16 + ((lane >> 3) & 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                mma_bf16(s[2 * nb], qa, b0, b1);
+                mma_bf16(s[2 * nb + 1], qa, b2, b3);
               }
             }
-
-            // ---- scale (and per-token K scale), mask, online softmax in base 2
-            const float sl = p.scale_log2;
+          } else {
+            const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
 #pragma unroll
-            for (int i = 0; i < NTS; ++i) {
+            for (int kq = 0; kq < D / 64; ++kq) {
+              uint32_t qa[4][4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int tok = tb + i * 8 + 2 * c4 + (e & 1);
-                float f = s[i][e] * sl;
-                if (FP8) f *= ksc[tok * p.Hkv + it.g];
-                s[i][e] = tok < valid ? f : NEG_INF;
+                const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
+                qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
+              }
+#pragma unroll
+              for (int nt = 0; nt < NTS; ++nt) {
+                const int tok = tb + nt * 8 + (lane & 7);
+                const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
+                uint32_t kr[4];
+                ldsm_x4(kb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), kr[0], kr[1], kr[2], kr[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
               }
             }
-            float mx0 = NEG_INF, mx1 = NEG_INF;
+          }
+
+          // ---- scale (and per-token K scale), mask, online softmax in base 2
+          const float sl = p.scale_log2;
 #pragma unroll
-            for (int i = 0; i < NTS; ++i) {
-              mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][1]));
-              mx1 = fmaxf(mx1, fmaxf(s[i][2], s[i][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
-            const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
-            const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
-            m0 = mn0;
-            m1 = mn1;
-            float ls0 = 0.f, ls1 = 0.f;
+          for (int i = 0; i < NTS; ++i) {
 #pragma unroll
-            for (int i = 0; i < NTS; ++i) {
-              s[i][0] = ex2(s[i][0] - mu0);
-              s[i][1] = ex2(s[i][1] - mu0);
-              s[i][2] = ex2(s[i][2] - mu1);
-              s[i][3] = ex2(s[i][3] - mu1);
-              ls0 += s[i][0] + s[i][1];
-              ls1 += s[i][2] + s[i][3];
+            for (int e = 0; e < 4; ++e) {
+              const int tok = tb + i * 8 + 2 * c4 + (e & 1);
+              float f = s[i][e] * sl;
+              if (FP8) f *= ksc[tok * p.Hkv + it.g];
+              s[i][e] = tok < valid ? f : NEG_INF;
             }
-            l0 = l0 * al0 + ls0;
-            l1 = l1 * al1 + ls1;
+          }
+          float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+          for (int i = 0; i < NTS; ++i) {
+            mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[i][2], s[i][3]));
+          }
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
+          const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
+          const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+          m0 = mn0;
+          m1 = mn1;
+          float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < NTS; ++i) {
+            s[i][0] = ex2(s[i][0] - mu0);
+            s[i][1] = ex2(s[i][1] - mu0);
+            s[i][2] = ex2(s[i][2] - mu1);
+            s[i][3] = ex2(s[i][3] - mu1);
+            ls0 += s[i][0] + s[i][1];
+            ls1 += s[i][2] + s[i][3];
+          }
+          l0 = l0 * al0 + ls0;
+          l1 = l1 * al1 + ls1;
+          // The running max rarely moves after the first stages: rescale
+          // the accumulator only when some row's max grew.
+          if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
             for (int i = 0; i < NT8; ++i) {
               acc[i][0] *= al0;
@@ -591,64 +577,64 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               acc[i][2] *= al1;
               acc[i][3] *= al1;
             }
+          }
 
-            // ---- O += P V: the score fragments are the A operand as they are
-            const bool partial = valid < tb + TSUB;
+          // ---- O += P V: the score fragments are the A operand as they are
+          const bool partial = valid < tb + TSL;
 #pragma unroll
-            for (int kb = 0; kb < NTS / 2; ++kb) {
-              const int t0 = tb + kb * 16 + 2 * c4;  // tokens of the lo fragment; +8 for the hi one
-              uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-              if (partial) {
-                vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-                vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-              }
-              uint32_t pa[4];
-              if (!FP8) {
-                pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
-                pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
-                pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
-                pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
+          for (int kb = 0; kb < NTS / 2; ++kb) {
+            const int t0 = tb + kb * 16 + 2 * c4;  // tokens of the lo fragment; +8 for the hi one
+            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+            if (partial) {
+              vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+              vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+            }
+            uint32_t pa[4];
+            if (!FP8) {
+              pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
+              pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
+              pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
+              pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
 #pragma unroll
-                for (int nd = 0; nd < D / 16; ++nd) {
-                  const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                  const int d = nd * 16 + (lane >> 4) * 8;
-                  uint32_t b0, b1, b2, b3;
-                  ldsm_x4_trans(vb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
-                  if (partial) {
-                    b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
-                  }
-                  mma_bf16(acc[2 * nd], pa, b0, b1);
-                  mma_bf16(acc[2 * nd + 1], pa, b2, b3);
+              for (int nd = 0; nd < D / 16; ++nd) {
+                const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int d = nd * 16 + (lane >> 4) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                if (partial) {
+                  b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
                 }
-              } else {
-                // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
-                float vs[4];
-                vs[0] = t0 < valid ? vsc[t0 * p.Hkv + it.g] : 0.f;
-                vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + it.g] : 0.f;
-                vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + it.g] : 0.f;
-                vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + it.g] : 0.f;
-                pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
-                pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
-                pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
-                pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
+                mma_bf16(acc[2 * nd], pa, b0, b1);
+                mma_bf16(acc[2 * nd + 1], pa, b2, b3);
+              }
+            } else {
+              // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
+              float vs[4];
+              vs[0] = t0 < valid ? vsc[t0 * p.Hkv + it.g] : 0.f;
+              vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + it.g] : 0.f;
+              vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + it.g] : 0.f;
+              vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + it.g] : 0.f;
+              pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
+              pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
+              pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
+              pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
 #pragma unroll
-                for (int uu = 0; uu < D / 32; ++uu) {
-                  const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                  const int unit = 2 * uu + (lane >> 4);
-                  uint32_t R[4];
-                  ldsm_x4_trans(vb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), R[0], R[1], R[2], R[3]);
-                  if (partial) {
-                    R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
-                  }
+              for (int uu = 0; uu < D / 32; ++uu) {
+                const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int unit = 2 * uu + (lane >> 4);
+                uint32_t R[4];
+                ldsm_x4_trans(vb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), R[0], R[1], R[2], R[3]);
+                if (partial) {
+                  R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
+                }
 #pragma unroll
-                  for (int k = 0; k < 2; ++k) {
-                    // bytes (tok 2c d 2r, tok 2c d 2r+1, tok 2c+1 d 2r, tok 2c+1 d 2r+1)
-                    const uint32_t x = prmt(R[2 * k], 0, 0x3120);
-                    const uint32_t y = prmt(R[2 * k + 1], 0, 0x3120);
-                    const int nt = 2 * (2 * uu + k);
-                    mma_f16(acc[nt], pa, e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(y));
-                    mma_f16(acc[nt + 1], pa, e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y >> 16));
-                  }
+                for (int k = 0; k < 2; ++k) {
+                  // bytes (tok 2c d 2r, tok 2c d 2r+1, tok 2c+1 d 2r, tok 2c+1 d 2r+1)
+                  const uint32_t x = prmt(R[2 * k], 0, 0x3120);
+                  const uint32_t y = prmt(R[2 * k + 1], 0, 0x3120);
+                  const int nt = 2 * (2 * uu + k);
+                  mma_f16(acc[nt], pa, e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(y));
+                  mma_f16(acc[nt + 1], pa, e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y >> 16));
                 }
               }
             }
@@ -657,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
       }
-      if (grp < NG && it.nst > grp) mycnt += (it.nst - grp + NG - 1) / NG;
+      stage += it.nst;
       if (FP8) fence_proxy_async_smem();  // the slot was rewritten through the generic proxy
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_qempty + 8 * qs);
@@ -675,15 +661,15 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     const int rho0 = mt * 16 + r, rho1 = rho0 + 8;
     if (NGW > 1) {
       named_barrier_sync(1, 32 * kConsumerWarps);
-      if (grp > 0) {
-        float* rb = red + (size_t)(grp - 1) * C::ROWS * C::RSTR;
+      if (tg > 0) {
+        float* rb = red + (size_t)(tg - 1) * C::ROWS * C::RSTR;
 #pragma unroll
         for (int i = 0; i < NT8; ++i) {
           *reinterpret_cast<float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][0], acc[i][1]);
           *reinterpret_cast<float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][2], acc[i][3]);
         }
         if (c4 == 0) {
-          float* ml = redml + (size_t)(grp - 1) * C::ROWS * 2;
+          float* ml = redml + (size_t)(tg - 1) * C::ROWS * 2;
           ml[2 * rho0] = m0;
           ml[2 * rho0 + 1] = l0;
           ml[2 * rho1] = m1;
@@ -692,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       }
       named_barrier_sync(1, 32 * kConsumerWarps);
     }
-    if (grp != 0) continue;
+    if (tg != 0) continue;
 
     float M0 = m0, M1 = m1;
 #pragma unroll
