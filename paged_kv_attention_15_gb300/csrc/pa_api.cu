@@ -98,16 +98,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map, dims innermost first, strides in bytes for dims 1..3, 128-byte swizzle.
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims[4],
-              const uint64_t strides[3], const uint32_t box[4]) {
+// Rank-R map (R = 4 or 5), dims innermost first, strides in bytes for dims
+// 1..R-1, 128-byte swizzle.
+template <int R>
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[R],
+              const uint64_t (&strides)[R - 1], const uint32_t (&box)[R]) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
-  cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
-  cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, dt, 4, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  cuuint64_t gd[R], gs[R - 1];
+  cuuint32_t bx[R], es[R];
+  for (int i = 0; i < R; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i < R - 1) gs[i] = strides[i];
+  }
+  return fn(m, dt, R, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
@@ -262,18 +268,22 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     const uint32_t box[4] = {64u, (uint32_t)G, (uint32_t)T, 1u};
     if (!make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, dims, str, box)) return PA_ERR_INVALID_ARG;
   }
+  // KV caches as 5-D (128-byte column chunk, kv head, slot, chunk index,
+  // page): one box copies every chunk of up to 64 rows of one page and head,
+  // landing in shared memory as [chunk][row][128 B].
+  const uint64_t nch = (uint64_t)D * e / 128;
   {
-    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)P, (uint64_t)s.num_pages};
-    const uint64_t str[3] = {(uint64_t)D * e, (uint64_t)Hkv * D * e, (uint64_t)P * Hkv * D * e};
-    const uint32_t box[4] = {(uint32_t)(128 / e), 1u, (uint32_t)(P < pa::kTS ? P : pa::kTS), 1u};
+    const uint64_t dims[5] = {128 / e, (uint64_t)Hkv, (uint64_t)P, nch, (uint64_t)s.num_pages};
+    const uint64_t str[4] = {(uint64_t)D * e, (uint64_t)Hkv * D * e, 128, (uint64_t)P * Hkv * D * e};
+    const uint32_t box[5] = {(uint32_t)(128 / e), 1u, (uint32_t)(P < pa::kTS ? P : pa::kTS), (uint32_t)nch, 1u};
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (!make_map(&p.tm_k, dt, a.k_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
     if (!make_map(&p.tm_v, dt, a.v_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
   }
   if (a.kind == Kind::kTidar) {
-    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
-    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2, (uint64_t)T * Hkv * D * 2};
-    const uint32_t box[4] = {64u, 1u, (uint32_t)T, 1u};
+    const uint64_t dims[5] = {64, (uint64_t)Hkv, (uint64_t)T, nch, (uint64_t)B};
+    const uint64_t str[4] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2, 128, (uint64_t)T * Hkv * D * 2};
+    const uint32_t box[5] = {64u, 1u, (uint32_t)T, (uint32_t)nch, 1u};
     if (!make_map(&p.tm_ks, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k_scratch, dims, str, box) ||
         !make_map(&p.tm_vs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v_scratch, dims, str, box))
       return PA_ERR_INVALID_ARG;

@@ -89,7 +89,6 @@ struct Cfg {
   static constexpr int ELEM = FP8 ? 1 : 2;
   static constexpr int CE = 128 / ELEM;         // elements per 128-byte row chunk
   static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
-  static constexpr int CHUNK = kTS * 128;       // bytes of one chunk column of a stage tile
   static constexpr int TILE = kTS * D * ELEM;   // bytes of the K (or V) tile of a stage
   static constexpr int SCALE = FP8 ? kTS * kMaxHkvFp8 * 4 : 0;
   static constexpr int STAGE = round_up(2 * TILE + 2 * SCALE, 1024);
@@ -201,6 +200,17 @@ __device__ __forceinline__ uint32_t swz(int row, int unit) {
   return (uint32_t)(row * 128 + (((unit) ^ (row & 7)) << 4));
 }
 
+// Byte offset, in a stage tile laid out [box][chunk][box row][128 B] with
+// br rows per box (NCH chunks), of 16-byte unit `unit` of column chunk
+// `chunk` of token `tok`. The 128-byte swizzle XORs the unit with bits
+// 7..9 of the row's offset (tiles are 1024-byte aligned).
+template <int NCH>
+__device__ __forceinline__ uint32_t kv_unit_impl(int tok, int chunk, int unit, int br) {
+  const int box = tok / br, rr = tok - box * br;
+  const uint32_t row = (uint32_t)(((box * NCH + chunk) * br + rr) * 128);
+  return row + ((uint32_t)(unit ^ ((row >> 7) & 7)) << 4);
+}
+
 // Waits (bounded, ignoring the abort flag) for the last fill of every ring
 // slot and Q slot this producer issued, so that no copy is still in flight
 // when the CTA exits. `filled` has bit s set if slot s was ever filled, and
@@ -229,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   constexpr int TSL = kTS / NGW;       // tokens of a stage per warp
   constexpr int NTS = TSL / 8;         // n8 tiles of a warp's slice
   constexpr int NT8 = D / 8;           // n8 tiles of the output row
+  auto kv_unit = [](int tok, int chunk, int unit, int br) { return kv_unit_impl<C::NCH>(tok, chunk, unit, br); };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -337,11 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         if (it.scratch && j == it.nst - 1) {
           if (lane == 0) {
             mbar_arrive_expect_tx(full, 2 * C::NCH * p.T * 128);
-#pragma unroll
-            for (int c = 0; c < C::NCH; ++c) {
-              tma_load_4d(kdst + c * C::CHUNK, &p.tm_ks, full, c * C::CE, it.g, 0, it.b, pol_kv);
-              tma_load_4d(vdst + c * C::CHUNK, &p.tm_vs, full, c * C::CE, it.g, 0, it.b, pol_kv);
-            }
+            tma_load_5d(kdst, &p.tm_ks, full, 0, it.g, 0, 0, it.b, pol_kv);
+            tma_load_5d(vdst, &p.tm_vs, full, 0, it.g, 0, 0, it.b, pol_kv);
           }
           continue;
         }
@@ -360,11 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           for (int i = 0; i < npg; ++i) {
             const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase + i);
             if (lane == 0) {
-#pragma unroll
-              for (int c = 0; c < C::NCH; ++c) {
-                tma_load_4d(kdst + c * C::CHUNK + i * P * 128, &p.tm_k, full, c * C::CE, it.g, 0, page, pol_kv);
-                tma_load_4d(vdst + c * C::CHUNK + i * P * 128, &p.tm_v, full, c * C::CE, it.g, 0, page, pol_kv);
-              }
+              // one box per page: every column chunk of its P rows
+              tma_load_5d(kdst + i * C::NCH * P * 128, &p.tm_k, full, 0, it.g, 0, 0, page, pol_kv);
+              tma_load_5d(vdst + i * C::NCH * P * 128, &p.tm_v, full, 0, it.g, 0, 0, page, pol_kv);
               if (FP8) {
                 const uint32_t sb = P * p.Hkv * 4;
                 const size_t off = (size_t)page * P * p.Hkv;
@@ -378,11 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase);
           if (lane == 0) {
             mbar_arrive_expect_tx(full, 2 * kTS * (C::NCH * 128 + (FP8 ? p.Hkv * 4 : 0)));
-#pragma unroll
-            for (int c = 0; c < C::NCH; ++c) {
-              tma_load_4d(kdst + c * C::CHUNK, &p.tm_k, full, c * C::CE, it.g, row0, page, pol_kv);
-              tma_load_4d(vdst + c * C::CHUNK, &p.tm_v, full, c * C::CE, it.g, row0, page, pol_kv);
-            }
+            tma_load_5d(kdst, &p.tm_k, full, 0, it.g, row0, 0, page, pol_kv);
+            tma_load_5d(vdst, &p.tm_v, full, 0, it.g, row0, 0, page, pol_kv);
             if (FP8) {
               const uint32_t sb = kTS * p.Hkv * 4;
               const size_t off = ((size_t)page * P + row0) * p.Hkv;
@@ -476,6 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         const int valid = scr ? p.T : min(kTS, it.tok_end - (it.tok0 + j * kTS));
         const int tb = tg * TSL;  // first token of this warp's slice
         if (ok && tb < valid) {
+          // A stage tile is [box][chunk][box row][128 B]; a box holds br rows
+          // (the page, or 64 rows of a large page, or the T scratch rows).
+          const int br = scr ? p.T : (P < kTS ? P : kTS);
           const uint32_t kb_ = sbase + slot * C::STAGE;
           const uint32_t vb_ = kb_ + C::TILE;
           const float* ksc = reinterpret_cast<const float*>(smem + slot * C::STAGE + 2 * C::TILE);
@@ -499,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 const int tok = tb + nb * 16 + (lane >> 4) * 8 + (lane & 7);
                 const int d = kk * 16 + ((lane >> 3) & 1) * 8;
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                ldsm_x4(kb_ + kv_unit(tok, d / 64, (d % 64) / 8, br), b0, b1, b2, b3);
                 mma_bf16(s[2 * nb], qa, b0, b1);
                 mma_bf16(s[2 * nb + 1], qa, b2, b3);
               }
@@ -519,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 const int tok = tb + nt * 8 + (lane & 7);
                 const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
                 uint32_t kr[4];
-                ldsm_x4(kb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), kr[0], kr[1], kr[2], kr[3]);
+                ldsm_x4(kb_ + kv_unit(tok, unit / 8, unit % 8, br), kr[0], kr[1], kr[2], kr[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                   mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
@@ -600,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
                 const int d = nd * 16 + (lane >> 4) * 8;
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vb_ + (d / 64) * C::CHUNK + swz(tok, (d % 64) / 8), b0, b1, b2, b3);
+                ldsm_x4_trans(vb_ + kv_unit(tok, d / 64, (d % 64) / 8, br), b0, b1, b2, b3);
                 if (partial) {
                   b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
                 }
@@ -623,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
                 const int unit = 2 * uu + (lane >> 4);
                 uint32_t R[4];
-                ldsm_x4_trans(vb_ + (unit / 8) * C::CHUNK + swz(tok, unit % 8), R[0], R[1], R[2], R[3]);
+                ldsm_x4_trans(vb_ + kv_unit(tok, unit / 8, unit % 8, br), R[0], R[1], R[2], R[3]);
                 if (partial) {
                   R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
                 }
