@@ -41,6 +41,10 @@ namespace pa {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kTS = 64;  // tokens per pipeline stage
+// Pages smaller than this are gathered with 16-byte cp.async by the 32
+// producer lanes instead of one TMA box per page: a copy engine box of a
+// 16-row page is too small to keep enough bytes in flight per SM.
+constexpr int kLsuPageLimit = 32;
 constexpr int kMaxHkvFp8 = 8;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -60,6 +64,10 @@ struct SplitParams {
   const int32_t* context_lens;
   const float* k_scale;
   const float* v_scale;
+  const void* k_cache;    // raw pointers for the cp.async gather
+  const void* v_cache;
+  const void* k_scratch;
+  const void* v_scratch;
   __nv_bfloat16* out;
   float* lse;
   float* part_o;
@@ -259,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, p.P < kLsuPageLimit ? 32 : 1);
       mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
     for (int q = 0; q < 2; ++q) {
@@ -311,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     Item it;
     int stage = 0, qn = 0;
     uint32_t filled = 0, fill_parity = 0;
+    const bool lsu = P < kLsuPageLimit;
     bool ok = true;
     while (ok && next_item(p, s_ctx, s_start, cur, it)) {
       if (it.nst == 0) continue;
@@ -345,6 +354,63 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         const uint32_t vdst = kdst + C::TILE;
         const uint32_t ksd = kdst + 2 * C::TILE;
         const uint32_t vsd = ksd + C::SCALE;
+        if (lsu) {
+          // ---- gather with cp.async: lane l copies 16-byte units l, l+32, ...
+          // into the same swizzled [box][chunk][row][128 B] layout the TMA
+          // boxes produce; the stage completes on 32 noinc arrivals.
+          constexpr int U = D * C::ELEM / 16;  // 16-byte units per KV row
+          const bool scr = it.scratch && j == it.nst - 1;
+          if (scr) {
+            const size_t rstride = (size_t)p.Hkv * D;  // scratch row stride (elements, bf16)
+            const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(p.k_scratch) +
+                                      ((size_t)it.b * p.T * p.Hkv + it.g) * D;
+            const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(p.v_scratch) +
+                                      ((size_t)it.b * p.T * p.Hkv + it.g) * D;
+            for (int u = lane; u < p.T * U; u += 32) {
+              const int row = u / U, cu = u % U;
+              const uint32_t off = kv_unit_impl<C::NCH>(row, cu / 8, cu % 8, p.T);
+              cp_async_16(kdst + off, ks + row * rstride + cu * 8, pol_kv);
+              cp_async_16(vdst + off, vs + row * rstride + cu * 8, pol_kv);
+            }
+          } else {
+            const int t_first = it.tok0 + j * kTS;
+            const int valid = min(kTS, it.tok_end - t_first);
+            const int pidx0 = t_first / P - pbase;
+            while (pidx0 >= ibase + 32) {
+              ibase += 32;
+              ids = ids_next;
+              ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
+            }
+            const int npg = (valid + P - 1) / P;
+            const size_t rstride = (size_t)p.Hkv * D * C::ELEM;  // bytes between slots of a page
+            for (int i = 0; i < npg; ++i) {
+              const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase + i);
+              // Page ids outside the pool would read out of bounds: skip them
+              // (the slots keep stale data; only a corrupt table gets here).
+              if ((unsigned)page >= (unsigned)p.num_pages) continue;
+              const size_t pbyte = ((size_t)page * P * p.Hkv + it.g) * D * C::ELEM;
+              const char* kp = reinterpret_cast<const char*>(p.k_cache) + pbyte;
+              const char* vp = reinterpret_cast<const char*>(p.v_cache) + pbyte;
+#pragma unroll 4
+              for (int u = lane; u < P * U; u += 32) {
+                const int row = u / U, cu = u % U;
+                const uint32_t off = kv_unit_impl<C::NCH>(i * P + row, cu / 8, cu % 8, P);
+                cp_async_16(kdst + off, kp + row * rstride + cu * 16, pol_kv);
+                cp_async_16(vdst + off, vp + row * rstride + cu * 16, pol_kv);
+              }
+              if (FP8) {
+                const int su = P * p.Hkv * 4 / 16;  // 16-byte units of the page's scales
+                const size_t off = (size_t)page * P * p.Hkv;
+                for (int u = lane; u < su; u += 32) {
+                  cp_async_16(ksd + i * P * p.Hkv * 4 + u * 16, p.k_scale + off + u * 4, pol_kv);
+                  cp_async_16(vsd + i * P * p.Hkv * 4 + u * 16, p.v_scale + off + u * 4, pol_kv);
+                }
+              }
+            }
+          }
+          cp_async_mbar_arrive(full);
+          continue;
+        }
         if (it.scratch && j == it.nst - 1) {
           if (lane == 0) {
             mbar_arrive_expect_tx(full, 2 * C::NCH * p.T * 128);
@@ -398,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     }
     if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
     // Let every copy this warp issued land before the CTA can exit.
-    drain_copies(bar_full, bar_qfull, NS, filled, fill_parity, qn);
+    cp_async_wait_all();
+    drain_copies(bar_full, bar_qfull, lsu ? 0 : NS, filled, fill_parity, qn);
     return;
   }
 
