@@ -346,14 +346,25 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     r.tidar = p.tidar;
     r.num_splits = plan.balanced ? 0 : plan.splits;
     r.grid = plan.grid;
-    void* rargs[] = {&r};
+    // Programmatic dependent launch: the reduce grid may start while the
+    // split grid drains and waits (griddepcontrol.wait) for its results.
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t err;
-    if (plan.balanced)
-      err = cudaLaunchKernel(reinterpret_cast<const void*>(&pa::pa_reduce_balanced_kernel), dim3(B * Hkv),
-                             dim3(128), rargs, 0, a.stream);
-    else
-      err = cudaLaunchKernel(reinterpret_cast<const void*>(&pa::pa_reduce_splits_kernel),
-                             dim3((unsigned)(((size_t)B * T * Hq + 3) / 4)), dim3(128), rargs, 0, a.stream);
+    if (plan.balanced) {
+      cfg.gridDim = dim3(B * Hkv);
+      err = cudaLaunchKernelEx(&cfg, pa::pa_reduce_balanced_kernel, r);
+    } else {
+      cfg.gridDim = dim3((unsigned)(((size_t)B * T * Hq + 3) / 4));
+      err = cudaLaunchKernelEx(&cfg, pa::pa_reduce_splits_kernel, r);
+    }
     if (err != cudaSuccess) return PA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -16,10 +16,12 @@
 // e4m3fn KV with symmetric per-token scale, split-K partial combine).
 //
 // GB300 design. One CTA per SM (persistent) or per (sequence, kv head,
-// split). Warp 4 is the producer: it walks the block table and issues TMA
-// box copies of whole pages (K, V, and for fp8 the per-token scales) into
-// a ring of NS shared-memory stages of 64 tokens, each guarded by a pair of
-// mbarriers (full: bytes landed; empty: consumers done). Warps 0-3 consume:
+// split). Warps 4-7 produce: they walk the block table and fill a ring of
+// NS shared-memory stages of 64 tokens, each guarded by a pair of mbarriers
+// (full: bytes landed; empty: consumers done). Pages of 32 rows or more
+// arrive as one TMA box per page (K, V; fp8 scales by bulk copy), issued by
+// warp 4; 16-row pages are gathered with 16-byte cp.async by all four
+// producer warps. Warps 0-3 consume:
 // QK^T and PV run as mma.sync m16n8k16 with fp32 accumulators; the score
 // fragment becomes the P operand in registers; K is read with ldmatrix and
 // V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). Stages
@@ -39,11 +41,12 @@
 namespace pa {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kProducerWarps = 4;  // one copy warp per SM sub-partition (cp.async path)
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr int kTS = 64;  // tokens per pipeline stage
-// Pages smaller than this are gathered with 16-byte cp.async by the 32
-// producer lanes instead of one TMA box per page: a copy engine box of a
-// 16-row page is too small to keep enough bytes in flight per SM.
+// Pages smaller than this are gathered with 16-byte cp.async by the 128
+// producer threads instead of one TMA box per page: the copy engine's box
+// of a 16-row page is too small to keep enough bytes in flight per SM.
 constexpr int kLsuPageLimit = 32;
 constexpr int kMaxHkvFp8 = 8;
 constexpr int kSmemBudget = 220 * 1024;
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full + 8 * s, p.P < kLsuPageLimit ? 32 : 1);
+      mbar_init(bar_full + 8 * s, p.P < kLsuPageLimit ? 32 * kProducerWarps : 1);
       mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
     for (int q = 0; q < 2; ++q) {
@@ -303,13 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   }
   fence_proxy_async_smem();
   __syncthreads();
+  // The split-K reduce may be scheduled now: it waits for this grid to
+  // complete before it reads any partial.
+  launch_dependents();
 
   const int P = p.P;
-  if (warp == kConsumerWarps) {
+  if (warp >= kConsumerWarps) {
     // ================================================================ producer
+    // Warp 4 issues every TMA copy (Q, and the pages when P >= 32); with
+    // smaller pages warps 4-7 share the cp.async gather of each stage.
+    const bool lsu = P < kLsuPageLimit;
+    const int pw = warp - kConsumerWarps;
+    const int pt = pw * 32 + lane;  // producer thread index
+    if (!lsu && pw > 0) return;
+    const bool leader = pw == 0 && lane == 0;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
-    if (lane == 0) {
+    if (leader) {
       prefetch_tensormap(&p.tm_q);
       prefetch_tensormap(&p.tm_k);
       prefetch_tensormap(&p.tm_v);
@@ -319,14 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     Item it;
     int stage = 0, qn = 0;
     uint32_t filled = 0, fill_parity = 0;
-    const bool lsu = P < kLsuPageLimit;
     bool ok = true;
     while (ok && next_item(p, s_ctx, s_start, cur, it)) {
       if (it.nst == 0) continue;
       const int qs = qn & 1;
       if (qn >= 2) ok = mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort);
       if (!ok) break;
-      if (lane == 0) {
+      if (leader) {
         const uint32_t qdst = sbase + C::OFF_Q + qs * C::QSLOT;
         mbar_arrive_expect_tx(bar_qfull + 8 * qs, C::QCH * p.M * 128);
 #pragma unroll
@@ -355,10 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         const uint32_t ksd = kdst + 2 * C::TILE;
         const uint32_t vsd = ksd + C::SCALE;
         if (lsu) {
-          // ---- gather with cp.async: lane l copies 16-byte units l, l+32, ...
-          // into the same swizzled [box][chunk][row][128 B] layout the TMA
-          // boxes produce; the stage completes on 32 noinc arrivals.
+          // ---- gather with cp.async: producer thread pt copies 16-byte units
+          // pt, pt+128, ... into the same swizzled [box][chunk][row][128 B]
+          // layout the TMA boxes produce; the stage completes on 128 noinc
+          // arrivals.
           constexpr int U = D * C::ELEM / 16;  // 16-byte units per KV row
+          constexpr int NPT = 32 * kProducerWarps;
           const bool scr = it.scratch && j == it.nst - 1;
           if (scr) {
             const size_t rstride = (size_t)p.Hkv * D;  // scratch row stride (elements, bf16)
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                                       ((size_t)it.b * p.T * p.Hkv + it.g) * D;
             const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(p.v_scratch) +
                                       ((size_t)it.b * p.T * p.Hkv + it.g) * D;
-            for (int u = lane; u < p.T * U; u += 32) {
+            for (int u = pt; u < p.T * U; u += NPT) {
               const int row = u / U, cu = u % U;
               const uint32_t off = kv_unit_impl<C::NCH>(row, cu / 8, cu % 8, p.T);
               cp_async_16(kdst + off, ks + row * rstride + cu * 8, pol_kv);
@@ -381,30 +395,39 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               ids = ids_next;
               ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
             }
-            const int npg = (valid + P - 1) / P;
+            const int npg = (valid + P - 1) / P;  // <= kTS / P = 4 pages, all in this id window
+            int pg[kTS / 16];
+#pragma unroll
+            for (int i = 0; i < kTS / 16; ++i) pg[i] = __shfl_sync(0xffffffffu, ids, (pidx0 - ibase + i) & 31);
             const size_t rstride = (size_t)p.Hkv * D * C::ELEM;  // bytes between slots of a page
-            for (int i = 0; i < npg; ++i) {
-              const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase + i);
-              // Page ids outside the pool would read out of bounds: skip them
+            const int per_page = P * U;
+            for (int u = pt; u < npg * per_page; u += NPT) {
+              const int i = u / per_page, rem = u - i * per_page;
+              const int row = rem / U, cu = rem % U;
+              int page = pg[0];
+#pragma unroll
+              for (int q = 1; q < kTS / 16; ++q)
+                if (i == q) page = pg[q];
+              // Page ids outside the pool are skipped, never dereferenced
               // (the slots keep stale data; only a corrupt table gets here).
               if ((unsigned)page >= (unsigned)p.num_pages) continue;
-              const size_t pbyte = ((size_t)page * P * p.Hkv + it.g) * D * C::ELEM;
-              const char* kp = reinterpret_cast<const char*>(p.k_cache) + pbyte;
-              const char* vp = reinterpret_cast<const char*>(p.v_cache) + pbyte;
-#pragma unroll 4
-              for (int u = lane; u < P * U; u += 32) {
-                const int row = u / U, cu = u % U;
-                const uint32_t off = kv_unit_impl<C::NCH>(i * P + row, cu / 8, cu % 8, P);
-                cp_async_16(kdst + off, kp + row * rstride + cu * 16, pol_kv);
-                cp_async_16(vdst + off, vp + row * rstride + cu * 16, pol_kv);
-              }
-              if (FP8) {
-                const int su = P * p.Hkv * 4 / 16;  // 16-byte units of the page's scales
-                const size_t off = (size_t)page * P * p.Hkv;
-                for (int u = lane; u < su; u += 32) {
-                  cp_async_16(ksd + i * P * p.Hkv * 4 + u * 16, p.k_scale + off + u * 4, pol_kv);
-                  cp_async_16(vsd + i * P * p.Hkv * 4 + u * 16, p.v_scale + off + u * 4, pol_kv);
-                }
+              const size_t src = ((size_t)page * P * p.Hkv + it.g) * D * C::ELEM + row * rstride + cu * 16;
+              const uint32_t off = kv_unit_impl<C::NCH>(i * P + row, cu / 8, cu % 8, P);
+              cp_async_16(kdst + off, reinterpret_cast<const char*>(p.k_cache) + src, pol_kv);
+              cp_async_16(vdst + off, reinterpret_cast<const char*>(p.v_cache) + src, pol_kv);
+            }
+            if (FP8) {
+              const int su = P * p.Hkv / 4;  // 16-byte units of one page's scales
+              for (int u = pt; u < npg * su; u += NPT) {
+                const int i = u / su, rem = u - i * su;
+                int page = pg[0];
+#pragma unroll
+                for (int q = 1; q < kTS / 16; ++q)
+                  if (i == q) page = pg[q];
+                if ((unsigned)page >= (unsigned)p.num_pages) continue;
+                const size_t off = (size_t)page * P * p.Hkv + rem * 4;
+                cp_async_16(ksd + (i * su + rem) * 16, p.k_scale + off, pol_kv);
+                cp_async_16(vsd + (i * su + rem) * 16, p.v_scale + off, pol_kv);
               }
             }
           }
@@ -463,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       }
     }
     if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
-    // Let every copy this warp issued land before the CTA can exit.
+    // Let every copy this thread issued land before the CTA can exit.
     cp_async_wait_all();
-    drain_copies(bar_full, bar_qfull, lsu ? 0 : NS, filled, fill_parity, qn);
+    if (pw == 0) drain_copies(bar_full, bar_qfull, lsu ? 0 : NS, filled, fill_parity, qn);
     return;
   }
 

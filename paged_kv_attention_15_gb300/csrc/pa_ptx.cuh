@@ -134,6 +134,15 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// ------------------------------------------------- programmatic dependent launch
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialisation) start once every CTA of this grid has executed it.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Waits until the grids this one depends on have completed and their
+// memory operations are visible.
+__device__ __forceinline__ void wait_prerequisite_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- named barrier
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_cons
   const size_t rows = (size_t)p.B * p.T * p.Hq;
   if (row >= rows) return;
   const size_t base = row * p.num_splits;
+  wait_prerequisite_grids();  // the partials come from the split kernel
   reduce_row(p, row, p.part_o + base * p.D, p.part_lse + base, 1, p.num_splits, lane);
 }
 
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_co
     }
     return;
   }
+  wait_prerequisite_grids();  // the partials and final rows come from the split kernel
   const long long G64 = p.grid;
   const int i0 = (int)(((us + 1) * G64 - 1) / N);
   const int i1 = (int)((ue * G64 - 1) / N);
