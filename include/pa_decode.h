@@ -33,8 +33,8 @@
  *    [B, T, Hkv, D] bf16.
  *  - context_lens[b] is clamped on the device to [0, max_blocks_per_seq * P];
  *    only the first ceil(C_b / P) block-table entries of a row are read.
- *    A page id outside [0, num_pages) is never dereferenced and never
- *    faults; the keys and values of such a page are unspecified.
+ *    A page id outside [0, num_pages) reads zeros (the copy engine fills
+ *    out-of-range boxes); it never faults.
  *  - Ownership: the caller owns every buffer, including the workspace. The
  *    library allocates nothing, keeps no pointer after return, performs no
  *    host<->device copy and no synchronisation. Work is enqueued on `stream`

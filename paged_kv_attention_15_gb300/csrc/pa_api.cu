@@ -288,10 +288,6 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
         !make_map(&p.tm_vs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v_scratch, dims, str, box))
       return PA_ERR_INVALID_ARG;
   }
-  p.k_cache = a.k_cache;
-  p.v_cache = a.v_cache;
-  p.k_scratch = a.k_scratch;
-  p.v_scratch = a.v_scratch;
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.k_scale = a.k_scale;

@@ -16,12 +16,10 @@
 // e4m3fn KV with symmetric per-token scale, split-K partial combine).
 //
 // GB300 design. One CTA per SM (persistent) or per (sequence, kv head,
-// split). Warps 4-7 produce: they walk the block table and fill a ring of
-// NS shared-memory stages of 64 tokens, each guarded by a pair of mbarriers
-// (full: bytes landed; empty: consumers done). Pages of 32 rows or more
-// arrive as one TMA box per page (K, V; fp8 scales by bulk copy), issued by
-// warp 4; 16-row pages are gathered with 16-byte cp.async by all four
-// producer warps. Warps 0-3 consume:
+// split). Warp 4 is the producer: it walks the block table and issues TMA
+// box copies of whole pages (K, V, and for fp8 the per-token scales) into
+// a ring of NS shared-memory stages of 64 tokens, each guarded by a pair of
+// mbarriers (full: bytes landed; empty: consumers done). Warps 0-3 consume:
 // QK^T and PV run as mma.sync m16n8k16 with fp32 accumulators; the score
 // fragment becomes the P operand in registers; K is read with ldmatrix and
 // V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). Stages
@@ -41,13 +39,8 @@
 namespace pa {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarps = 4;  // one copy warp per SM sub-partition (cp.async path)
-constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kTS = 64;  // tokens per pipeline stage
-// Pages smaller than this are gathered with 16-byte cp.async by the 128
-// producer threads instead of one TMA box per page: the copy engine's box
-// of a 16-row page is too small to keep enough bytes in flight per SM.
-constexpr int kLsuPageLimit = 32;
 constexpr int kMaxHkvFp8 = 8;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -67,10 +60,6 @@ struct SplitParams {
   const int32_t* context_lens;
   const float* k_scale;
   const float* v_scale;
-  const void* k_cache;    // raw pointers for the cp.async gather
-  const void* v_cache;
-  const void* k_scratch;
-  const void* v_scratch;
   __nv_bfloat16* out;
   float* lse;
   float* part_o;
@@ -270,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar_full + 8 * s, p.P < kLsuPageLimit ? 32 * kProducerWarps : 1);
+      mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
     for (int q = 0; q < 2; ++q) {
@@ -311,18 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   launch_dependents();
 
   const int P = p.P;
-  if (warp >= kConsumerWarps) {
+  if (warp == kConsumerWarps) {
     // ================================================================ producer
-    // Warp 4 issues every TMA copy (Q, and the pages when P >= 32); with
-    // smaller pages warps 4-7 share the cp.async gather of each stage.
-    const bool lsu = P < kLsuPageLimit;
-    const int pw = warp - kConsumerWarps;
-    const int pt = pw * 32 + lane;  // producer thread index
-    if (!lsu && pw > 0) return;
-    const bool leader = pw == 0 && lane == 0;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
-    if (leader) {
+    if (lane == 0) {
       prefetch_tensormap(&p.tm_q);
       prefetch_tensormap(&p.tm_k);
       prefetch_tensormap(&p.tm_v);
@@ -338,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       const int qs = qn & 1;
       if (qn >= 2) ok = mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort);
       if (!ok) break;
-      if (leader) {
+      if (lane == 0) {
         const uint32_t qdst = sbase + C::OFF_Q + qs * C::QSLOT;
         mbar_arrive_expect_tx(bar_qfull + 8 * qs, C::QCH * p.M * 128);
 #pragma unroll
@@ -366,74 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         const uint32_t vdst = kdst + C::TILE;
         const uint32_t ksd = kdst + 2 * C::TILE;
         const uint32_t vsd = ksd + C::SCALE;
-        if (lsu) {
-          // ---- gather with cp.async: producer thread pt copies 16-byte units
-          // pt, pt+128, ... into the same swizzled [box][chunk][row][128 B]
-          // layout the TMA boxes produce; the stage completes on 128 noinc
-          // arrivals.
-          constexpr int U = D * C::ELEM / 16;  // 16-byte units per KV row
-          constexpr int NPT = 32 * kProducerWarps;
-          const bool scr = it.scratch && j == it.nst - 1;
-          if (scr) {
-            const size_t rstride = (size_t)p.Hkv * D;  // scratch row stride (elements, bf16)
-            const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(p.k_scratch) +
-                                      ((size_t)it.b * p.T * p.Hkv + it.g) * D;
-            const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(p.v_scratch) +
-                                      ((size_t)it.b * p.T * p.Hkv + it.g) * D;
-            for (int u = pt; u < p.T * U; u += NPT) {
-              const int row = u / U, cu = u % U;
-              const uint32_t off = kv_unit_impl<C::NCH>(row, cu / 8, cu % 8, p.T);
-              cp_async_16(kdst + off, ks + row * rstride + cu * 8, pol_kv);
-              cp_async_16(vdst + off, vs + row * rstride + cu * 8, pol_kv);
-            }
-          } else {
-            const int t_first = it.tok0 + j * kTS;
-            const int valid = min(kTS, it.tok_end - t_first);
-            const int pidx0 = t_first / P - pbase;
-            while (pidx0 >= ibase + 32) {
-              ibase += 32;
-              ids = ids_next;
-              ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
-            }
-            const int npg = (valid + P - 1) / P;  // <= kTS / P = 4 pages, all in this id window
-            int pg[kTS / 16];
-#pragma unroll
-            for (int i = 0; i < kTS / 16; ++i) pg[i] = __shfl_sync(0xffffffffu, ids, (pidx0 - ibase + i) & 31);
-            const size_t rstride = (size_t)p.Hkv * D * C::ELEM;  // bytes between slots of a page
-            const int per_page = P * U;
-            for (int u = pt; u < npg * per_page; u += NPT) {
-              const int i = u / per_page, rem = u - i * per_page;
-              const int row = rem / U, cu = rem % U;
-              int page = pg[0];
-#pragma unroll
-              for (int q = 1; q < kTS / 16; ++q)
-                if (i == q) page = pg[q];
-              // Page ids outside the pool are skipped, never dereferenced
-              // (the slots keep stale data; only a corrupt table gets here).
-              if ((unsigned)page >= (unsigned)p.num_pages) continue;
-              const size_t src = ((size_t)page * P * p.Hkv + it.g) * D * C::ELEM + row * rstride + cu * 16;
-              const uint32_t off = kv_unit_impl<C::NCH>(i * P + row, cu / 8, cu % 8, P);
-              cp_async_16(kdst + off, reinterpret_cast<const char*>(p.k_cache) + src, pol_kv);
-              cp_async_16(vdst + off, reinterpret_cast<const char*>(p.v_cache) + src, pol_kv);
-            }
-            if (FP8) {
-              const int su = P * p.Hkv / 4;  // 16-byte units of one page's scales
-              for (int u = pt; u < npg * su; u += NPT) {
-                const int i = u / su, rem = u - i * su;
-                int page = pg[0];
-#pragma unroll
-                for (int q = 1; q < kTS / 16; ++q)
-                  if (i == q) page = pg[q];
-                if ((unsigned)page >= (unsigned)p.num_pages) continue;
-                const size_t off = (size_t)page * P * p.Hkv + rem * 4;
-                cp_async_16(ksd + (i * su + rem) * 16, p.k_scale + off, pol_kv);
-                cp_async_16(vsd + (i * su + rem) * 16, p.v_scale + off, pol_kv);
-              }
-            }
-          }
-          cp_async_mbar_arrive(full);
-          continue;
-        }
         if (it.scratch && j == it.nst - 1) {
           if (lane == 0) {
             mbar_arrive_expect_tx(full, 2 * C::NCH * p.T * 128);
@@ -486,9 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       }
     }
     if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
-    // Let every copy this thread issued land before the CTA can exit.
-    cp_async_wait_all();
-    if (pw == 0) drain_copies(bar_full, bar_qfull, lsu ? 0 : NS, filled, fill_parity, qn);
+    // Let every copy this warp issued land before the CTA can exit.
+    drain_copies(bar_full, bar_qfull, NS, filled, fill_parity, qn);
     return;
   }
 

@@ -119,21 +119,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// ------------------------------------------------------------ cp.async (LSU)
-// 16-byte global -> shared copy through the load/store unit, L1 bypassed.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
-               : "memory");
-}
-
-// The mbarrier receives one arrival when every cp.async this thread issued
-// so far has landed (counts against the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // ------------------------------------------------- programmatic dependent launch
 // Lets the next kernel in the stream (launched with programmatic stream
 // serialisation) start once every CTA of this grid has executed it.
