@@ -490,10 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           const float* ksc = reinterpret_cast<const float*>(smem + slot * C::STAGE + 2 * C::TILE);
           const float* vsc = ksc + C::SCALE / 4;
 
-          // ---- S = Q K^T: 16 rows x TSL tokens
-          float s[NTS][4];
+          // ---- S = Q K^T: 16 rows x TSL tokens. Two accumulators per tile
+          // (even and odd k-steps) halve the dependent MMA chain.
+          float s[NTS][4], s2[NTS][4];
 #pragma unroll
-          for (int i = 0; i < NTS; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+          for (int i = 0; i < NTS; ++i) {
+            s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+            s2[i][0] = s2[i][1] = s2[i][2] = s2[i][3] = 0.f;
+          }
           if (!FP8) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -509,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 const int d = kk * 16 + ((lane >> 3) & 1) * 8;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kb_ + kv_unit(tok, d / 64, (d % 64) / 8, br), b0, b1, b2, b3);
-                mma_bf16(s[2 * nb], qa, b0, b1);
-                mma_bf16(s[2 * nb + 1], qa, b2, b3);
+                mma_bf16((kk & 1) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
+                mma_bf16((kk & 1) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
               }
             }
           } else {
@@ -531,9 +535,17 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 ldsm_x4(kb_ + kv_unit(tok, unit / 8, unit % 8, br), kr[0], kr[1], kr[2], kr[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                  mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
+                  mma_f16((e & 1) ? s2[nt] : s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
               }
             }
+          }
+
+#pragma unroll
+          for (int i = 0; i < NTS; ++i) {
+            s[i][0] += s2[i][0];
+            s[i][1] += s2[i][1];
+            s[i][2] += s2[i][2];
+            s[i][3] += s2[i][3];
           }
 
           // ---- scale (and per-token K scale), mask, online softmax in base 2
