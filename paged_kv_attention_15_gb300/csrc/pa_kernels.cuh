@@ -295,9 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   }
   fence_proxy_async_smem();
   __syncthreads();
-  // The split-K reduce may be scheduled now: it waits for this grid to
-  // complete before it reads any partial.
-  launch_dependents();
 
   const int P = p.P;
   if (warp == kConsumerWarps) {
@@ -399,6 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         }
       }
     }
+    // Near the end of this CTA's work: the split-K reduce may be scheduled
+    // (it waits for this grid to complete before reading any partial).
+    launch_dependents();
     if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
     // Let every copy this warp issued land before the CTA can exit.
     drain_copies(bar_full, bar_qfull, NS, filled, fill_parity, qn);
@@ -782,6 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       }
     }
   }
+  launch_dependents();
 }
 
 }  // namespace pa
