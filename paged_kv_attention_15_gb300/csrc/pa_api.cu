@@ -143,17 +143,75 @@ pa_status check_shape(const pa_shape* s, Kind kind) {
   return PA_OK;
 }
 
-SplitKernel pick_kernel(Kind kind, int D, int MT) {
-  return kind == Kind::kFp8 ? pa::split_kernel_fp8(D, MT) : pa::split_kernel_bf16(D, MT);
+SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL) {
+  return kind == Kind::kFp8 ? pa::split_kernel_fp8(D, MT, TSL) : pa::split_kernel_bf16(D, MT, TSL);
 }
 
-int row_tiles(const pa_shape* s) {
-  const int M = (s->num_q_heads / s->num_kv_heads) * s->q_tokens;
-  return (M + 15) / 16;
+// Work-unit geometry: H2 kv heads per CTA unit, their M = H2 * G * T query
+// rows in MT m16 tiles, TS = 64 / H2 tokens per stage, TSL tokens per warp.
+struct Geom {
+  int GT, H2, NHG, M, MT, TS, TSL, BR, lbr, TP;
+  SplitKernel k;
+};
+
+int ilog2(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
+  const int G = s->num_q_heads / s->num_kv_heads, T = s->q_tokens, P = s->page_size, D = s->head_dim;
+  const int GT = G * T, M = H2 * GT;
+  if (M > 64 || s->num_kv_heads % H2) return false;
+  // With several heads per unit, a head's rows must fill whole m16 tiles or
+  // share one evenly.
+  if (H2 > 1 && (GT < 16 ? 16 % GT : GT % 16)) return false;
+  const int MT = (M + 15) / 16;
+  if (MT != 1 && MT != 2 && MT != 4) return false;
+  const int NGW = pa::kConsumerWarps / MT;
+  const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
+  if (NGW % HT) return false;
+  const int NSL = NGW / HT, TS = pa::kStageRows / H2;
+  if (TS % NSL) return false;
+  const int TSL = TS / NSL;
+  if (TSL != 16 && TSL != 32) return false;
+  const SplitKernel k = pick_kernel(kind, D, MT, TSL);
+  if (!k.fn) return false;
+  g->GT = GT;
+  g->H2 = H2;
+  g->NHG = s->num_kv_heads / H2;
+  g->M = M;
+  g->MT = MT;
+  g->TS = TS;
+  g->TSL = TSL;
+  g->BR = P < TS ? P : TS;
+  g->lbr = ilog2(g->BR);
+  g->TP = (T + 7) / 8 * 8;
+  g->k = k;
+  return true;
+}
+
+// One kv head per unit, or more while a page's box stays under 16 KB: a
+// 16-row page of one head is a 4 KB copy, too small to keep enough bytes in
+// flight per SM.
+pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out) {
+  Geom best;
+  if (!geom_for(s, kind, 1, &best)) return PA_ERR_UNSUPPORTED;
+  const int e = kind == Kind::kFp8 ? 1 : 2;
+  for (int cand = 2; cand <= 4; cand *= 2) {
+    if ((long)best.BR * best.H2 * s->head_dim * e >= 16384) break;
+    Geom g;
+    if (!geom_for(s, kind, cand, &g)) break;
+    best = g;
+  }
+  *out = best;
+  return PA_OK;
 }
 
 // The launch plan of a call: mode, grid and workspace.
 struct Plan {
+  Geom geo;
   bool balanced = false;  // equal shares of the flattened pages, one CTA per SM
   int splits = 1;         // explicit mode
   int grid = 0;           // balanced mode CTAs
@@ -163,18 +221,21 @@ struct Plan {
 };
 
 pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d, Plan* plan) {
-  const SplitKernel k = pick_kernel(kind, s->head_dim, row_tiles(s));
-  if (!k.fn) return PA_ERR_UNSUPPORTED;
-  const int B = s->batch, T = s->q_tokens, Hq = s->num_q_heads, Hkv = s->num_kv_heads, D = s->head_dim;
-  const int M = (Hq / Hkv) * T;
+  Geom geo;
+  pa_status st = pick_geometry(s, kind, &geo);
+  if (st != PA_OK) return st;
+  const SplitKernel k = geo.k;
+  const int B = s->batch, T = s->q_tokens, Hq = s->num_q_heads, D = s->head_dim;
+  const int M = geo.M, units = B * geo.NHG;
   Plan p;
+  p.geo = geo;
   if (num_splits == 0) {
     const size_t smem = (size_t)k.smem_fixed + (size_t)(2 * B + 1) * 4;
     if (smem <= (size_t)d->smem_optin) {
       p.balanced = true;
       p.grid = d->sms;
       p.smem = smem;
-      const size_t slots = (size_t)B * Hkv + p.grid;
+      const size_t slots = (size_t)units + p.grid;
       p.part_lse_off = align256(slots * M * D * sizeof(float));
       p.ws_bytes = p.part_lse_off + align256(slots * M * sizeof(float));
       *plan = p;
@@ -182,7 +243,6 @@ pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d
     }
     // Too many sequences for the on-chip table: explicit splits that give
     // every SM about two CTAs.
-    const int units = B * Hkv;
     int S = (2 * d->sms + units - 1) / units;
     S = S < 1 ? 1 : (S > s->max_blocks_per_seq ? s->max_blocks_per_seq : S);
     num_splits = S;
@@ -255,7 +315,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   }
 
   const int B = s.batch, T = s.q_tokens, Hq = s.num_q_heads, Hkv = s.num_kv_heads, D = s.head_dim;
-  const int P = s.page_size, G = Hq / Hkv, M = G * T;
+  const int P = s.page_size, G = Hq / Hkv;
   const bool fp8 = a.kind == Kind::kFp8;
   const uint64_t e = fp8 ? 1 : 2;
 
@@ -268,22 +328,24 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     const uint32_t box[4] = {64u, (uint32_t)G, (uint32_t)T, 1u};
     if (!make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, dims, str, box)) return PA_ERR_INVALID_ARG;
   }
-  // KV caches as 5-D (128-byte column chunk, kv head, slot, chunk index,
-  // page): one box copies every chunk of up to 64 rows of one page and head,
-  // landing in shared memory as [chunk][row][128 B].
+  // KV caches as 5-D (128-byte column chunk, slot, kv head, chunk index,
+  // page): one box copies every chunk of BR rows of one page for the H2
+  // heads of a unit, landing in shared memory as [chunk][head][row][128 B].
+  const Geom& geo = plan.geo;
   const uint64_t nch = (uint64_t)D * e / 128;
   {
-    const uint64_t dims[5] = {128 / e, (uint64_t)Hkv, (uint64_t)P, nch, (uint64_t)s.num_pages};
-    const uint64_t str[4] = {(uint64_t)D * e, (uint64_t)Hkv * D * e, 128, (uint64_t)P * Hkv * D * e};
-    const uint32_t box[5] = {(uint32_t)(128 / e), 1u, (uint32_t)(P < pa::kTS ? P : pa::kTS), (uint32_t)nch, 1u};
+    const uint64_t dims[5] = {128 / e, (uint64_t)P, (uint64_t)Hkv, nch, (uint64_t)s.num_pages};
+    const uint64_t str[4] = {(uint64_t)Hkv * D * e, (uint64_t)D * e, 128, (uint64_t)P * Hkv * D * e};
+    const uint32_t box[5] = {(uint32_t)(128 / e), (uint32_t)geo.BR, (uint32_t)geo.H2, (uint32_t)nch, 1u};
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (!make_map(&p.tm_k, dt, a.k_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
     if (!make_map(&p.tm_v, dt, a.v_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
   }
   if (a.kind == Kind::kTidar) {
-    const uint64_t dims[5] = {64, (uint64_t)Hkv, (uint64_t)T, nch, (uint64_t)B};
-    const uint64_t str[4] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2, 128, (uint64_t)T * Hkv * D * 2};
-    const uint32_t box[5] = {64u, 1u, (uint32_t)T, (uint32_t)nch, 1u};
+    // Rows T..TP-1 of the box fall outside the tensor and read as zeros.
+    const uint64_t dims[5] = {64, (uint64_t)T, (uint64_t)Hkv, nch, (uint64_t)B};
+    const uint64_t str[4] = {(uint64_t)Hkv * D * 2, (uint64_t)D * 2, 128, (uint64_t)T * Hkv * D * 2};
+    const uint32_t box[5] = {64u, (uint32_t)geo.TP, (uint32_t)geo.H2, (uint32_t)nch, 1u};
     if (!make_map(&p.tm_ks, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k_scratch, dims, str, box) ||
         !make_map(&p.tm_vs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v_scratch, dims, str, box))
       return PA_ERR_INVALID_ARG;
@@ -300,8 +362,15 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = G;
-  p.M = M;
+  p.M = geo.M;
   p.P = P;
+  p.H2 = geo.H2;
+  p.NHG = geo.NHG;
+  p.GT = geo.GT;
+  p.TS = geo.TS;
+  p.BR = geo.BR;
+  p.lbr = geo.lbr;
+  p.TP = geo.TP;
   p.max_blocks = s.max_blocks_per_seq;
   p.num_pages = s.num_pages;
   p.num_splits = plan.balanced ? 0 : plan.splits;
@@ -313,9 +382,9 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     p.part_lse = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + plan.part_lse_off);
   }
 
-  const SplitKernel k = pick_kernel(a.kind, D, row_tiles(a.shape));
+  const SplitKernel k = geo.k;
   if ((st = ensure_smem_attr(d, k.fn)) != PA_OK) return st;
-  const dim3 grid = plan.balanced ? dim3(plan.grid) : dim3(B * Hkv, plan.splits);
+  const dim3 grid = plan.balanced ? dim3(plan.grid) : dim3(B * geo.NHG, plan.splits);
   void* args[] = {&p};
   if (ev_start && cudaEventRecord(ev_start, a.stream) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaLaunchKernel(k.fn, grid, dim3(pa::kThreads), args, plan.smem, a.stream) != cudaSuccess)
@@ -335,7 +404,10 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     r.Hq = Hq;
     r.Hkv = Hkv;
     r.G = G;
-    r.M = M;
+    r.M = geo.M;
+    r.H2 = geo.H2;
+    r.NHG = geo.NHG;
+    r.GT = geo.GT;
     r.D = D;
     r.P = P;
     r.max_blocks = s.max_blocks_per_seq;
@@ -355,7 +427,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     cfg.numAttrs = 1;
     cudaError_t err;
     if (plan.balanced) {
-      cfg.gridDim = dim3(B * Hkv);
+      cfg.gridDim = dim3(B * geo.NHG);
       err = cudaLaunchKernelEx(&cfg, pa::pa_reduce_balanced_kernel, r);
     } else {
       cfg.gridDim = dim3((unsigned)(((size_t)B * T * Hq + 3) / 4));

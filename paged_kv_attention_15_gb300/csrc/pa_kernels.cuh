@@ -1,11 +1,12 @@
 // Paged-KV decode attention kernels for sm_103a.
 //
-// The split kernel computes softmax attention of the M = G * T query rows
-// that share one kv head (head packing: the GQA group times the draft
-// tokens form the MMA M dimension) over a contiguous range of that
-// sequence's paged keys, FlashAttention style: online max and sum in base 2,
-// rescaled accumulator, and a log-sum-exp per row. The reduce kernel merges
-// split-K partials by their log-sum-exp.
+// The split kernel computes softmax attention of the query rows of H2
+// consecutive kv heads (head packing: the GQA group times the draft tokens,
+// times H2 kv heads, form the MMA M dimension) over a contiguous range of
+// one sequence's paged keys, FlashAttention style: online max and sum in
+// base 2, rescaled accumulator, and a log-sum-exp per row. A row only sees
+// the keys of its own kv head (block-diagonal mask). The reduce kernels
+// merge split-K partials by their log-sum-exp.
 // Sources: ROCm blog "Implementing a High-Performance Custom Diffusion
 // Attention Kernel with FlyDSL" (introduction items 1-3; "Match MFMA Operands
 // to the Desired Fragment Layout": the score fragment feeds the P x V
@@ -15,18 +16,21 @@
 // head-packed matrix-core decode with double-buffered loads, native fp8
 // e4m3fn KV with symmetric per-token scale, split-K partial combine).
 //
-// GB300 design. One CTA per SM (persistent) or per (sequence, kv head,
-// split). Warp 4 is the producer: it walks the block table and issues TMA
-// box copies of whole pages (K, V, and for fp8 the per-token scales) into
-// a ring of NS shared-memory stages of 64 tokens, each guarded by a pair of
-// mbarriers (full: bytes landed; empty: consumers done). Warps 0-3 consume:
+// GB300 design. One CTA per SM (persistent) or per (sequence, head group,
+// split). Warp 4 produces: it walks the block table and issues one TMA box
+// per page and stage (every column chunk of the page's rows of H2 kv heads;
+// for fp8 also the page's per-token scales by bulk copy) into a ring of NS
+// shared-memory stages of 64 key rows (64/H2 tokens x H2 heads), each
+// guarded by a pair of mbarriers (full: bytes landed; empty: consumers
+// done). H2 is chosen so a 16-row page still makes a large box: small
+// boxes cannot keep enough bytes in flight per SM. Warps 0-3 consume the
+// ring in order: warp w takes row tile w % MT and, inside it, one kv head
+// and one token slice of every stage, keeping its own online-softmax state.
 // QK^T and PV run as mma.sync m16n8k16 with fp32 accumulators; the score
 // fragment becomes the P operand in registers; K is read with ldmatrix and
-// V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). Stages
-// are consumed in order by all four consumer warps: warp w takes row tile
-// w % MT (MT = m16 tiles of query rows) and a token slice of every stage,
-// keeping its own online-softmax state; at the end of a work item the
-// slices merge through shared memory. Every wait is bounded in time, so a protocol error cannot hang
+// V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). At
+// the end of a work item the warps of a row tile merge through shared
+// memory. Every wait is bounded in time, so a protocol error cannot hang
 // the GPU.
 #pragma once
 
@@ -40,7 +44,7 @@ namespace pa {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kTS = 64;  // tokens per pipeline stage
+constexpr int kStageRows = 64;  // key rows per pipeline stage (tokens x heads)
 constexpr int kMaxHkvFp8 = 8;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -51,10 +55,10 @@ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 constexpr int clamp_int(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
 
 struct SplitParams {
-  CUtensorMap tm_q;   // q       (D, Hq, T, B)          box (64, G, T, 1)
-  CUtensorMap tm_k;   // k_cache (D, Hkv, P, num_pages) box (128 B, 1, min(P,64), 1)
+  CUtensorMap tm_q;   // q       (D, Hq, T, B)                      box (64, G, T, 1)
+  CUtensorMap tm_k;   // k_cache (128 B, slot, head, chunk, page)   box (128 B, BR, H2, NCH, 1)
   CUtensorMap tm_v;   // v_cache likewise
-  CUtensorMap tm_ks;  // k_scratch (D, Hkv, T, B)       box (64, 1, T, 1)
+  CUtensorMap tm_ks;  // k_scratch (64, t, head, chunk, b)          box (64, TP, H2, NCH, 1)
   CUtensorMap tm_vs;  // v_scratch likewise
   const int32_t* block_tables;
   const int32_t* context_lens;
@@ -66,6 +70,12 @@ struct SplitParams {
   float* part_lse;
   int* err_flags;
   int B, T, Hq, Hkv, G, M, P, max_blocks, num_pages;
+  int H2;          // kv heads per work unit
+  int NHG;         // head groups per sequence, Hkv / H2
+  int GT;          // query rows per kv head, G * T
+  int TS;          // tokens per stage, 64 / H2
+  int BR, lbr;     // rows of a page box, min(P, TS), and its log2
+  int TP;          // scratch rows per box: T rounded up to a multiple of 8
   int num_splits;  // >= 1: explicit splits (grid = units x splits); 0: balanced (grid = CTAs)
   int tidar;       // 1: each sequence also attends to its T scratch tokens
   int grid;        // CTAs of a balanced launch
@@ -79,24 +89,25 @@ struct ReduceParams {
   float* lse;
   const int32_t* context_lens;
   int B, T, Hq, Hkv, G, M, D, P, max_blocks, tidar;
+  int H2, NHG, GT;
   int num_splits;  // >= 1: explicit layout [B][T][Hq][S]; 0: balanced-launch slots
   int grid;        // CTAs of the balanced split launch
 };
 
-// Shared-memory plan of one kernel instance.
-template <int D, int MT, bool FP8>
+// Shared-memory plan of one kernel instance (TSL: tokens per warp slice).
+template <int D, int MT, bool FP8, int TSL>
 struct Cfg {
   static constexpr int ELEM = FP8 ? 1 : 2;
   static constexpr int CE = 128 / ELEM;         // elements per 128-byte row chunk
   static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
-  static constexpr int TILE = kTS * D * ELEM;   // bytes of the K (or V) tile of a stage
-  static constexpr int SCALE = FP8 ? kTS * kMaxHkvFp8 * 4 : 0;
+  static constexpr int TILE = kStageRows * D * ELEM;  // bytes of the K (or V) tile of a stage
+  static constexpr int SCALE = FP8 ? kStageRows * kMaxHkvFp8 * 4 : 0;
   static constexpr int STAGE = round_up(2 * TILE + 2 * SCALE, 1024);
   static constexpr int ROWS = 16 * MT;
   static constexpr int QCH = D / 64;
   static constexpr int QCHUNK = ROWS * 128;
   static constexpr int QSLOT = QCH * QCHUNK;
-  static constexpr int NGW = kConsumerWarps / MT;  // warp groups (each holds a partial result)
+  static constexpr int NGW = kConsumerWarps / MT;  // warps per row tile, each holding a partial result
   static constexpr int RSTR = D + 8;               // floats per row of the merge buffer
   static constexpr int RED = (NGW - 1) * ROWS * RSTR * 4;
   static constexpr int REDML = (NGW - 1) * ROWS * 2 * 4;
@@ -110,12 +121,13 @@ struct Cfg {
   static constexpr int OFF_PREFIX = OFF_BAR + BARS;
   static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1024 to align the dynamic base
   static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
-  static_assert(MT == 1 || MT == 2, "unsupported row tiles");
+  static_assert(MT == 1 || MT == 2 || MT == 4, "unsupported row tiles");
+  static_assert(TSL == 16 || TSL == 32, "unsupported warp slice");
 };
 
 // ----------------------------------------------------------------- schedule
 struct Item {
-  int b, g;
+  int b, hg;          // sequence and head group (kv heads hg*H2 .. hg*H2+H2-1)
   int tok0, tok_end;  // paged tokens [tok0, tok_end) of sequence b
   int scratch;        // 1: the T draft-block scratch tokens follow (last stage)
   int nst;            // pipeline stages
@@ -135,7 +147,7 @@ __device__ __forceinline__ int clamp_ctx(const SplitParams& p, int c) {
 __device__ __forceinline__ void cursor_init(const SplitParams& p, const int* s_start, Cursor& cur) {
   cur.done = 0;
   if (p.num_splits == 0) {
-    const long long N = (long long)p.Hkv * s_start[p.B];
+    const long long N = (long long)p.NHG * s_start[p.B];
     cur.f0 = N * blockIdx.x / p.grid;
     cur.f1 = N * (blockIdx.x + 1) / p.grid;
     cur.f = cur.f0;
@@ -143,6 +155,7 @@ __device__ __forceinline__ void cursor_init(const SplitParams& p, const int* s_s
 }
 
 // The next work item of this CTA; identical on every thread that calls it.
+// Units are (sequence b, head group hg), u = b * NHG + hg.
 __device__ __forceinline__ bool next_item(const SplitParams& p, const int* s_ctx, const int* s_start,
                                           Cursor& cur, Item& it) {
   const int P = p.P;
@@ -152,8 +165,8 @@ __device__ __forceinline__ bool next_item(const SplitParams& p, const int* s_ctx
     const int S = p.num_splits;
     const int s = blockIdx.y;
     const int u = blockIdx.x;
-    it.b = u / p.Hkv;
-    it.g = u % p.Hkv;
+    it.b = u / p.NHG;
+    it.hg = u % p.NHG;
     const int ctx = clamp_ctx(p, __ldg(p.context_lens + it.b));
     const int n = (ctx + P - 1) / P;
     const int pps = (n + S - 1) / S;
@@ -166,17 +179,17 @@ __device__ __forceinline__ bool next_item(const SplitParams& p, const int* s_ctx
   } else {
     if (cur.f >= cur.f1) return false;
     const long long f = cur.f;
-    const int Hkv = p.Hkv;
-    int lo = 0, hi = p.B - 1;  // largest b with Hkv * start[b] <= f (a non-empty sequence)
+    const int NHG = p.NHG;
+    int lo = 0, hi = p.B - 1;  // largest b with NHG * start[b] <= f (a non-empty sequence)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if ((long long)Hkv * s_start[mid] <= f) lo = mid; else hi = mid - 1;
+      if ((long long)NHG * s_start[mid] <= f) lo = mid; else hi = mid - 1;
     }
     const int b = lo;
     const int nv = s_start[b + 1] - s_start[b];
-    const long long ub = (long long)Hkv * s_start[b];
-    const int g = (int)((f - ub) / nv);
-    const long long us = ub + (long long)g * nv;
+    const long long ub = (long long)NHG * s_start[b];
+    const int hg = (int)((f - ub) / nv);
+    const long long us = ub + (long long)hg * nv;
     const long long ue = us + nv;
     const long long end = ue < cur.f1 ? ue : cur.f1;
     const int vp0 = (int)(f - us);
@@ -184,31 +197,21 @@ __device__ __forceinline__ bool next_item(const SplitParams& p, const int* s_ctx
     const int ctx = s_ctx[b];
     const int n = (ctx + P - 1) / P;
     it.b = b;
-    it.g = g;
+    it.hg = hg;
     it.tok0 = vp0 * P;
     it.tok_end = max(it.tok0, min(min(vp1, n) * P, ctx));
     it.scratch = (p.tidar && vp1 == nv) ? 1 : 0;  // the scratch is the unit's last virtual page
-    it.part = (us >= cur.f0 && ue <= cur.f1) ? -1 : (b * Hkv + g + (int)blockIdx.x);
+    it.part = (us >= cur.f0 && ue <= cur.f1) ? -1 : (b * NHG + hg + (int)blockIdx.x);
     cur.f = end;
   }
-  it.nst = (it.tok_end - it.tok0 + kTS - 1) / kTS + it.scratch;
+  it.nst = (it.tok_end - it.tok0 + p.TS - 1) / p.TS + it.scratch;
   return true;
 }
 
-// Swizzled byte offset of 16-byte unit `unit` in row `row` of a 128-byte-row tile.
+// Swizzled byte offset of 16-byte unit `unit` in row `row` of a 128-byte-row
+// tile whose base is 1024-byte aligned.
 __device__ __forceinline__ uint32_t swz(int row, int unit) {
   return (uint32_t)(row * 128 + (((unit) ^ (row & 7)) << 4));
-}
-
-// Byte offset, in a stage tile laid out [box][chunk][box row][128 B] with
-// br rows per box (NCH chunks), of 16-byte unit `unit` of column chunk
-// `chunk` of token `tok`. The 128-byte swizzle XORs the unit with bits
-// 7..9 of the row's offset (tiles are 1024-byte aligned).
-template <int NCH>
-__device__ __forceinline__ uint32_t kv_unit_impl(int tok, int chunk, int unit, int br) {
-  const int box = tok / br, rr = tok - box * br;
-  const uint32_t row = (uint32_t)(((box * NCH + chunk) * br + rr) * 128);
-  return row + ((uint32_t)(unit ^ ((row >> 7) & 7)) << 4);
 }
 
 // Waits (bounded, ignoring the abort flag) for the last fill of every ring
@@ -231,15 +234,14 @@ __device__ __forceinline__ void raise_abort(volatile int* s_abort, int* err_flag
 }
 
 // ------------------------------------------------------------ split kernel
-template <int D, int MT, bool FP8>
+template <int D, int MT, bool FP8, int TSL>
 __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_constant__ SplitParams p) {
-  using C = Cfg<D, MT, FP8>;
+  using C = Cfg<D, MT, FP8, TSL>;
   constexpr int NS = C::NS;
-  constexpr int NGW = C::NGW;          // token groups, each holding a partial result
-  constexpr int TSL = kTS / NGW;       // tokens of a stage per warp
-  constexpr int NTS = TSL / 8;         // n8 tiles of a warp's slice
-  constexpr int NT8 = D / 8;           // n8 tiles of the output row
-  auto kv_unit = [](int tok, int chunk, int unit, int br) { return kv_unit_impl<C::NCH>(tok, chunk, unit, br); };
+  constexpr int NGW = C::NGW;
+  constexpr int NCH = C::NCH;
+  constexpr int NTS = TSL / 8;  // n8 tiles of a warp's slice
+  constexpr int NT8 = D / 8;    // n8 tiles of the output row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -297,6 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   __syncthreads();
 
   const int P = p.P;
+  const int H2 = p.H2;
+  const int TS = p.TS;
+  // Bytes per key row of all H2 heads (+ their fp8 scales) in a stage.
+  const uint32_t row_bytes = H2 * D * C::ELEM + (FP8 ? p.Hkv * 4 : 0);
   if (warp == kConsumerWarps) {
     // ================================================================ producer
     const uint64_t pol_kv = l2_policy_evict_first();
@@ -318,11 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       if (qn >= 2) ok = mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort);
       if (!ok) break;
       if (lane == 0) {
+        // Rows of kv head hl occupy rows [hl*GT, (hl+1)*GT) of each chunk.
         const uint32_t qdst = sbase + C::OFF_Q + qs * C::QSLOT;
         mbar_arrive_expect_tx(bar_qfull + 8 * qs, C::QCH * p.M * 128);
+        for (int hl = 0; hl < H2; ++hl)
 #pragma unroll
-        for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(qdst + c * C::QCHUNK, &p.tm_q, bar_qfull + 8 * qs, c * 64, it.g * p.G, 0, it.b, pol_q);
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_4d(qdst + c * C::QCHUNK + hl * p.GT * 128, &p.tm_q, bar_qfull + 8 * qs, c * 64,
+                        (it.hg * H2 + hl) * p.G, 0, it.b, pol_q);
       }
       ++qn;
 
@@ -346,31 +355,30 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         const uint32_t ksd = kdst + 2 * C::TILE;
         const uint32_t vsd = ksd + C::SCALE;
         if (it.scratch && j == it.nst - 1) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(full, 2 * C::NCH * p.T * 128);
-            tma_load_5d(kdst, &p.tm_ks, full, 0, it.g, 0, 0, it.b, pol_kv);
-            tma_load_5d(vdst, &p.tm_vs, full, 0, it.g, 0, 0, it.b, pol_kv);
+          if (lane == 0) {  // rows T..TP-1 of the box are outside the tensor: zero filled
+            mbar_arrive_expect_tx(full, 2 * NCH * H2 * p.TP * 128);
+            tma_load_5d(kdst, &p.tm_ks, full, 0, 0, it.hg * H2, 0, it.b, pol_kv);
+            tma_load_5d(vdst, &p.tm_vs, full, 0, 0, it.hg * H2, 0, it.b, pol_kv);
           }
           continue;
         }
-        const int t_first = it.tok0 + j * kTS;
-        const int valid = min(kTS, it.tok_end - t_first);
+        const int t_first = it.tok0 + j * TS;
+        const int valid = min(TS, it.tok_end - t_first);
         const int pidx0 = t_first / P - pbase;  // page of the stage, relative to the item
         while (pidx0 >= ibase + 32) {           // advance the block-table window
           ibase += 32;
           ids = ids_next;
           ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
         }
-        if (P < kTS) {
+        if (P < TS) {  // whole pages: one box each
           const int npg = (valid + P - 1) / P;
-          if (lane == 0)
-            mbar_arrive_expect_tx(full, 2 * npg * P * (C::NCH * 128 + (FP8 ? p.Hkv * 4 : 0)));
+          if (lane == 0) mbar_arrive_expect_tx(full, 2 * npg * P * row_bytes);
           for (int i = 0; i < npg; ++i) {
             const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase + i);
             if (lane == 0) {
-              // one box per page: every column chunk of its P rows
-              tma_load_5d(kdst + i * C::NCH * P * 128, &p.tm_k, full, 0, it.g, 0, 0, page, pol_kv);
-              tma_load_5d(vdst + i * C::NCH * P * 128, &p.tm_v, full, 0, it.g, 0, 0, page, pol_kv);
+              const uint32_t boff = i * NCH * H2 * P * 128;
+              tma_load_5d(kdst + boff, &p.tm_k, full, 0, 0, it.hg * H2, 0, page, pol_kv);
+              tma_load_5d(vdst + boff, &p.tm_v, full, 0, 0, it.hg * H2, 0, page, pol_kv);
               if (FP8) {
                 const uint32_t sb = P * p.Hkv * 4;
                 const size_t off = (size_t)page * P * p.Hkv;
@@ -379,15 +387,15 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               }
             }
           }
-        } else {
+        } else {  // TS rows of one page
           const int row0 = t_first % P;
           const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase);
           if (lane == 0) {
-            mbar_arrive_expect_tx(full, 2 * kTS * (C::NCH * 128 + (FP8 ? p.Hkv * 4 : 0)));
-            tma_load_5d(kdst, &p.tm_k, full, 0, it.g, row0, 0, page, pol_kv);
-            tma_load_5d(vdst, &p.tm_v, full, 0, it.g, row0, 0, page, pol_kv);
+            mbar_arrive_expect_tx(full, 2 * TS * row_bytes);
+            tma_load_5d(kdst, &p.tm_k, full, 0, row0, it.hg * H2, 0, page, pol_kv);
+            tma_load_5d(vdst, &p.tm_v, full, 0, row0, it.hg * H2, 0, page, pol_kv);
             if (FP8) {
-              const uint32_t sb = kTS * p.Hkv * 4;
+              const uint32_t sb = TS * p.Hkv * 4;
               const size_t off = ((size_t)page * P + row0) * p.Hkv;
               bulk_load(ksd, p.k_scale + off, sb, full, pol_kv);
               bulk_load(vsd, p.v_scale + off, sb, full, pol_kv);
@@ -406,13 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   }
 
   // ================================================================ consumers
-  // Warp w owns row tile mt = w % MT and the token slice tg = w / MT of every
-  // stage (TSL tokens); all consumer warps read every stage, so the ring is
-  // consumed strictly in order and NS - 1 stages stay in flight.
+  // Warp w: row tile mt = w % MT; among the NGW warps of that tile, gi picks
+  // the kv head hl (when a tile holds several heads' rows) and the token
+  // slice ts of every stage (TSL tokens).
+  const int GT = p.GT;
   const int mt = warp % MT;
-  const int tg = warp / MT;
+  const int gi = warp / MT;
+  const int hl_base = (mt * 16) / GT;
+  const int ht = GT >= 16 ? 1 : min(16 / GT, H2 - hl_base);
+  const int hl = hl_base + gi % ht;
+  const int ts = gi / ht;
   const int r = lane >> 2;
   const int c4 = lane & 3;
+  const int rho0 = mt * 16 + r, rho1 = rho0 + 8;
+  const bool rok0 = rho0 < p.M && rho0 / GT == hl;  // rows this warp computes
+  const bool rok1 = rho1 < p.M && rho1 / GT == hl;
   const float NEG_INF = -__int_as_float(0x7f800000);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* redml = reinterpret_cast<float*>(smem + C::OFF_REDML);
@@ -426,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
 
   while (next_item(p, s_ctx, s_start, cur, it)) {
     float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+    const int g = it.hg * H2 + hl;  // this warp's kv head
 
     if (it.nst > 0) {
       const int qs = qn & 1;
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         // d = 16 s + 4 c4 .. +3. The fragments of k-steps 4q..4q+3 of row
         // tile mt take exactly the 2 KB that the tile's rows occupy in
         // column chunk q, so each chunk is converted by its own warp.
-        if (tg == 0) {
+        if (gi == 0) {
           uint8_t* qs_ptr = smem + C::OFF_Q + qs * C::QSLOT;
           uint4* dst = reinterpret_cast<uint4*>(qs_ptr);
 #pragma unroll
@@ -479,16 +496,26 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
         const bool scr = it.scratch && j == it.nst - 1;
-        const int valid = scr ? p.T : min(kTS, it.tok_end - (it.tok0 + j * kTS));
-        const int tb = tg * TSL;  // first token of this warp's slice
+        const int valid = scr ? p.T : min(TS, it.tok_end - (it.tok0 + j * TS));
+        const int tb = ts * TSL;  // first token of this warp's slice
         if (ok && tb < valid) {
-          // A stage tile is [box][chunk][box row][128 B]; a box holds br rows
-          // (the page, or 64 rows of a large page, or the T scratch rows).
-          const int br = scr ? p.T : (P < kTS ? P : kTS);
+          // Stage tile: [box][chunk][head][box row][128 B]; a box holds the
+          // rows of one page (scratch: TP rows). Every token index used below
+          // is a multiple of 8 plus (lane & 7), so the 128-byte swizzle of its
+          // row is (lane & 7) and only the row base depends on the token.
+          const int lbt = scr ? 6 : p.lbr;
+          const int brows = scr ? p.TP : p.BR;
+          const uint32_t box_bytes = (uint32_t)(NCH * H2 * brows * 128);
+          const uint32_t cstride = (uint32_t)(H2 * brows * 128);
+          const uint32_t hoff = (uint32_t)(hl * brows * 128);
+          auto row_base = [&](int tok) -> uint32_t {
+            return (uint32_t)(tok >> lbt) * box_bytes + (uint32_t)(tok & ((1 << lbt) - 1)) * 128u + hoff;
+          };
           const uint32_t kb_ = sbase + slot * C::STAGE;
           const uint32_t vb_ = kb_ + C::TILE;
           const float* ksc = reinterpret_cast<const float*>(smem + slot * C::STAGE + 2 * C::TILE);
           const float* vsc = ksc + C::SCALE / 4;
+          const int sw = lane & 7;
 
           // ---- S = Q K^T: 16 rows x TSL tokens. Two accumulators per tile
           // (even and odd k-steps) halve the dependent MMA chain.
@@ -499,6 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
             s2[i][0] = s2[i][1] = s2[i][2] = s2[i][3] = 0.f;
           }
           if (!FP8) {
+            uint32_t krow[NTS / 2];
+#pragma unroll
+            for (int nb = 0; nb < NTS / 2; ++nb) krow[nb] = kb_ + row_base(tb + nb * 16 + (lane >> 4) * 8 + sw);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               uint32_t qa[4];
@@ -507,17 +537,20 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 const int d = kk * 16 + (lane >> 4) * 8;
                 ldsm_x4(qbase + (d / 64) * C::QCHUNK + swz(row, (d % 64) / 8), qa[0], qa[1], qa[2], qa[3]);
               }
+              const int unit = ((kk * 16) % 64) / 8 + ((lane >> 3) & 1);
+              const uint32_t coff = (kk / 4) * cstride + ((unit ^ sw) << 4);
 #pragma unroll
               for (int nb = 0; nb < NTS / 2; ++nb) {
-                const int tok = tb + nb * 16 + (lane >> 4) * 8 + (lane & 7);
-                const int d = kk * 16 + ((lane >> 3) & 1) * 8;
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb_ + kv_unit(tok, d / 64, (d % 64) / 8, br), b0, b1, b2, b3);
+                ldsm_x4(krow[nb] + coff, b0, b1, b2, b3);
                 mma_bf16((kk & 1) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
                 mma_bf16((kk & 1) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
               }
             }
           } else {
+            uint32_t krow[NTS];
+#pragma unroll
+            for (int nt = 0; nt < NTS; ++nt) krow[nt] = kb_ + row_base(tb + nt * 8 + sw);
             const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
 #pragma unroll
             for (int kq = 0; kq < D / 64; ++kq) {
@@ -527,19 +560,18 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
                 qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
               }
+              const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
+              const uint32_t coff = (unit / 8) * cstride + (((unit % 8) ^ sw) << 4);
 #pragma unroll
               for (int nt = 0; nt < NTS; ++nt) {
-                const int tok = tb + nt * 8 + (lane & 7);
-                const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
                 uint32_t kr[4];
-                ldsm_x4(kb_ + kv_unit(tok, unit / 8, unit % 8, br), kr[0], kr[1], kr[2], kr[3]);
+                ldsm_x4(krow[nt] + coff, kr[0], kr[1], kr[2], kr[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                   mma_f16((e & 1) ? s2[nt] : s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
               }
             }
           }
-
 #pragma unroll
           for (int i = 0; i < NTS; ++i) {
             s[i][0] += s2[i][0];
@@ -556,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
             for (int e = 0; e < 4; ++e) {
               const int tok = tb + i * 8 + 2 * c4 + (e & 1);
               float f = s[i][e] * sl;
-              if (FP8) f *= ksc[tok * p.Hkv + it.g];
-              s[i][e] = tok < valid ? f : NEG_INF;
+              if (FP8) f *= ksc[tok * p.Hkv + g];
+              s[i][e] = (tok < valid && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
             }
           }
           float mx0 = NEG_INF, mx1 = NEG_INF;
@@ -573,7 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
           const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
           const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
-          const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+          // alpha = 1 exactly when the running max did not move (also for
+          // rows this warp does not compute, which stay at -inf).
+          const float al0 = mn0 == m0 ? 1.f : ex2(m0 - mu0);
+          const float al1 = mn1 == m1 ? 1.f : ex2(m1 - mu1);
           m0 = mn0;
           m1 = mn1;
           float ls0 = 0.f, ls1 = 0.f;
@@ -610,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
               vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
             }
+            const uint32_t vrow = vb_ + row_base(tb + kb * 16 + ((lane >> 3) & 1) * 8 + sw);
             uint32_t pa[4];
             if (!FP8) {
               pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
@@ -618,10 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
 #pragma unroll
               for (int nd = 0; nd < D / 16; ++nd) {
-                const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int d = nd * 16 + (lane >> 4) * 8;
+                const int unit = ((nd * 16) % 64) / 8 + (lane >> 4);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vb_ + kv_unit(tok, d / 64, (d % 64) / 8, br), b0, b1, b2, b3);
+                ldsm_x4_trans(vrow + (nd / 4) * cstride + ((unit ^ sw) << 4), b0, b1, b2, b3);
                 if (partial) {
                   b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
                 }
@@ -631,20 +666,19 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
             } else {
               // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
               float vs[4];
-              vs[0] = t0 < valid ? vsc[t0 * p.Hkv + it.g] : 0.f;
-              vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + it.g] : 0.f;
-              vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + it.g] : 0.f;
-              vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + it.g] : 0.f;
+              vs[0] = t0 < valid ? vsc[t0 * p.Hkv + g] : 0.f;
+              vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + g] : 0.f;
+              vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + g] : 0.f;
+              vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + g] : 0.f;
               pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
               pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
               pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
               pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
 #pragma unroll
               for (int uu = 0; uu < D / 32; ++uu) {
-                const int tok = tb + kb * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
                 const int unit = 2 * uu + (lane >> 4);
                 uint32_t R[4];
-                ldsm_x4_trans(vb_ + kv_unit(tok, unit / 8, unit % 8, br), R[0], R[1], R[2], R[3]);
+                ldsm_x4_trans(vrow + (unit / 8) * cstride + (((unit % 8) ^ sw) << 4), R[0], R[1], R[2], R[3]);
                 if (partial) {
                   R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
                 }
@@ -674,23 +708,22 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
 
-    // ---- merge the NGW warp groups' partial results, then write
+    // ---- merge the NGW warps of each row tile, then write
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const int rho0 = mt * 16 + r, rho1 = rho0 + 8;
     if (NGW > 1) {
       named_barrier_sync(1, 32 * kConsumerWarps);
-      if (tg > 0) {
-        float* rb = red + (size_t)(tg - 1) * C::ROWS * C::RSTR;
+      if (gi > 0) {
+        float* rb = red + (size_t)(gi - 1) * C::ROWS * C::RSTR;
 #pragma unroll
         for (int i = 0; i < NT8; ++i) {
           *reinterpret_cast<float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][0], acc[i][1]);
           *reinterpret_cast<float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][2], acc[i][3]);
         }
         if (c4 == 0) {
-          float* ml = redml + (size_t)(tg - 1) * C::ROWS * 2;
+          float* ml = redml + (size_t)(gi - 1) * C::ROWS * 2;
           ml[2 * rho0] = m0;
           ml[2 * rho0 + 1] = l0;
           ml[2 * rho1] = m1;
@@ -699,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       }
       named_barrier_sync(1, 32 * kConsumerWarps);
     }
-    if (tg != 0) continue;
+    if (gi != 0) continue;
 
     float M0 = m0, M1 = m1;
 #pragma unroll
@@ -746,8 +779,10 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     for (int h2 = 0; h2 < 2; ++h2) {
       const int rho = h2 ? rho1 : rho0;
       if (rho >= p.M) continue;
-      const int t = rho / p.G;
-      const int h = it.g * p.G + rho % p.G;
+      // row rho = hl * GT + t * G + j  ->  query head (hg * H2 + hl) * G + j
+      const int rhl = rho / GT, rem = rho - rhl * GT;
+      const int t = rem / p.G;
+      const int h = (it.hg * H2 + rhl) * p.G + (rem - t * p.G);
       const size_t row = ((size_t)it.b * p.T + t) * p.Hq + h;
       const float lsev = h2 ? lse1 : lse0;
       if (it.part < 0) {

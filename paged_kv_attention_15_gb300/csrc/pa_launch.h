@@ -13,8 +13,9 @@ struct SplitKernel {
   int stages;       // pipeline depth of the instance
 };
 
-// Kernel instance for (head_dim, row tiles, fp8); fn == nullptr if not built.
-SplitKernel split_kernel_bf16(int head_dim, int row_tiles);
-SplitKernel split_kernel_fp8(int head_dim, int row_tiles);
+// Kernel instance for (head_dim, row tiles, tokens per warp slice);
+// fn == nullptr if that combination is not built.
+SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice);
+SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice);
 
 }  // namespace pa

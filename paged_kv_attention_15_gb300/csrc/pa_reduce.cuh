@@ -45,6 +45,13 @@ __device__ __forceinline__ void reduce_row(const ReduceParams& p, size_t row, co
   if (lane == 0 && p.lse) p.lse[row] = (mx + lg2(L) * kLn2);
 }
 
+// Output row of row rho of unit (b, hg) in [B, T, Hq].
+__device__ __forceinline__ size_t unit_row(const ReduceParams& p, int b, int hg, int rho) {
+  const int hl = rho / p.GT, rem = rho - hl * p.GT;
+  const int t = rem / p.G;
+  return ((size_t)b * p.T + t) * p.Hq + (size_t)(hg * p.H2 + hl) * p.G + (rem - t * p.G);
+}
+
 // Explicit splits: grid covers B*T*Hq rows, 4 rows (warps) per CTA.
 __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_constant__ ReduceParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -56,13 +63,14 @@ __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_cons
   reduce_row(p, row, p.part_o + base * p.D, p.part_lse + base, 1, p.num_splits, lane);
 }
 
-// Balanced launch: one CTA per (sequence, kv head) unit; combines the
-// pieces that the split CTAs wrote to slots unit + cta.
+// Balanced launch: one CTA per (sequence, head group) unit; combines the
+// pieces that the split CTAs wrote to slots unit + cta. Row rho of a unit is
+// query token t = (rho % GT) / G of head (hg * H2 + rho / GT) * G + rho % G.
 __global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_constant__ ReduceParams p) {
   __shared__ long long s_sum[2][4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
-  const int b = u / p.Hkv, g = u % p.Hkv;
+  const int b = u / p.NHG, hg = u % p.NHG;
   const int cap = p.max_blocks * p.P;
   long long before = 0, total = 0;
   for (int i = threadIdx.x; i < p.B; i += 128) {
@@ -87,13 +95,13 @@ __global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_co
   int cb = __ldg(p.context_lens + b);
   cb = cb < 0 ? 0 : (cb > cap ? cap : cb);
   const long long nvb = (cb + p.P - 1) / p.P + p.tidar;
-  const long long N = total * p.Hkv;
-  const long long us = before * p.Hkv + (long long)g * nvb;
+  const long long N = total * p.NHG;
+  const long long us = before * p.NHG + (long long)hg * nvb;
   const long long ue = us + nvb;
   const float NEG_INF = -__int_as_float(0x7f800000);
   if (nvb == 0) {  // no keys at all: out = 0, lse = -inf
     for (int rho = warp; rho < p.M; rho += 4) {
-      const size_t row = ((size_t)b * p.T + rho / p.G) * p.Hq + g * p.G + rho % p.G;
+      const size_t row = unit_row(p, b, hg, rho);
       for (int d = lane * 4; d < p.D; d += 128) *reinterpret_cast<uint2*>(p.out + row * p.D + d) = make_uint2(0u, 0u);
       if (lane == 0 && p.lse) p.lse[row] = NEG_INF;
     }
@@ -106,7 +114,7 @@ __global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_co
   if (i0 == i1) return;  // one piece: the split kernel wrote the final rows
   // Pieces are the CTAs i0..i1 whose share is non-empty; slot = u + i.
   for (int rho = warp; rho < p.M; rho += 4) {
-    const size_t row = ((size_t)b * p.T + rho / p.G) * p.Hq + g * p.G + rho % p.G;
+    const size_t row = unit_row(p, b, hg, rho);
     float mx = NEG_INF;
     for (int i = i0 + lane; i <= i1; i += 32) {
       const bool nonempty = (N * i / G64) < (N * (i + 1) / G64);
