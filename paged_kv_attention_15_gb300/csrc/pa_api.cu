@@ -427,7 +427,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     cfg.numAttrs = 1;
     cudaError_t err;
     if (plan.balanced) {
-      cfg.gridDim = dim3(B * geo.NHG);
+      cfg.gridDim = dim3(B * geo.NHG, (geo.M + 3) / 4);
       err = cudaLaunchKernelEx(&cfg, pa::pa_reduce_balanced_kernel, r);
     } else {
       cfg.gridDim = dim3((unsigned)(((size_t)B * T * Hq + 3) / 4));

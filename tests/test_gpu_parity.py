@@ -91,6 +91,11 @@ SWEEP = [
     dict(q_tokens=3, num_q_heads=10, num_kv_heads=2),           # 15 rows, odd group
     dict(context_lens=(0, 37, 0, 500)),                         # empty sequences
     dict(batch=9, ctx_range=(1, 700), context_lens=None, pool_pages=400),
+    # head-group units: 4 kv heads x 8 rows in two row tiles; 4 x 16 rows in
+    # four row tiles; 4 x (2 tokens x 2 heads) in one tile
+    dict(num_q_heads=32, num_kv_heads=4),
+    dict(num_q_heads=64, num_kv_heads=4),
+    dict(q_tokens=2, num_q_heads=8, num_kv_heads=4),
 ]
 
 
