@@ -220,42 +220,59 @@ def aggregate_throughput(bytes_per_step: int, steps: int, max_elapsed_s: float, 
 
 
 # --------------------------------------------------------------------------- oracle timing
-def oracle_sample_run(inp, budget_s: float, start_unit: int = 0):
+def _oracle_bits(inp):
+    import oracle
+
+    return oracle.as_oracle_inputs(inp.numpy_bits(), inp.spec.kv_format)
+
+
+def _unit_rows(spec, b, g):
+    return [(b, t, h) for t in range(spec.q_tokens) for h in range(g * spec.group, (g + 1) * spec.group)]
+
+
+def oracle_seconds_per_key(inp) -> float:
+    """Oracle time per key of one (sequence, kv head) unit, from a prefix of
+    up to 4096 keys of the first unit."""
+    import oracle
+
+    spec = inp.spec
+    bits = _oracle_bits(inp)
+    trial = dict(bits)
+    trial["context_lens"] = bits["context_lens"].copy()
+    probe = int(min(int(trial["context_lens"][0]), 4096))
+    trial["context_lens"][0] = max(probe, 1)
+    t = time.perf_counter()
+    oracle.decode(trial, spec.scale, rows=_unit_rows(spec, 0, 0))
+    return max((time.perf_counter() - t) / max(probe, 1), 1e-9)
+
+
+def oracle_sample_run(inp, budget_s: float, start_unit: int = 0, per_key: float = None):
     """Runs the oracle, as it stands, on whole (sequence, kv head) units (a
     context prefix for the first unit when one unit alone exceeds the
     budget). Returns (seconds, algorithmic bytes, description)."""
     import oracle
 
     spec = inp.spec
-    bits = oracle.as_oracle_inputs(inp.numpy_bits(), spec.kv_format)
+    bits = _oracle_bits(inp)
     ctx = bits["context_lens"].astype(np.int64)
     units = [(b, g) for b in range(spec.batch) for g in range(spec.num_kv_heads)]
-    rows_of = lambda b, g: [(b, t, h) for t in range(spec.q_tokens)
-                            for h in range(g * spec.group, (g + 1) * spec.group)]
-    # calibrate on a prefix of the first unit
-    b0, g0 = units[start_unit % len(units)]
-    probe = min(int(ctx[b0]), 4096)
-    trial = dict(bits)
-    trial["context_lens"] = bits["context_lens"].copy()
-    trial["context_lens"][b0] = probe
-    t = time.perf_counter()
-    oracle.decode(trial, spec.scale, rows=rows_of(b0, g0))
-    per_token = max((time.perf_counter() - t) / max(probe, 1), 1e-9)
+    if per_key is None:
+        per_key = oracle_seconds_per_key(inp)
     done_s, done_bytes, n_units, prefix = 0.0, 0, 0, None
     i = start_unit
     while done_s < budget_s and n_units < len(units):
         b, g = units[i % len(units)]
         c = int(ctx[b])
         run = dict(bits)
-        if per_token * c > budget_s - done_s and n_units == 0:
-            c = max(1, int((budget_s - done_s) / per_token))
+        if per_key * c > budget_s - done_s and n_units == 0:
+            c = max(1, int((budget_s - done_s) / per_key))
             run["context_lens"] = bits["context_lens"].copy()
             run["context_lens"][b] = c
             prefix = c
-        elif per_token * c > 2 * (budget_s - done_s) and n_units > 0:
+        elif per_key * c > 2 * (budget_s - done_s) and n_units > 0:
             break
         t = time.perf_counter()
-        oracle.decode(run, spec.scale, rows=rows_of(b, g))
+        oracle.decode(run, spec.scale, rows=_unit_rows(spec, b, g))
         done_s += time.perf_counter() - t
         done_bytes += unit_bytes(spec, c)
         n_units += 1
@@ -440,12 +457,13 @@ def run_reference(args):
     spec = workload_spec(args)
     host = gen.make_inputs(spec)
     budget = max(0.002, args.reference_seconds / (args.steps + args.warmup))
+    per_key = oracle_seconds_per_key(host)
     for w in range(args.warmup):
-        oracle_sample_run(host, budget, start_unit=w)
+        oracle_sample_run(host, budget, start_unit=w, per_key=per_key)
     secs, nbytes, desc = 0.0, 0, None
     t0 = time.perf_counter()
     for i in range(args.steps):
-        s, b, d = oracle_sample_run(host, budget, start_unit=args.warmup + i)
+        s, b, d = oracle_sample_run(host, budget, start_unit=args.warmup + i, per_key=per_key)
         secs += s
         nbytes += b
         desc = desc or d

@@ -1,0 +1,53 @@
+"""Host-side pieces of bench.py: the algorithmic byte count (the GB/s
+numerator) and the reference arm's JSON line (the oracle on host cores)."""
+
+import io
+import json
+from contextlib import redirect_stdout
+
+import bench
+from paged_kv_attention_15_gb300 import inputs as gen
+
+
+def test_algorithmic_bytes_by_hand():
+    spec = gen.custom_spec(batch=2, q_tokens=1, num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=16,
+                           context_lens=(37, 100), seed=1)
+    inp = gen.make_inputs(spec)
+    kv = 2 * (37 + 100) * 2 * 64 * 2          # K and V rows of valid tokens, 2 kv heads, bf16
+    table = (3 + 7) * 4                        # block-table entries in use
+    rows = 2 * 1 * 4
+    qo = rows * 64 * 2 * 2 + rows * 4 + 2 * 4  # q, out, lse, context_lens
+    assert bench.algorithmic_bytes(inp) == kv + table + qo
+
+
+def test_algorithmic_bytes_fp8_and_scratch():
+    spec = gen.custom_spec(batch=1, q_tokens=2, num_q_heads=2, num_kv_heads=1, head_dim=128, page_size=16,
+                           context_lens=(20,), kv_format="fp8", seed=1)
+    inp = gen.make_inputs(spec)
+    expect = 2 * 20 * 128 * 1 + 2 * 20 * 4 + 2 * 4 + (4 * 128 * 2 * 2 + 4 * 4 + 4)
+    assert bench.algorithmic_bytes(inp) == expect
+    spec = gen.custom_spec(batch=1, q_tokens=2, num_q_heads=2, num_kv_heads=1, head_dim=64, page_size=16,
+                           context_lens=(20,), draft_scratch=True, seed=1)
+    inp = gen.make_inputs(spec)
+    expect = 2 * 20 * 64 * 2 + 2 * 4 + (4 * 64 * 2 * 2 + 4 * 4 + 4) + 2 * 2 * 64 * 2
+    assert bench.algorithmic_bytes(inp) == expect
+
+
+def test_unit_bytes_sum_to_call_bytes():
+    spec = gen.SPECS["tiny"]
+    inp = gen.make_inputs(spec)
+    total = sum(bench.unit_bytes(spec, int(c)) for c in inp.context_lens for _ in range(spec.num_kv_heads))
+    assert total + spec.batch * 4 == bench.algorithmic_bytes(inp)
+
+
+def test_reference_arm_prints_the_contract_line():
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "3",
+                         "--reference-seconds", "0.5"])
+    assert rc == 0
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["metric"] == bench.METRIC and line["steps"] == 2 and line["warmup"] == 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
