@@ -143,15 +143,8 @@ pa_status check_shape(const pa_shape* s, Kind kind) {
   return PA_OK;
 }
 
-// Prefers the head-dim-split instance (twice the consumer warps) where one
-// is built.
 SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL) {
-  for (int ds = 2; ds >= 1; --ds) {
-    const SplitKernel k = kind == Kind::kFp8 ? pa::split_kernel_fp8(D, MT, TSL, ds)
-                                             : pa::split_kernel_bf16(D, MT, TSL, ds);
-    if (k.fn) return k;
-  }
-  return SplitKernel{nullptr, 0, 0, 0};
+  return kind == Kind::kFp8 ? pa::split_kernel_fp8(D, MT, TSL) : pa::split_kernel_bf16(D, MT, TSL);
 }
 
 // Work-unit geometry: H2 kv heads per CTA unit, their M = H2 * G * T query
@@ -394,7 +387,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   const dim3 grid = plan.balanced ? dim3(plan.grid) : dim3(B * geo.NHG, plan.splits);
   void* args[] = {&p};
   if (ev_start && cudaEventRecord(ev_start, a.stream) != cudaSuccess) return PA_ERR_CUDA;
-  if (cudaLaunchKernel(k.fn, grid, dim3(k.threads), args, plan.smem, a.stream) != cudaSuccess)
+  if (cudaLaunchKernel(k.fn, grid, dim3(pa::kThreads), args, plan.smem, a.stream) != cudaSuccess)
     return PA_ERR_CUDA;
   if (ev_split && cudaEventRecord(ev_split, a.stream) != cudaSuccess) return PA_ERR_CUDA;
 

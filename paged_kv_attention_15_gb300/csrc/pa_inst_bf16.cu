@@ -3,34 +3,29 @@
 
 namespace pa {
 
-template <int D, int MT, int TSL, int DS>
+template <int D, int MT, int TSL>
 static SplitKernel entry() {
-  using C = Cfg<D, MT, false, TSL, DS>;
-  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, false, TSL, DS>), C::SMEM_FIXED, C::NS,
-                     C::THREADS};
+  using C = Cfg<D, MT, false, TSL>;
+  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, false, TSL>), C::SMEM_FIXED, C::NS};
 }
 
-template <int D, int DS>
+template <int D>
 static SplitKernel by_tiles(int row_tiles, int slice) {
-  if (row_tiles == 1 && slice == 16) return entry<D, 1, 16, DS>();
-  if (row_tiles == 2 && slice == 16) return entry<D, 2, 16, DS>();
-  if (row_tiles == 2 && slice == 32) return entry<D, 2, 32, DS>();
+  if (row_tiles == 1 && slice == 16) return entry<D, 1, 16>();
+  if (row_tiles == 2 && slice == 16) return entry<D, 2, 16>();
+  if (row_tiles == 2 && slice == 32) return entry<D, 2, 32>();
   if constexpr (D == 128) {
-    if (row_tiles == 4 && slice == 16) return entry<D, 4, 16, DS>();
-    if (row_tiles == 4 && slice == 32) return entry<D, 4, 32, DS>();
+    if (row_tiles == 4 && slice == 16) return entry<D, 4, 16>();
+    if (row_tiles == 4 && slice == 32) return entry<D, 4, 32>();
   }
-  return SplitKernel{nullptr, 0, 0, 0};
+  return SplitKernel{nullptr, 0, 0};
 }
 
-SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice, int dsplit) {
-  if (dsplit == 1) {
-    if (head_dim == 64) return by_tiles<64, 1>(row_tiles, slice);
-    if (head_dim == 128) return by_tiles<128, 1>(row_tiles, slice);
-    if (head_dim == 256) return by_tiles<256, 1>(row_tiles, slice);
-  } else if (dsplit == 2) {
-    if (head_dim == 128) return by_tiles<128, 2>(row_tiles, slice);
-  }
-  return SplitKernel{nullptr, 0, 0, 0};
+SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice) {
+  if (head_dim == 64) return by_tiles<64>(row_tiles, slice);
+  if (head_dim == 128) return by_tiles<128>(row_tiles, slice);
+  if (head_dim == 256) return by_tiles<256>(row_tiles, slice);
+  return SplitKernel{nullptr, 0, 0};
 }
 
 }  // namespace pa

@@ -42,10 +42,11 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 4;  // consumer warps per head-dim slice
-constexpr int kStageRows = 64;     // key rows per pipeline stage (tokens x heads)
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kStageRows = 64;  // key rows per pipeline stage (tokens x heads)
 constexpr int kMaxHkvFp8 = 8;
-constexpr int kSmemBudget = 226 * 1024;
+constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kErrWaitTimeout = 1;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -93,14 +94,9 @@ struct ReduceParams {
   int grid;        // CTAs of the balanced split launch
 };
 
-// Shared-memory plan of one kernel instance. TSL: tokens per warp slice;
-// DS: head-dim split (2: pairs of warps each own half of D for P V and
-// exchange their partial Q K^T sums, halving the accumulator so twice as
-// many consumer warps fit).
-template <int D, int MT, bool FP8, int TSL, int DS>
+// Shared-memory plan of one kernel instance (TSL: tokens per warp slice).
+template <int D, int MT, bool FP8, int TSL>
 struct Cfg {
-  static constexpr int CW = kConsumerWarps * DS;  // consumer warps
-  static constexpr int THREADS = 32 * (CW + 1);
   static constexpr int ELEM = FP8 ? 1 : 2;
   static constexpr int CE = 128 / ELEM;         // elements per 128-byte row chunk
   static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
@@ -112,27 +108,21 @@ struct Cfg {
   static constexpr int QCHUNK = ROWS * 128;
   static constexpr int QSLOT = QCH * QCHUNK;
   static constexpr int NGW = kConsumerWarps / MT;  // warps per row tile, each holding a partial result
-  static constexpr int RSTR = D + 4;               // floats per row of the merge buffer
+  static constexpr int RSTR = D + 8;               // floats per row of the merge buffer
   static constexpr int RED = (NGW - 1) * ROWS * RSTR * 4;
   static constexpr int REDML = (NGW - 1) * ROWS * 2 * 4;
-  // Partial-score exchange of the warp pairs (DS = 2): per pair and half,
-  // TSL / 2 floats per lane.
-  static constexpr int XCH = DS == 2 ? kConsumerWarps * 2 * (TSL / 2) * 32 * 4 : 0;
   static constexpr int BARS = 256;
-  static constexpr int FIXED = 2 * QSLOT + round_up(RED + REDML, 1024) + XCH + BARS;
+  static constexpr int FIXED = 2 * QSLOT + round_up(RED + REDML, 1024) + BARS;
   static constexpr int NS = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
   static constexpr int OFF_Q = NS * STAGE;
   static constexpr int OFF_RED = OFF_Q + 2 * QSLOT;
   static constexpr int OFF_REDML = OFF_RED + RED;
-  static constexpr int OFF_XCH = round_up(OFF_REDML + REDML, 1024);
-  static constexpr int OFF_BAR = OFF_XCH + XCH;
+  static constexpr int OFF_BAR = round_up(OFF_REDML + REDML, 1024);
   static constexpr int OFF_PREFIX = OFF_BAR + BARS;
   static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1024 to align the dynamic base
   static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
   static_assert(MT == 1 || MT == 2 || MT == 4, "unsupported row tiles");
   static_assert(TSL == 16 || TSL == 32, "unsupported warp slice");
-  static_assert(DS == 1 || DS == 2, "unsupported head-dim split");
-  static_assert(D / DS >= 64 && (!FP8 || D / DS >= 64), "head-dim slices must hold whole 64-wide chunks");
 };
 
 // ----------------------------------------------------------------- schedule
@@ -244,18 +234,14 @@ __device__ __forceinline__ void raise_abort(volatile int* s_abort, int* err_flag
 }
 
 // ------------------------------------------------------------ split kernel
-template <int D, int MT, bool FP8, int TSL, int DS>
-__global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
-    pa_split_kernel(const __grid_constant__ SplitParams p) {
-  using C = Cfg<D, MT, FP8, TSL, DS>;
+template <int D, int MT, bool FP8, int TSL>
+__global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_constant__ SplitParams p) {
+  using C = Cfg<D, MT, FP8, TSL>;
   constexpr int NS = C::NS;
   constexpr int NGW = C::NGW;
   constexpr int NCH = C::NCH;
-  constexpr int CW = C::CW;
-  constexpr int THREADS = C::THREADS;
-  constexpr int NTS = TSL / 8;      // n8 tiles of a warp's slice
-  constexpr int NT8 = D / 8;        // n8 tiles of the output row
-  constexpr int NTW = NT8 / DS;     // n8 tiles of this warp's head-dim slice
+  constexpr int NTS = TSL / 8;  // n8 tiles of a warp's slice
+  constexpr int NT8 = D / 8;    // n8 tiles of the output row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -276,11 +262,11 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, CW);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(bar_qfull + 8 * q, 1);
-      mbar_init(bar_qempty + 8 * q, CW);
+      mbar_init(bar_qempty + 8 * q, kConsumerWarps);
     }
     *s_abort = 0;
     fence_mbar_init();
@@ -288,10 +274,10 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
   // Query rows past M read as zero: clear both Q slots once.
   {
     uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q);
-    for (int i = tid; i < 2 * C::QSLOT / 16; i += THREADS) q4[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < 2 * C::QSLOT / 16; i += kThreads) q4[i] = make_uint4(0, 0, 0, 0);
   }
   if (p.num_splits == 0) {
-    for (int i = tid; i < p.B; i += THREADS) s_ctx[i] = clamp_ctx(p, __ldg(p.context_lens + i));
+    for (int i = tid; i < p.B; i += kThreads) s_ctx[i] = clamp_ctx(p, __ldg(p.context_lens + i));
     __syncthreads();
     if (warp == 0) {  // exclusive prefix sum of virtual pages per sequence
       int carry = 0;
@@ -317,7 +303,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
   const int TS = p.TS;
   // Bytes per key row of all H2 heads (+ their fp8 scales) in a stage.
   const uint32_t row_bytes = H2 * D * C::ELEM + (FP8 ? p.Hkv * 4 : 0);
-  if (warp == CW) {
+  if (warp == kConsumerWarps) {
     // ================================================================ producer
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
@@ -428,19 +414,12 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
   }
 
   // ================================================================ consumers
-  // Consumer warp w: head-dim half dh = w / 4 (when DS = 2); row tile
-  // mt = (w % 4) % MT; among the NGW warps of that tile, gi picks the kv head
-  // hl (when a tile holds several heads' rows) and the token slice ts of
-  // every stage (TSL tokens). With DS = 2, warps w and w ^ 4 form a pair with
-  // the same rows, head and tokens: each computes Q K^T over its half of D,
-  // they exchange the partial scores through shared memory (both then hold
-  // the same full scores, summed in the same order), and each runs P V for
-  // its half of D.
+  // Warp w: row tile mt = w % MT; among the NGW warps of that tile, gi picks
+  // the kv head hl (when a tile holds several heads' rows) and the token
+  // slice ts of every stage (TSL tokens).
   const int GT = p.GT;
-  const int dh = DS == 2 ? warp / kConsumerWarps : 0;
-  const int w4 = warp % kConsumerWarps;
-  const int mt = w4 % MT;
-  const int gi = w4 / MT;
+  const int mt = warp % MT;
+  const int gi = warp / MT;
   const int hl_base = (mt * 16) / GT;
   const int ht = GT >= 16 ? 1 : min(16 / GT, H2 - hl_base);
   const int hl = hl_base + gi % ht;
@@ -453,19 +432,13 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
   const float NEG_INF = -__int_as_float(0x7f800000);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* redml = reinterpret_cast<float*>(smem + C::OFF_REDML);
-  float* xmine = reinterpret_cast<float*>(smem + C::OFF_XCH) + (size_t)(w4 * 2 + dh) * (TSL / 2) * 32;
-  float* xpeer = reinterpret_cast<float*>(smem + C::OFF_XCH) + (size_t)(w4 * 2 + (dh ^ 1)) * (TSL / 2) * 32;
-  constexpr int KK = D / 16 / DS;  // bf16 k-steps of this warp's half
-  constexpr int KQ = D / 64 / DS;  // fp8 groups of four k-steps of this warp's half
-  constexpr int ND = D / 16 / DS;  // bf16 P V: pairs of n8 tiles of this half
-  constexpr int UU = D / 32 / DS;  // fp8 P V: groups of four n8 tiles of this half
 
   Cursor cur;
   cursor_init(p, s_start, cur);
   Item it;
   int stage = 0, qn = 0;
   bool ok = true;
-  float acc[NTW][4];
+  float acc[NT8][4];
 
   while (next_item(p, s_ctx, s_start, cur, it)) {
     float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
@@ -488,8 +461,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
           uint8_t* qs_ptr = smem + C::OFF_Q + qs * C::QSLOT;
           uint4* dst = reinterpret_cast<uint4*>(qs_ptr);
 #pragma unroll
-          for (int ql = 0; ql < KQ; ++ql) {
-            const int q = dh * KQ + ql;
+          for (int q = 0; q < D / 64; ++q) {
             uint32_t fr[4][4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -511,10 +483,10 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
             __syncwarp();
           }
         }
-        named_barrier_sync(1, 32 * CW);
+        named_barrier_sync(1, 32 * kConsumerWarps);
       }
 #pragma unroll
-      for (int i = 0; i < NTW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
       for (int j = 0; j < it.nst; ++j) {
         const int st = stage + j;
@@ -526,7 +498,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
         const bool scr = it.scratch && j == it.nst - 1;
         const int valid = scr ? p.T : min(TS, it.tok_end - (it.tok0 + j * TS));
         const int tb = ts * TSL;  // first token of this warp's slice
-        if (tb < valid) {  // identical for the two warps of a pair
+        if (ok && tb < valid) {
           // Stage tile: [box][chunk][head][box row][128 B]; a box holds the
           // rows of one page (scratch: TP rows). Every token index used below
           // is a multiple of 8 plus (lane & 7), so the 128-byte swizzle of its
@@ -545,203 +517,179 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
           const float* vsc = ksc + C::SCALE / 4;
           const int sw = lane & 7;
 
-          // ---- S = Q K^T: 16 rows x TSL tokens, over this warp's half of D.
-          // Two accumulators per tile (even and odd k-steps) halve the
-          // dependent MMA chain.
+          // ---- S = Q K^T: 16 rows x TSL tokens. Two accumulators per tile
+          // (even and odd k-steps) halve the dependent MMA chain.
           float s[NTS][4], s2[NTS][4];
 #pragma unroll
           for (int i = 0; i < NTS; ++i) {
             s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
             s2[i][0] = s2[i][1] = s2[i][2] = s2[i][3] = 0.f;
           }
-          if (ok) {
+          if (!FP8) {
+            uint32_t krow[NTS / 2];
+#pragma unroll
+            for (int nb = 0; nb < NTS / 2; ++nb) krow[nb] = kb_ + row_base(tb + nb * 16 + (lane >> 4) * 8 + sw);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              uint32_t qa[4];
+              {
+                const int row = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int d = kk * 16 + (lane >> 4) * 8;
+                ldsm_x4(qbase + (d / 64) * C::QCHUNK + swz(row, (d % 64) / 8), qa[0], qa[1], qa[2], qa[3]);
+              }
+              const int unit = ((kk * 16) % 64) / 8 + ((lane >> 3) & 1);
+              const uint32_t coff = (kk / 4) * cstride + ((unit ^ sw) << 4);
+#pragma unroll
+              for (int nb = 0; nb < NTS / 2; ++nb) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(krow[nb] + coff, b0, b1, b2, b3);
+                mma_bf16((kk & 1) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
+                mma_bf16((kk & 1) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
+              }
+            }
+          } else {
+            uint32_t krow[NTS];
+#pragma unroll
+            for (int nt = 0; nt < NTS; ++nt) krow[nt] = kb_ + row_base(tb + nt * 8 + sw);
+            const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
+#pragma unroll
+            for (int kq = 0; kq < D / 64; ++kq) {
+              uint32_t qa[4][4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
+                qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
+              }
+              const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
+              const uint32_t coff = (unit / 8) * cstride + (((unit % 8) ^ sw) << 4);
+#pragma unroll
+              for (int nt = 0; nt < NTS; ++nt) {
+                uint32_t kr[4];
+                ldsm_x4(krow[nt] + coff, kr[0], kr[1], kr[2], kr[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  mma_f16((e & 1) ? s2[nt] : s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NTS; ++i) {
+            s[i][0] += s2[i][0];
+            s[i][1] += s2[i][1];
+            s[i][2] += s2[i][2];
+            s[i][3] += s2[i][3];
+          }
+
+          // ---- scale (and per-token K scale), mask, online softmax in base 2
+          const float sl = p.scale_log2;
+#pragma unroll
+          for (int i = 0; i < NTS; ++i) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = tb + i * 8 + 2 * c4 + (e & 1);
+              float f = s[i][e] * sl;
+              if (FP8) f *= ksc[tok * p.Hkv + g];
+              s[i][e] = (tok < valid && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
+            }
+          }
+          float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+          for (int i = 0; i < NTS; ++i) {
+            mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[i][2], s[i][3]));
+          }
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
+          const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
+          // alpha = 1 exactly when the running max did not move (also for
+          // rows this warp does not compute, which stay at -inf).
+          const float al0 = mn0 == m0 ? 1.f : ex2(m0 - mu0);
+          const float al1 = mn1 == m1 ? 1.f : ex2(m1 - mu1);
+          m0 = mn0;
+          m1 = mn1;
+          float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < NTS; ++i) {
+            s[i][0] = ex2(s[i][0] - mu0);
+            s[i][1] = ex2(s[i][1] - mu0);
+            s[i][2] = ex2(s[i][2] - mu1);
+            s[i][3] = ex2(s[i][3] - mu1);
+            ls0 += s[i][0] + s[i][1];
+            ls1 += s[i][2] + s[i][3];
+          }
+          l0 = l0 * al0 + ls0;
+          l1 = l1 * al1 + ls1;
+          // The running max rarely moves after the first stages: rescale
+          // the accumulator only when some row's max grew.
+          if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < NT8; ++i) {
+              acc[i][0] *= al0;
+              acc[i][1] *= al0;
+              acc[i][2] *= al1;
+              acc[i][3] *= al1;
+            }
+          }
+
+          // ---- O += P V: the score fragments are the A operand as they are
+          const bool partial = valid < tb + TSL;
+#pragma unroll
+          for (int kb = 0; kb < NTS / 2; ++kb) {
+            const int t0 = tb + kb * 16 + 2 * c4;  // tokens of the lo fragment; +8 for the hi one
+            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+            if (partial) {
+              vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+              vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+            }
+            const uint32_t vrow = vb_ + row_base(tb + kb * 16 + ((lane >> 3) & 1) * 8 + sw);
+            uint32_t pa[4];
             if (!FP8) {
-              uint32_t krow[NTS / 2];
+              pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
+              pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
+              pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
+              pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
 #pragma unroll
-              for (int nb = 0; nb < NTS / 2; ++nb) krow[nb] = kb_ + row_base(tb + nb * 16 + (lane >> 4) * 8 + sw);
-              const int qrow = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-#pragma unroll
-              for (int kl = 0; kl < KK; ++kl) {
-                const int kk = dh * KK + kl;
-                uint32_t qa[4];
-                ldsm_x4(qbase + (kk >> 2) * C::QCHUNK + swz(qrow, (kk & 3) * 2 + (lane >> 4)), qa[0], qa[1], qa[2], qa[3]);
-                const int unit = (kk & 3) * 2 + ((lane >> 3) & 1);
-                const uint32_t coff = (kk >> 2) * cstride + ((unit ^ sw) << 4);
-#pragma unroll
-                for (int nb = 0; nb < NTS / 2; ++nb) {
-                  uint32_t b0, b1, b2, b3;
-                  ldsm_x4(krow[nb] + coff, b0, b1, b2, b3);
-                  mma_bf16((kl & 1) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
-                  mma_bf16((kl & 1) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
+              for (int nd = 0; nd < D / 16; ++nd) {
+                const int unit = ((nd * 16) % 64) / 8 + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vrow + (nd / 4) * cstride + ((unit ^ sw) << 4), b0, b1, b2, b3);
+                if (partial) {
+                  b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
                 }
+                mma_bf16(acc[2 * nd], pa, b0, b1);
+                mma_bf16(acc[2 * nd + 1], pa, b2, b3);
               }
             } else {
-              uint32_t krow[NTS];
+              // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
+              float vs[4];
+              vs[0] = t0 < valid ? vsc[t0 * p.Hkv + g] : 0.f;
+              vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + g] : 0.f;
+              vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + g] : 0.f;
+              vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + g] : 0.f;
+              pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
+              pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
+              pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
+              pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
 #pragma unroll
-              for (int nt = 0; nt < NTS; ++nt) krow[nt] = kb_ + row_base(tb + nt * 8 + sw);
-              const uint4* qf = reinterpret_cast<const uint4*>(smem + C::OFF_Q + qs * C::QSLOT);
-#pragma unroll
-              for (int kql = 0; kql < KQ; ++kql) {
-                const int kq = dh * KQ + kql;
-                uint32_t qa[4][4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const uint4 v = qf[(kq * C::QCHUNK + mt * 2048) / 16 + e * 32 + lane];
-                  qa[e][0] = v.x; qa[e][1] = v.y; qa[e][2] = v.z; qa[e][3] = v.w;
+              for (int uu = 0; uu < D / 32; ++uu) {
+                const int unit = 2 * uu + (lane >> 4);
+                uint32_t R[4];
+                ldsm_x4_trans(vrow + (unit / 8) * cstride + (((unit % 8) ^ sw) << 4), R[0], R[1], R[2], R[3]);
+                if (partial) {
+                  R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
                 }
-                const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
-                const uint32_t coff = (unit >> 3) * cstride + (((unit & 7) ^ sw) << 4);
 #pragma unroll
-                for (int nt = 0; nt < NTS; ++nt) {
-                  uint32_t kr[4];
-                  ldsm_x4(krow[nt] + coff, kr[0], kr[1], kr[2], kr[3]);
-#pragma unroll
-                  for (int e = 0; e < 4; ++e)
-                    mma_f16((e & 1) ? s2[nt] : s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
-                }
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < NTS; ++i) {
-              s[i][0] += s2[i][0];
-              s[i][1] += s2[i][1];
-              s[i][2] += s2[i][2];
-              s[i][3] += s2[i][3];
-            }
-          }
-          if (DS == 2) {
-            // Pair exchange of the partial scores. The first barrier keeps a
-            // warp from overwriting its slot before the peer read it last
-            // stage; both warps add half 0 + half 1 in that order.
-            named_barrier_sync(2 + w4, 64);
-#pragma unroll
-            for (int i = 0; i < NTS; ++i)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) xmine[(i * 4 + e) * 32 + lane] = s[i][e];
-            named_barrier_sync(2 + w4, 64);
-#pragma unroll
-            for (int i = 0; i < NTS; ++i)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float o = xpeer[(i * 4 + e) * 32 + lane];
-                s[i][e] = dh == 0 ? s[i][e] + o : o + s[i][e];
-              }
-          }
-
-          if (ok) {
-            // ---- scale (and per-token K scale), mask, online softmax in base 2
-            const float sl = p.scale_log2;
-#pragma unroll
-            for (int i = 0; i < NTS; ++i) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int tok = tb + i * 8 + 2 * c4 + (e & 1);
-                float f = s[i][e] * sl;
-                if (FP8) f *= ksc[tok * p.Hkv + g];
-                s[i][e] = (tok < valid && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
-              }
-            }
-            float mx0 = NEG_INF, mx1 = NEG_INF;
-#pragma unroll
-            for (int i = 0; i < NTS; ++i) {
-              mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][1]));
-              mx1 = fmaxf(mx1, fmaxf(s[i][2], s[i][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
-            const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
-            // alpha = 1 exactly when the running max did not move (also for
-            // rows this warp does not compute, which stay at -inf).
-            const float al0 = mn0 == m0 ? 1.f : ex2(m0 - mu0);
-            const float al1 = mn1 == m1 ? 1.f : ex2(m1 - mu1);
-            m0 = mn0;
-            m1 = mn1;
-            float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < NTS; ++i) {
-              s[i][0] = ex2(s[i][0] - mu0);
-              s[i][1] = ex2(s[i][1] - mu0);
-              s[i][2] = ex2(s[i][2] - mu1);
-              s[i][3] = ex2(s[i][3] - mu1);
-              ls0 += s[i][0] + s[i][1];
-              ls1 += s[i][2] + s[i][3];
-            }
-            l0 = l0 * al0 + ls0;
-            l1 = l1 * al1 + ls1;
-            // The running max rarely moves after the first stages: rescale
-            // the accumulator only when some row's max grew.
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-              for (int i = 0; i < NTW; ++i) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al0;
-                acc[i][2] *= al1;
-                acc[i][3] *= al1;
-              }
-            }
-
-            // ---- O += P V over this warp's half of D: the score fragments
-            // are the A operand as they are
-            const bool partial = valid < tb + TSL;
-#pragma unroll
-            for (int kb = 0; kb < NTS / 2; ++kb) {
-              const int t0 = tb + kb * 16 + 2 * c4;  // tokens of the lo fragment; +8 for the hi one
-              uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-              if (partial) {
-                vm0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-                vm1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-              }
-              const uint32_t vrow = vb_ + row_base(tb + kb * 16 + ((lane >> 3) & 1) * 8 + sw);
-              uint32_t pa[4];
-              if (!FP8) {
-                pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
-                pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
-                pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
-                pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
-#pragma unroll
-                for (int nl = 0; nl < ND; ++nl) {
-                  const int nd = dh * ND + nl;
-                  const int unit = (nd & 3) * 2 + (lane >> 4);
-                  uint32_t b0, b1, b2, b3;
-                  ldsm_x4_trans(vrow + (nd >> 2) * cstride + ((unit ^ sw) << 4), b0, b1, b2, b3);
-                  if (partial) {
-                    b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
-                  }
-                  mma_bf16(acc[2 * nl], pa, b0, b1);
-                  mma_bf16(acc[2 * nl + 1], pa, b2, b3);
-                }
-              } else {
-                // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
-                float vs[4];
-                vs[0] = t0 < valid ? vsc[t0 * p.Hkv + g] : 0.f;
-                vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + g] : 0.f;
-                vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + g] : 0.f;
-                vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + g] : 0.f;
-                pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
-                pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
-                pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
-                pa[3] = pack_f16x2(s[2 * kb + 1][2] * vs[2], s[2 * kb + 1][3] * vs[3]);
-#pragma unroll
-                for (int ul = 0; ul < UU; ++ul) {
-                  const int unit = 2 * (dh * UU + ul) + (lane >> 4);
-                  uint32_t R[4];
-                  ldsm_x4_trans(vrow + (unit >> 3) * cstride + (((unit & 7) ^ sw) << 4), R[0], R[1], R[2], R[3]);
-                  if (partial) {
-                    R[0] &= vm0; R[1] &= vm1; R[2] &= vm0; R[3] &= vm1;
-                  }
-#pragma unroll
-                  for (int k = 0; k < 2; ++k) {
-                    // bytes (tok 2c d 2r, tok 2c d 2r+1, tok 2c+1 d 2r, tok 2c+1 d 2r+1)
-                    const uint32_t x = prmt(R[2 * k], 0, 0x3120);
-                    const uint32_t y = prmt(R[2 * k + 1], 0, 0x3120);
-                    const int nt = 2 * (2 * ul + k);
-                    mma_f16(acc[nt], pa, e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(y));
-                    mma_f16(acc[nt + 1], pa, e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y >> 16));
-                  }
+                for (int k = 0; k < 2; ++k) {
+                  // bytes (tok 2c d 2r, tok 2c d 2r+1, tok 2c+1 d 2r, tok 2c+1 d 2r+1)
+                  const uint32_t x = prmt(R[2 * k], 0, 0x3120);
+                  const uint32_t y = prmt(R[2 * k + 1], 0, 0x3120);
+                  const int nt = 2 * (2 * uu + k);
+                  mma_f16(acc[nt], pa, e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(y));
+                  mma_f16(acc[nt + 1], pa, e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y >> 16));
                 }
               }
             }
@@ -757,25 +705,24 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
       ++qn;
     } else {
 #pragma unroll
-      for (int i = 0; i < NTW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
 
-    // ---- merge the NGW warps of each row tile (per head-dim half), then write
+    // ---- merge the NGW warps of each row tile, then write
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const int col0 = dh * NTW * 8;  // first logical column of this warp's half
     if (NGW > 1) {
-      named_barrier_sync(1, 32 * CW);
+      named_barrier_sync(1, 32 * kConsumerWarps);
       if (gi > 0) {
-        float* rb = red + (size_t)(gi - 1) * C::ROWS * C::RSTR + col0;
+        float* rb = red + (size_t)(gi - 1) * C::ROWS * C::RSTR;
 #pragma unroll
-        for (int i = 0; i < NTW; ++i) {
+        for (int i = 0; i < NT8; ++i) {
           *reinterpret_cast<float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][0], acc[i][1]);
           *reinterpret_cast<float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][2], acc[i][3]);
         }
-        if (c4 == 0 && dh == 0) {  // m and l are the same in both halves
+        if (c4 == 0) {
           float* ml = redml + (size_t)(gi - 1) * C::ROWS * 2;
           ml[2 * rho0] = m0;
           ml[2 * rho0 + 1] = l0;
@@ -783,7 +730,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
           ml[2 * rho1 + 1] = l1;
         }
       }
-      named_barrier_sync(1, 32 * CW);
+      named_barrier_sync(1, 32 * kConsumerWarps);
     }
     if (gi != 0) continue;
 
@@ -808,11 +755,11 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
     const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
     const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
 #pragma unroll
-    for (int i = 0; i < NTW; ++i) {
+    for (int i = 0; i < NT8; ++i) {
       float a0 = acc[i][0] * w00, a1 = acc[i][1] * w00, a2 = acc[i][2] * w01, a3 = acc[i][3] * w01;
 #pragma unroll
       for (int q = 0; q < NGW - 1; ++q) {
-        const float* rb = red + (size_t)q * C::ROWS * C::RSTR + col0;
+        const float* rb = red + (size_t)q * C::ROWS * C::RSTR;
         const float2 x = *reinterpret_cast<const float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4);
         const float2 y = *reinterpret_cast<const float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4);
         a0 += wq0[q] * x.x;
@@ -839,35 +786,34 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8, TSL, DS>::THREADS, 1)
       const size_t row = ((size_t)it.b * p.T + t) * p.Hq + h;
       const float lsev = h2 ? lse1 : lse0;
       if (it.part < 0) {
-        __nv_bfloat16* o = p.out + row * D + col0;
+        __nv_bfloat16* o = p.out + row * D;
         if (!FP8) {
 #pragma unroll
-          for (int i = 0; i < NTW; ++i)
+          for (int i = 0; i < NT8; ++i)
             *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * c4) = pack_bf16x2(acc[i][2 * h2], acc[i][2 * h2 + 1]);
         } else {
-          // fp8 column order: tiles 2u, 2u+1 of unit u hold d = 16 u + 4 c4 .. +3
 #pragma unroll
-          for (int u = 0; u < NTW / 2; ++u)
+          for (int u = 0; u < D / 16; ++u)
             *reinterpret_cast<uint2*>(o + 16 * u + 4 * c4) =
                 make_uint2(pack_bf16x2(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2]),
                            pack_bf16x2(acc[2 * u][2 * h2 + 1], acc[2 * u + 1][2 * h2 + 1]));
         }
-        if (c4 == 0 && dh == 0 && p.lse) p.lse[row] = lsev;
+        if (c4 == 0 && p.lse) p.lse[row] = lsev;
       } else {
         const size_t prow = p.num_splits > 0 ? row * p.num_splits + it.part : (size_t)it.part * p.M + rho;
-        float* o = p.part_o + prow * D + col0;
+        float* o = p.part_o + prow * D;
         if (!FP8) {
 #pragma unroll
-          for (int i = 0; i < NTW; ++i)
+          for (int i = 0; i < NT8; ++i)
             *reinterpret_cast<float2*>(o + i * 8 + 2 * c4) = make_float2(acc[i][2 * h2], acc[i][2 * h2 + 1]);
         } else {
 #pragma unroll
-          for (int u = 0; u < NTW / 2; ++u)
+          for (int u = 0; u < D / 16; ++u)
             *reinterpret_cast<float4*>(o + 16 * u + 4 * c4) =
                 make_float4(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2], acc[2 * u][2 * h2 + 1],
                             acc[2 * u + 1][2 * h2 + 1]);
         }
-        if (c4 == 0 && dh == 0) p.part_lse[prow] = lsev;
+        if (c4 == 0) p.part_lse[prow] = lsev;
       }
     }
   }

@@ -11,12 +11,11 @@ struct SplitKernel {
   const void* fn;   // __global__ function, launched with cudaLaunchKernel
   int smem_fixed;   // dynamic shared memory without the per-sequence table
   int stages;       // pipeline depth of the instance
-  int threads;      // block size
 };
 
-// Kernel instance for (head_dim, row tiles, tokens per warp slice, head-dim
-// split); fn == nullptr if that combination is not built.
-SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice, int dsplit);
-SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice, int dsplit);
+// Kernel instance for (head_dim, row tiles, tokens per warp slice);
+// fn == nullptr if that combination is not built.
+SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice);
+SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice);
 
 }  // namespace pa
