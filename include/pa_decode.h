@@ -102,6 +102,18 @@ typedef struct pa_shape {
  * device's SM count. Returns 0 as well for an invalid shape. */
 size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits);
 
+/* What num_splits == 0 resolves to on the current device, for this shape and
+ * KV format (fp8_kv: 0 for bf16 pages, as pa_decode and pa_decode_tidar;
+ * 1 for pa_decode_fp8). Returns 0 when it runs the balanced schedule (one
+ * CTA per SM, each taking an equal share of all the shape's pages, so a
+ * sequence is split wherever two shares meet), or the explicit split count
+ * S >= 1 it falls back to when the per-sequence table does not fit in
+ * shared memory (S = ceil(2 * SMs / (B * kv head groups)), at most
+ * max_blocks_per_seq). Returns -1 for an invalid or unsupported shape, or
+ * when no CUDA device is usable. The split scheduler of the north-star
+ * problem statement: the grid fills the SMs. */
+int32_t pa_decode_choose_splits(const pa_shape* shape, int32_t fp8_kv);
+
 /* Dense bf16 paged decode (the MSLK page's dense decode kernel).
  * q, k_cache, v_cache, out: bf16 as above. lse may be NULL. scale: the
  * softmax scale (finite), e.g. 1/sqrt(D). */

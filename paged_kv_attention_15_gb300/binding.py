@@ -47,6 +47,7 @@ _P = ctypes.c_void_p
 _DECODE_TAIL = [ctypes.POINTER(PaShape), ctypes.c_float, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]
 _SIGNATURES = {
     "pa_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(PaShape), ctypes.c_int32]),
+    "pa_decode_choose_splits": (ctypes.c_int32, [ctypes.POINTER(PaShape), ctypes.c_int32]),
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_tidar": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
@@ -113,6 +114,12 @@ def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tenso
 
 def workspace_size(shape: PaShape, num_splits: int) -> int:
     return int(lib().pa_decode_workspace_size(ctypes.byref(shape), int(num_splits)))
+
+
+def choose_splits(shape: PaShape, fp8: bool = False) -> int:
+    """What num_splits=0 resolves to: 0 for the balanced schedule, else the
+    explicit split count; -1 for an unsupported shape or no device."""
+    return int(lib().pa_decode_choose_splits(ctypes.byref(shape), int(bool(fp8))))
 
 
 def _need_contig(**tensors):

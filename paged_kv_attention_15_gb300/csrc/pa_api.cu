@@ -463,6 +463,16 @@ size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits) {
   return best;
 }
 
+int32_t pa_decode_choose_splits(const pa_shape* shape, int32_t fp8_kv) {
+  const Kind kind = fp8_kv ? Kind::kFp8 : Kind::kBf16;
+  if (check_shape(shape, kind) != PA_OK) return -1;
+  DeviceState* d = nullptr;
+  if (device_state(&d) != PA_OK) return -1;
+  Plan plan;
+  if (make_plan(shape, kind, 0, d, &plan) != PA_OK) return -1;
+  return plan.balanced ? 0 : plan.splits;
+}
+
 pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                     const int32_t* context_lens, const pa_shape* shape, float scale, void* out, float* lse,
                     int32_t num_splits, void* workspace, size_t workspace_bytes, pa_stream_t stream) {

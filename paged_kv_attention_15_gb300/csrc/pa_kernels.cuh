@@ -321,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     while (ok && next_item(p, s_ctx, s_start, cur, it)) {
       if (it.nst == 0) continue;
       const int qs = qn & 1;
-      if (qn >= 2) ok = mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort);
+      // Warp-uniform verdicts: the lanes leave the loops together.
+      if (qn >= 2) ok = __all_sync(0xffffffffu, mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort));
       if (!ok) break;
       if (lane == 0) {
         // Rows of kv head hl occupy rows [hl*GT, (hl+1)*GT) of each chunk.
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       for (int j = 0; j < it.nst; ++j, ++stage) {
         const int slot = stage % NS;
         if (stage >= NS) {
-          ok = mbar_wait(bar_empty + 8 * slot, ((stage / NS) - 1) & 1, kWaitLimitNs, s_abort);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * slot, ((stage / NS) - 1) & 1, kWaitLimitNs, s_abort));
           if (!ok) break;
         }
         filled |= 1u << slot;
@@ -370,6 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           ids = ids_next;
           ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
         }
+        // fp8 scales: rows [token][Hkv] of the stage's pages, one bulk copy
+        // per page and tensor. A page id outside the pool reads zero codes
+        // (tensor-map fill); its scales come from page 0 so that they stay
+        // finite and the copy stays in bounds.
+        auto copy_scales = [&](uint32_t soff, int page, int row0, int rows) {
+          const uint32_t sb = rows * p.Hkv * 4;
+          if ((unsigned)page >= (unsigned)p.num_pages) page = 0;
+          const size_t off = ((size_t)page * P + row0) * p.Hkv;
+          bulk_load(ksd + soff, p.k_scale + off, sb, full, pol_kv);
+          bulk_load(vsd + soff, p.v_scale + off, sb, full, pol_kv);
+        };
         if (P < TS) {  // whole pages: one box each
           const int npg = (valid + P - 1) / P;
           if (lane == 0) mbar_arrive_expect_tx(full, 2 * npg * P * row_bytes);
@@ -379,12 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               const uint32_t boff = i * NCH * H2 * P * 128;
               tma_load_5d(kdst + boff, &p.tm_k, full, 0, 0, it.hg * H2, 0, page, pol_kv);
               tma_load_5d(vdst + boff, &p.tm_v, full, 0, 0, it.hg * H2, 0, page, pol_kv);
-              if (FP8) {
-                const uint32_t sb = P * p.Hkv * 4;
-                const size_t off = (size_t)page * P * p.Hkv;
-                bulk_load(ksd + i * sb, p.k_scale + off, sb, full, pol_kv);
-                bulk_load(vsd + i * sb, p.v_scale + off, sb, full, pol_kv);
-              }
+              if (FP8) copy_scales(i * P * p.Hkv * 4, page, 0, P);
             }
           }
         } else {  // TS rows of one page
@@ -394,12 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
             mbar_arrive_expect_tx(full, 2 * TS * row_bytes);
             tma_load_5d(kdst, &p.tm_k, full, 0, row0, it.hg * H2, 0, page, pol_kv);
             tma_load_5d(vdst, &p.tm_v, full, 0, row0, it.hg * H2, 0, page, pol_kv);
-            if (FP8) {
-              const uint32_t sb = TS * p.Hkv * 4;
-              const size_t off = ((size_t)page * P + row0) * p.Hkv;
-              bulk_load(ksd, p.k_scale + off, sb, full, pol_kv);
-              bulk_load(vsd, p.v_scale + off, sb, full, pol_kv);
-            }
+            if (FP8) copy_scales(0, page, row0, TS);
           }
         }
       }

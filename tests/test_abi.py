@@ -105,6 +105,12 @@ def test_explicit_split_workspace_size(lib):
     assert lib.pa_decode_workspace_size(ctypes.byref(s), -2) == 0
 
 
+def test_choose_splits_rejects_bad_shapes(lib):
+    assert lib.pa_decode_choose_splits(ctypes.byref(shape(head_dim=96)), 0) == -1
+    assert lib.pa_decode_choose_splits(ctypes.byref(shape(head_dim=64)), 1) == -1  # fp8 needs D >= 128
+    assert lib.pa_decode_choose_splits(ctypes.byref(shape(q_tokens=0)), 0) == -1
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pb, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(pb, "_lib", None)

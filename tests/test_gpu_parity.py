@@ -149,6 +149,36 @@ def test_unread_values_are_never_read(kv_format, num_splits):
     check_full(dirty, num_splits)
 
 
+@pytest.mark.parametrize("kv_format", ["bf16", "fp8"])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_out_of_range_page_ids_read_zeros(kv_format, num_splits):
+    """Block-table entries outside [0, num_pages) inside the context act as
+    pages of zero keys and values (the copy engine fills out-of-range boxes):
+    the result equals the oracle's on a pool with one extra all-zero page
+    (fp8: zero codes, scale 1) that those entries point to."""
+    s = spec(kv_format=kv_format, context_lens=(100, 40, 250, 17), pool_pages=60)
+    inp = gen.make_inputs(s)
+    n = inp.num_pages
+    bad = inp.block_tables.clone()
+    bad[0, 2] = n + 3
+    bad[2, 0] = -1
+    bad[2, 9] = n
+    gpu_in = dataclasses.replace(inp, block_tables=bad)
+    ref = dataclasses.replace(inp)
+    ref.k_cache = torch.cat([inp.k_cache, torch.zeros_like(inp.k_cache[:1])])
+    ref.v_cache = torch.cat([inp.v_cache, torch.zeros_like(inp.v_cache[:1])])
+    if kv_format == "fp8":
+        ref.k_scale = torch.cat([inp.k_scale, torch.ones_like(inp.k_scale[:1])])
+        ref.v_scale = torch.cat([inp.v_scale, torch.ones_like(inp.v_scale[:1])])
+    fixed = bad.clone()
+    fixed[(bad < 0) | (bad >= n)] = n
+    fixed[inp.block_tables < 0] = inp.block_tables[inp.block_tables < 0]
+    ref.block_tables = fixed
+    ref_out, ref_lse = oracle.decode(ora_inputs(ref), inp.scale)
+    out, lse = to_np(*gpu_decode(gpu_in, num_splits))
+    assert_match(out, lse, ref_out, ref_lse, tol_of(s))
+
+
 @pytest.mark.parametrize("num_splits", [0, 1, 3])
 def test_page_relabelling_is_bit_exact(num_splits):
     inp = gen.make_inputs(spec(pool_pages=80, context_lens=(300, 7, 129, 64)))
@@ -206,6 +236,27 @@ def test_split_counts_beyond_pages_and_single_page():
     inp = gen.make_inputs(spec(context_lens=(16, 1, 17, 40)))
     for S in (1, 2, 3, 4, 9, 100):
         check_full(inp, S)
+
+
+@pytest.mark.parametrize("kv_format", ["bf16", "fp8"])
+def test_auto_splits_fall_back_to_explicit_splits_for_many_sequences(kv_format):
+    """num_splits=0 runs the balanced schedule while the per-sequence table
+    fits in shared memory; for 8000 sequences it resolves to the explicit
+    split count pa_decode_choose_splits reports, bit for bit."""
+    small = gen.make_inputs(spec(kv_format=kv_format))
+    assert pb.choose_splits(pb.make_shape(small.q, small.k_cache, small.block_tables), kv_format == "fp8") == 0
+    s = spec(kv_format=kv_format, batch=8000, context_lens=None, ctx_range=(1, 40), pool_pages=24000)
+    inp = gen.make_inputs(s)
+    shp = pb.make_shape(inp.q, inp.k_cache, inp.block_tables)
+    S = pb.choose_splits(shp, kv_format == "fp8")
+    assert S >= 1
+    assert pb.workspace_size(shp, 0) == pb.workspace_size(shp, S)
+    dev = inp.to("cuda")
+    a = gpu_decode(inp, 0, dev=dev)
+    b = gpu_decode(inp, S, dev=dev)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    ref_out, ref_lse = oracle.decode(ora_inputs(inp), inp.scale)
+    assert_match(*to_np(*a), ref_out, ref_lse, tol_of(s))
 
 
 # ----------------------------------------------------- full-size workloads
