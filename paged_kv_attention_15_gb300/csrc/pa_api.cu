@@ -398,17 +398,16 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     r.part_lse = p.part_lse;
     r.out = p.out;
     r.lse = p.lse;
-    r.context_lens = p.context_lens;
     r.B = B;
     r.T = T;
     r.Hq = Hq;
-    r.Hkv = Hkv;
+    r.D = D;
+    r.context_lens = p.context_lens;
     r.G = G;
     r.M = geo.M;
     r.H2 = geo.H2;
     r.NHG = geo.NHG;
     r.GT = geo.GT;
-    r.D = D;
     r.P = P;
     r.max_blocks = s.max_blocks_per_seq;
     r.tidar = p.tidar;
