@@ -4,6 +4,7 @@ TEST INFRASTRUCTURE. Only tests/, the package entry module's smoke() and
 bench.py's cpu_baseline leg may import it. The product path never does.
 """
 
+from . import kv_append  # noqa: F401
 from .pa_oracle import (  # noqa: F401
     as_oracle_inputs,
     attend,
