@@ -4,9 +4,12 @@
 One step = one decode call (split kernel + split-K reduce) over the whole
 batch of the workload, inputs resident in HBM, issued as a CUDA-graph
 replay. Two device copies of the inputs (one graph each) are alternated so
-that no step finds its KV in the 129 MB L2.
+that no step finds its KV in the 129 MB L2. The append workloads
+(append, append_fp8, append_step) time the KV-cache append that precedes a
+decode instead: one step = one pa_kv_append(_fp8) call.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gqa|long|fp8|tidar]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--config gqa|long|fp8|tidar|append|append_fp8|append_step]
                     [--impl ours|reference]
 
 Prints one JSON line on rank 0. `value` is the achieved algorithmic HBM
@@ -55,7 +58,13 @@ WORKLOADS = {
     "long": "long-context split-K decode: B4 T1 Hq64 Hkv8 D128 P64 ctx 131072 bf16",
     "fp8": "native fp8 KV decode: B64 T1 Hq32 Hkv2 D256 P16 ctx U[1024,16384] e4m3fn KV + fp32 per-token scale",
     "tidar": "TiDAR draft-block decode: B16 T8 Hq32 Hkv8 D128 P16 ctx U[2048,8192] + scratch KV [16,8,8,128] bf16",
+    "append": "KV-cache append of a 512-token chunk: B64 T512 Hkv8 D128 P16 ctx U[0,4096] bf16",
+    "append_fp8": "KV-cache append with e4m3fn quantisation: B64 T512 Hkv2 D256 P16 ctx U[0,8192] "
+                  "bf16 rows -> e4m3fn + fp32 per-token scale",
+    "append_step": "KV-cache append of one decode step: B32 T1 Hkv8 D128 P16 ctx U[512,8192] bf16",
 }
+APPEND_CONFIGS = ("append", "append_fp8", "append_step")
+APPEND_METRIC = "KV-cache append µs/call and achieved HBM GB/s (fraction of 8 TB/s) on 1 GB300"
 SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -79,6 +88,20 @@ def algorithmic_bytes(inp) -> int:
     if s.draft_scratch:
         nbytes += 2 * s.batch * s.q_tokens * s.num_kv_heads * s.head_dim * 2
     return nbytes
+
+
+def append_bytes(inp) -> int:
+    """Bytes an append call must move: read the new K and V rows (bf16), write
+    them into the cache (bf16, or e4m3fn codes + an fp32 scale per row),
+    read context_lens and the block-table entries the new positions use."""
+    s = inp.spec
+    cap = inp.block_tables.shape[1] * s.page_size
+    lens = inp.context_lens.to(torch.int64).clamp(0, cap)
+    ends = (lens + s.new_tokens).clamp(max=cap)
+    rows = int((ends - lens).sum()) * s.num_kv_heads * 2  # (token, kv head) rows of K and V
+    written = s.head_dim + 4 if s.kv_format == "fp8" else 2 * s.head_dim
+    pages = int(((ends - 1) // s.page_size - lens // s.page_size + 1).clamp(min=0)[ends > lens].sum())
+    return rows * (2 * s.head_dim + written) + pages * 4 + s.batch * 4
 
 
 def unit_bytes(spec, ctx: int) -> int:
@@ -413,6 +436,138 @@ def run_ours(args, world, rank, local):
     return result
 
 
+def append_oracle_run(host, budget_s: float, start_seq: int = 0):
+    """The append oracle, as it stands, on whole sequences until the budget
+    is spent. Returns (seconds, algorithmic bytes, description)."""
+    from oracle import kv_append as ka
+
+    bits = host.numpy_bits()
+    caches = {n: bits[n] for n in ("k_cache", "v_cache", "k_scale", "v_scale") if n in bits}
+    spec = host.spec
+    done_s, done_b, n = 0.0, 0, 0
+    per_seq = append_bytes(host) / spec.batch
+    while done_s < budget_s and n < spec.batch:
+        b = (start_seq + n) % spec.batch
+        t = time.perf_counter()
+        ka.append(caches, bits["k_new"][b:b + 1], bits["v_new"][b:b + 1], bits["block_tables"][b:b + 1],
+                  bits["context_lens"][b:b + 1], spec.page_size)
+        done_s += time.perf_counter() - t
+        done_b += per_seq
+        n += 1
+    return done_s, int(done_b), f"{n} sequence(s) of the {spec.name} workload (mean bytes per sequence)"
+
+
+def run_append(args, world, rank, local):
+    """One step = one KV-cache append call over the whole batch."""
+    from paged_kv_attention_15_gb300 import binding as pb
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    host = gen.make_append_inputs(gen.APPEND_SPECS[args.config])
+    spec = host.spec
+    pb.lib()
+    sets = [host.to(dev), host.to(dev)]
+    stream = torch.cuda.current_stream(dev)
+
+    def call(d, st):
+        pb.kv_append(d.k_new, d.v_new, d.block_tables, d.context_lens, d.k_cache, d.v_cache,
+                     k_scale=d.k_scale, v_scale=d.v_scale, stream=st)
+
+    nbytes = append_bytes(host)
+    for i in range(args.warmup):
+        call(sets[i & 1], stream)
+    torch.cuda.synchronize(dev)
+    graphs = []
+    cap_stream = torch.cuda.Stream(dev)
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        for j in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                call(sets[j], cap_stream)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i & 1].replay()
+    torch.cuda.synchronize(dev)
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    with torch.cuda.stream(cap_stream):
+        t0.record(cap_stream)
+        for i in range(args.steps):
+            graphs[i & 1].replay()
+        t1.record(cap_stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks.stop()
+    max_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms_per_step = max_ms / args.steps
+
+    # the append kernel alone: CUDA events around eager calls (one launch each)
+    kcalls = max(1, min(args.steps, args.kernel_steps))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kcalls)]
+    torch.cuda.synchronize(dev)
+    for i in range(kcalls):
+        ev[i][0].record(stream)
+        call(sets[i & 1], stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    kern_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    peak, peak_src = load_peak()
+    achieved = nbytes / (kern_ms / 1e3) / 1e9
+
+    # end to end: the new rows, tables and lengths copied from pinned host
+    # memory every step; the result stays in the device cache (no read-back)
+    pinned = {n: getattr(host, n).pin_memory() for n in ("k_new", "v_new", "block_tables", "context_lens")}
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d = sets[0]
+    k = max(1, min(args.steps, args.e2e_steps))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(k + 3):
+        if it == 3:
+            a.record(stream)
+        for n, t in pinned.items():
+            getattr(d, n).copy_(t, non_blocking=True)
+        call(d, stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev) / k
+
+    result = {
+        "metric": APPEND_METRIC, "value": aggregate_throughput(nbytes, args.steps, max_ms / 1e3, world),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16->e4m3fn" if spec.kv_format == "fp8" else "bf16", "data": "synthetic",
+        "config": {
+            "workload": WORKLOADS[args.config], "batch": spec.batch, "new_tokens": spec.new_tokens,
+            "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "page_size": spec.page_size,
+            "seed": spec.seed, "algorithmic_bytes_per_step": nbytes,
+            "l2": f"two device copies of the inputs and caches alternated ({nbytes / 1e6:.0f} MB moved per call)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "us_per_call": ms_per_step * 1e3,
+        "frac_of_8tbs": aggregate_throughput(nbytes, args.steps, max_ms / 1e3, world) / world / NOMINAL_HBM_GBS,
+        "kernels_us": {"append": kern_ms * 1e3},
+        "timing": "CUDA-graph replays (one graph per input set, alternated); the append kernel from CUDA "
+                  "events around eager calls",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": load_traffic(args.config), "peak_source": peak_src, "kernel": "pa_kv_append_kernel"},
+        "clocks": clocks.summary(),
+        "e2e": {"value": nbytes * world / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 0, "steps": k, "ms_per_step": e2e_ms,
+                "note": "the appended rows stay in the device cache; nothing is read back"},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, nb, desc = append_oracle_run(host, args.cpu_budget)
+        result["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": desc, "seconds": secs}
+    return result
+
+
 def run_e2e(args, host, dev, pb, nbytes, world):
     """Same metric through the public call with host buffers: every step
     copies its inputs from pinned host memory and reads out + lse back."""
@@ -451,9 +606,36 @@ def run_e2e(args, host, dev, pb, nbytes, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": ms / k}
 
 
+def run_reference_append(args):
+    """The append oracle on host cores, each step a bounded sample."""
+    host = gen.make_append_inputs(gen.APPEND_SPECS[args.config])
+    budget = max(0.002, args.reference_seconds / (args.steps + args.warmup))
+    for w in range(args.warmup):
+        append_oracle_run(host, budget, start_seq=w)
+    secs, nbytes, desc = 0.0, 0, None
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s, b, d = append_oracle_run(host, budget, start_seq=args.warmup + i)
+        secs += s
+        nbytes += b
+        desc = desc or d
+    wall = time.perf_counter() - t0
+    value = nbytes / secs / 1e9
+    return {"metric": APPEND_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOADS[args.config]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"per step: {desc}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
 def run_reference(args):
     """The fp64 CPU oracle, as it stands, on host cores: each step is a
     bounded sample of the workload sized so the whole run takes minutes."""
+    if args.config in APPEND_CONFIGS:
+        return run_reference_append(args)
     spec = workload_spec(args)
     host = gen.make_inputs(spec)
     budget = max(0.002, args.reference_seconds / (args.steps + args.warmup))
@@ -506,7 +688,7 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-    result = run_ours(args, world, rank, local)
+    result = (run_append if args.config in APPEND_CONFIGS else run_ours)(args, world, rank, local)
     if rank == 0:
         print(json.dumps(result))
     if world > 1:

@@ -157,6 +157,38 @@ pa_status pa_decode_tidar(const void* q, const void* k_cache, const void* v_cach
 pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t num_splits,
                            const pa_shape* shape, void* out, float* lse, pa_stream_t stream);
 
+/* KV-cache append, the step before a decode: writes the T = shape->q_tokens
+ * new tokens of every sequence into its pages (the ROCm blog's paged cache,
+ * introduction item 1). Token t of sequence b takes logical position
+ * j = C_b + t, C_b = context_lens[b] (the tokens already cached, clamped to
+ * [0, max_blocks_per_seq * P]): slot j % P of page block_tables[b][j / P].
+ * For every kv head g the row k_new[b][t][g][:] (v_new likewise) goes to
+ * k_cache[page][slot][g][:].
+ *  - k_new, v_new: bf16 [B, T, Hkv, D], contiguous; k_cache, v_cache: bf16
+ *    [num_pages, P, Hkv, D]. D in {64, 128, 256}; num_q_heads is not used.
+ *  - context_lens is read, not advanced: the caller adds T after the call.
+ *  - Positions at or past max_blocks_per_seq * P, and page ids outside
+ *    [0, num_pages), are skipped (nothing written, no fault).
+ *  - Rows of two (b, t) that land in the same slot: one of them wins.
+ * Errors as for pa_decode; no workspace, no allocation, graph-capturable. */
+pa_status pa_kv_append(const void* k_new, const void* v_new, const int32_t* block_tables,
+                       const int32_t* context_lens, const pa_shape* shape, void* k_cache, void* v_cache,
+                       pa_stream_t stream);
+
+/* fp8 KV-cache append: as pa_kv_append, quantising each written row (token,
+ * kv head) to OCP e4m3fn with its own symmetric scale, computed when the
+ * cache is written (the MSLK page: native fp8 with a symmetric per-token
+ * scale, OCP e4m3fn; its review asks for scales at write time). With x the
+ * bf16 row widened to float32:
+ *     scale = amax_d |x_d| / 448   (IEEE float32 division; 1 if amax = 0)
+ *     code_d = e4m3fn(x_d / scale) (float32 division, round to nearest even,
+ *                                   magnitudes past 448 saturate to 448)
+ * scale goes to k_scale[page][slot][g] (v_scale likewise), fp32
+ * [num_pages, P, Hkv], the layout pa_decode_fp8 reads. x must be finite. */
+pa_status pa_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* block_tables,
+                           const int32_t* context_lens, const pa_shape* shape, uint8_t* k_cache, uint8_t* v_cache,
+                           float* k_scale, float* v_scale, pa_stream_t stream);
+
 /* pa_decode without a caller-provided workspace (the papers have no
  * counterpart; this is a convenience of this library). Some callers cannot
  * allocate device memory at the point where they decode: a plug-in that is

@@ -53,6 +53,8 @@ _SIGNATURES = {
     "pa_decode_tidar": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_reduce": (ctypes.c_int, [_P, _P, ctypes.c_int32, ctypes.POINTER(PaShape), _P, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pa_kv_append": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PaShape), _P, _P, _P]),
+    "pa_kv_append_fp8": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
     "pa_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32)]),
     "pa_decode_profile_events": (ctypes.c_int, [_P, _P]),
     "pa_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float, _P, _P,
@@ -172,6 +174,26 @@ def decode_inputs(inp, **kw):
     return decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale,
                   k_scale=inp.k_scale, v_scale=inp.v_scale, k_scratch=inp.k_scratch, v_scratch=inp.v_scratch,
                   **kw)
+
+
+def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+              k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor] = None,
+              v_scale: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Appends k_new/v_new [B, T, Hkv, D] (bf16) at positions context_lens[b] + t
+    through pa_kv_append, or pa_kv_append_fp8 when the caches are uint8
+    (e4m3fn codes; k_scale/v_scale [num_pages, P, Hkv] fp32 are written)."""
+    _need_contig(k_new=k_new, v_new=v_new, block_tables=block_tables, context_lens=context_lens,
+                 k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale)
+    B, T, Hkv, D = k_new.shape
+    shape = PaShape(B, T, Hkv, Hkv, D, k_cache.shape[1], k_cache.shape[0], block_tables.shape[1])
+    args = [_ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens), ctypes.byref(shape),
+            _ptr(k_cache), _ptr(v_cache)]
+    if k_cache.dtype == torch.uint8:
+        st = lib().pa_kv_append_fp8(*args, _ptr(k_scale), _ptr(v_scale), _stream(stream))
+        _check(st, "pa_kv_append_fp8")
+    else:
+        st = lib().pa_kv_append(*args, _stream(stream))
+        _check(st, "pa_kv_append")
 
 
 def split_workspace_views(workspace: torch.Tensor, B: int, T: int, Hq: int, S: int, D: int):

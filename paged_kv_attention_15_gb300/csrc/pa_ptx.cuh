@@ -197,6 +197,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return r;
 }
 
+// Two floats -> two e4m3fn codes, round to nearest even, magnitudes past 448
+// saturate to 448 (NaN stays NaN); `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Byte permute: result byte i = selector nibble i picks from {b (bytes 4-7), a (bytes 0-3)}.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;

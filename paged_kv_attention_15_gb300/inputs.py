@@ -43,6 +43,8 @@ _STREAM_K = 4
 _STREAM_V = 5
 _STREAM_KS = 6
 _STREAM_VS = 7
+_STREAM_KNEW = 8
+_STREAM_VNEW = 9
 
 # Elements per generator chunk (whole pages are kept together).
 _CHUNK_ELEMS = 1 << 22
@@ -319,3 +321,89 @@ def _poison(k, v, k_scale, v_scale, bt, lens, npages, pool, P):
 def custom_spec(name="custom", **kw) -> DecodeSpec:
     """A DecodeSpec for ad-hoc shapes (tests)."""
     return DecodeSpec(name=name, **kw)
+
+
+# ---------------------------------------------------------------------------
+# KV-cache append (the step before a decode)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class AppendSpec:
+    """Shape and value recipe of one KV-cache append: B sequences that cache
+    C_b tokens each receive T new tokens (K and V rows N(0,1) in bf16)."""
+
+    name: str
+    batch: int
+    new_tokens: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    context_lens: Optional[Sequence[int]] = None
+    ctx_range: Optional[tuple] = None
+    kv_format: str = "bf16"
+    pool_pages: Optional[int] = None
+    max_blocks_per_seq: Optional[int] = None
+    seed: int = 0
+
+
+# Append workloads: a prefill chunk of 512 tokens per sequence in the GQA
+# geometry (bf16) and in the fp8 geometry, and one decode step (T = 1).
+APPEND_SPECS = {
+    "append": AppendSpec("append", batch=64, new_tokens=512, num_kv_heads=8, head_dim=128, page_size=16,
+                         ctx_range=(0, 4096), max_blocks_per_seq=(4096 + 512) // 16, seed=5),
+    "append_fp8": AppendSpec("append_fp8", batch=64, new_tokens=512, num_kv_heads=2, head_dim=256, page_size=16,
+                             ctx_range=(0, 8192), kv_format="fp8", max_blocks_per_seq=(8192 + 512) // 16, seed=6),
+    "append_step": AppendSpec("append_step", batch=32, new_tokens=1, num_kv_heads=8, head_dim=128, page_size=16,
+                              ctx_range=(512, 8192), max_blocks_per_seq=8192 // 16 + 1, seed=7),
+}
+
+
+@dataclasses.dataclass
+class AppendInputs:
+    """Host (CPU) tensors of one append problem. The caches hold earlier
+    contents everywhere (the slots the append overwrites included); the
+    block tables cover C_b + T tokens of every sequence."""
+
+    spec: AppendSpec
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    block_tables: torch.Tensor
+    context_lens: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+
+    def tensors(self):
+        names = ["k_new", "v_new", "block_tables", "context_lens", "k_cache", "v_cache", "k_scale", "v_scale"]
+        return {n: getattr(self, n) for n in names if getattr(self, n) is not None}
+
+    def to(self, device, non_blocking: bool = False) -> "AppendInputs":
+        moved = {n: t.to(device, non_blocking=non_blocking) for n, t in self.tensors().items()}
+        return dataclasses.replace(self, **moved)
+
+    def clone(self) -> "AppendInputs":
+        return dataclasses.replace(self, **{n: t.clone() for n, t in self.tensors().items()})
+
+    def numpy_bits(self):
+        return DecodeInputs.numpy_bits(self)
+
+
+def make_append_inputs(spec: AppendSpec) -> AppendInputs:
+    """Pool, block tables and earlier cache contents as for a decode over
+    C_b + T tokens (make_inputs), then context_lens = C_b and the new rows."""
+    B, T, Hkv, D = spec.batch, spec.new_tokens, spec.num_kv_heads, spec.head_dim
+    lens = draw_context_lens(spec)
+    base = make_inputs(DecodeSpec(
+        name=spec.name, batch=B, q_tokens=1, num_q_heads=Hkv, num_kv_heads=Hkv, head_dim=D,
+        page_size=spec.page_size, context_lens=tuple(int(c) + T for c in lens), kv_format=spec.kv_format,
+        pool_pages=spec.pool_pages, max_blocks_per_seq=spec.max_blocks_per_seq, seed=spec.seed))
+    rows = max(1, _CHUNK_ELEMS // (T * Hkv * D))
+    return AppendInputs(
+        spec=spec,
+        k_new=_normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_KNEW, rows),
+        v_new=_normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_VNEW, rows),
+        block_tables=base.block_tables,
+        context_lens=torch.from_numpy(np.asarray(lens, dtype=np.int32)),
+        k_cache=base.k_cache, v_cache=base.v_cache, k_scale=base.k_scale, v_scale=base.v_scale)
+

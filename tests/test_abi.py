@@ -111,6 +111,25 @@ def test_choose_splits_rejects_bad_shapes(lib):
     assert lib.pa_decode_choose_splits(ctypes.byref(shape(q_tokens=0)), 0) == -1
 
 
+def test_append_validation(lib):
+    def call(s, fp8=False, **kw):
+        a = dict(kn=FAKE, vn=FAKE, bt=FAKE, cl=FAKE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE)
+        a.update(kw)
+        if fp8:
+            return lib.pa_kv_append_fp8(a["kn"], a["vn"], a["bt"], a["cl"], ctypes.byref(s), a["kc"], a["vc"],
+                                        a["ks"], a["vs"], None)
+        return lib.pa_kv_append(a["kn"], a["vn"], a["bt"], a["cl"], ctypes.byref(s), a["kc"], a["vc"], None)
+
+    assert call(shape(head_dim=96)) == pb.PA_ERR_UNSUPPORTED
+    assert call(shape(q_tokens=0)) == pb.PA_ERR_INVALID_ARG
+    assert call(shape(), kn=None) == pb.PA_ERR_INVALID_ARG
+    assert call(shape(), vc=FAKE + 8) == pb.PA_ERR_INVALID_ARG          # misaligned
+    assert call(shape(), fp8=True, ks=None) == pb.PA_ERR_INVALID_ARG
+    assert call(shape(batch=0)) == pb.PA_OK                              # nothing to do, no launch
+    assert call(shape(batch=0), fp8=True) == pb.PA_OK
+    assert lib.pa_kv_append(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None) == pb.PA_ERR_INVALID_ARG
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pb, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(pb, "_lib", None)
