@@ -35,6 +35,10 @@ changes). Readings of what the pages leave open:
     the OCP e4m3fn definition (bias 7, no infinities, S.1111.111 is NaN).
   * Draft-block mode: every draft token attends to the whole paged prefix
     and to all T scratch tokens of its sequence (no mask inside the block).
+    With a draft-block size bs (inputs["draft_block"]), draft token t sees
+    scratch token t' only if floor(t' / bs) <= floor(t / bs): the first
+    min(T, (floor(t / bs) + 1) * bs) scratch tokens. bs = 1 is causal,
+    bs >= T the unmasked mode.
   * Split-K (used to check the combine): split s of sequence b holds pages
     [s * pps, min((s + 1) * pps, n_b)) with pps = ceil(n_b / S) and
     n_b = ceil(C_b / P); the draft-block scratch tokens belong to split S-1.
@@ -110,11 +114,22 @@ def _paged_rows(cache: np.ndarray, scales: Optional[np.ndarray], kv_format: str,
     return out
 
 
+def visible_scratch(inputs: dict, t: int) -> int:
+    """How many scratch tokens (a prefix of the draft block) draft token t
+    sees: all T, or min(T, (floor(t / bs) + 1) * bs) with a block size bs."""
+    T = inputs["k_scratch"].shape[1]
+    bs = inputs.get("draft_block")
+    if bs is None:
+        return T
+    return min(T, (t // int(bs) + 1) * int(bs))
+
+
 def keys_values(inputs: dict, b: int, g: int, page_range: Optional[Tuple[int, int]] = None,
-                with_scratch: bool = True) -> Tuple[np.ndarray, np.ndarray]:
+                with_scratch: bool = True, scratch_count: Optional[int] = None) -> Tuple[np.ndarray, np.ndarray]:
     """Keys and values (float64, [N, D]) of sequence b, kv head g: the paged
     tokens (all of them, or those of the pages in page_range), then the
-    draft-block scratch tokens when present and with_scratch is set."""
+    draft-block scratch tokens (all, or the first scratch_count) when present
+    and with_scratch is set."""
     P = inputs["k_cache"].shape[1]
     ctx = max(0, int(inputs["context_lens"][b]))
     kv_format = inputs["kv_format"]
@@ -126,9 +141,20 @@ def keys_values(inputs: dict, b: int, g: int, page_range: Optional[Tuple[int, in
     ks = _paged_rows(inputs["k_cache"], inputs.get("k_scale"), kv_format, bt_row, ctx, P, g)[first:last]
     vs = _paged_rows(inputs["v_cache"], inputs.get("v_scale"), kv_format, bt_row, ctx, P, g)[first:last]
     if with_scratch and inputs.get("k_scratch") is not None:
-        ks = np.concatenate([ks, bf16_bits_to_f64(inputs["k_scratch"][b, :, g, :])], axis=0)
-        vs = np.concatenate([vs, bf16_bits_to_f64(inputs["v_scratch"][b, :, g, :])], axis=0)
+        n = inputs["k_scratch"].shape[1] if scratch_count is None else scratch_count
+        ks = np.concatenate([ks, bf16_bits_to_f64(inputs["k_scratch"][b, :n, g, :])], axis=0)
+        vs = np.concatenate([vs, bf16_bits_to_f64(inputs["v_scratch"][b, :n, g, :])], axis=0)
     return ks, vs
+
+
+def _by_key_set(inputs: dict, sel):
+    """Groups query rows (t, h) by the scratch tokens their draft token sees
+    (one group without a scratch block): {scratch count or None: rows}."""
+    groups = {}
+    for (t, h) in sel:
+        n = visible_scratch(inputs, t) if inputs.get("k_scratch") is not None else None
+        groups.setdefault(n, []).append((t, h))
+    return groups
 
 
 # ---------------------------------------------------------------------------
@@ -184,12 +210,13 @@ def decode(inputs: dict, scale: float,
             sel = [(t, h) for t in range(T) for h in range(g * G, (g + 1) * G)]
         else:
             sel = want[(b, g)]
-        keys, values = keys_values(inputs, b, g)
-        q_rows = np.stack([bf16_bits_to_f64(q[b, t, h]) for (t, h) in sel])
-        o, l = attend(q_rows, keys, values, scale)
-        for i, (t, h) in enumerate(sel):
-            out[b, t, h] = o[i]
-            lse[b, t, h] = l[i]
+        for n, group in _by_key_set(inputs, sel).items():
+            keys, values = keys_values(inputs, b, g, scratch_count=n)
+            q_rows = np.stack([bf16_bits_to_f64(q[b, t, h]) for (t, h) in group])
+            o, l = attend(q_rows, keys, values, scale)
+            for i, (t, h) in enumerate(group):
+                out[b, t, h] = o[i]
+                lse[b, t, h] = l[i]
     return out, lse
 
 
@@ -219,14 +246,15 @@ def decode_split(inputs: dict, scale: float, num_splits: int):
         n_pages = -(-ctx // P)
         for s, (a, e) in enumerate(split_page_ranges(n_pages, S)):
             for g in range(Hkv):
-                keys, values = keys_values(inputs, b, g, page_range=(a, e),
-                                           with_scratch=(s == S - 1))
                 sel = [(t, h) for t in range(T) for h in range(g * G, (g + 1) * G)]
-                q_rows = np.stack([bf16_bits_to_f64(q[b, t, h]) for (t, h) in sel])
-                o, l = attend(q_rows, keys, values, scale)
-                for i, (t, h) in enumerate(sel):
-                    part_out[b, t, h, s] = o[i]
-                    part_lse[b, t, h, s] = l[i]
+                for n, group in _by_key_set(inputs, sel).items():
+                    keys, values = keys_values(inputs, b, g, page_range=(a, e),
+                                               with_scratch=(s == S - 1), scratch_count=n)
+                    q_rows = np.stack([bf16_bits_to_f64(q[b, t, h]) for (t, h) in group])
+                    o, l = attend(q_rows, keys, values, scale)
+                    for i, (t, h) in enumerate(group):
+                        part_out[b, t, h, s] = o[i]
+                        part_lse[b, t, h, s] = l[i]
     return part_out, part_lse
 
 

@@ -264,6 +264,65 @@ def test_draft_block_equals_extra_pages():
     np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-13)
 
 
+def masked_by_extra_tokens(oi, scale, bs):
+    """Draft token t of a block-masked draft block computed as a plain decode
+    (no scratch) whose sequence carries, after its prefix, the scratch
+    tokens that t may see, appended as extra paged tokens."""
+    B, T, Hq, D = oi["q"].shape
+    P = oi["k_cache"].shape[1]
+    Hkv = oi["k_cache"].shape[2]
+    out = np.full((B, T, Hq, D), np.nan)
+    lse = np.full((B, T, Hq), np.nan)
+    for t in range(T):
+        n = T if bs is None else min(T, (t // bs + 1) * bs)
+        pool = oi["k_cache"].shape[0]
+        k = np.concatenate([oi["k_cache"], np.zeros((B, P, Hkv, D), np.uint16)], 0)
+        v = np.concatenate([oi["v_cache"], np.zeros((B, P, Hkv, D), np.uint16)], 0)
+        bt = np.concatenate([oi["block_tables"], np.full((B, 1), -1, np.int32)], 1)
+        ctx = oi["context_lens"].copy()
+        for b in range(B):
+            assert ctx[b] % P == 0  # the extra tokens start a fresh page
+            k[pool + b, :n] = oi["k_scratch"][b, :n]
+            v[pool + b, :n] = oi["v_scratch"][b, :n]
+            bt[b, ctx[b] // P] = pool + b
+            ctx[b] += n
+        plain = dict(oi, q=oi["q"][:, t:t + 1], k_cache=k, v_cache=v, block_tables=bt, context_lens=ctx,
+                     k_scratch=None, v_scratch=None, draft_block=None)
+        o, l = oracle.decode(plain, scale)
+        out[:, t], lse[:, t] = o[:, 0], l[:, 0]
+    return out, lse
+
+
+@pytest.mark.parametrize("bs", [1, 2, 3, 5, 8])
+def test_block_masked_draft_equals_extra_tokens(bs):
+    """Causal (bs 1) and block-causal draft blocks: token t sees the first
+    min(T, (t // bs + 1) * bs) scratch tokens; bs >= T is the unmasked mode."""
+    spec = small_spec(draft_scratch=True, q_tokens=5, page_size=16, context_lens=(32, 0, 48))
+    inp = gen.make_inputs(spec)
+    oi = dict(ora_inputs(inp), draft_block=bs)
+    out, lse = oracle.decode(oi, inp.scale)
+    out2, lse2 = masked_by_extra_tokens(oi, inp.scale, bs)
+    np.testing.assert_allclose(out, out2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-13)
+    if bs >= 5:
+        ref, ref_lse = oracle.decode(ora_inputs(inp), inp.scale)
+        np.testing.assert_array_equal(out, ref)
+    # the split variant keeps the mask on the last split
+    po, pl = oracle.decode_split(oi, inp.scale, 3)
+    co, cl = oracle.combine(po, pl)
+    np.testing.assert_allclose(co, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(cl, lse, rtol=0, atol=1e-12)
+
+
+def test_planted_mask_slip_is_caught(monkeypatch):
+    """Seeing one scratch token too many fails the extra-token pin."""
+    orig = pa_oracle.visible_scratch
+    monkeypatch.setattr(pa_oracle, "visible_scratch", lambda inputs, t: min(orig(inputs, t) + 1,
+                                                                             inputs["k_scratch"].shape[1]))
+    with pytest.raises(AssertionError):
+        test_block_masked_draft_equals_extra_tokens(1)
+
+
 # ---------------------------------------------------------------------------
 # Closed forms
 # ---------------------------------------------------------------------------
