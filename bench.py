@@ -58,6 +58,10 @@ WORKLOADS = {
     "long": "long-context split-K decode: B4 T1 Hq64 Hkv8 D128 P64 ctx 131072 bf16",
     "fp8": "native fp8 KV decode: B64 T1 Hq32 Hkv2 D256 P16 ctx U[1024,16384] e4m3fn KV + fp32 per-token scale",
     "tidar": "TiDAR draft-block decode: B16 T8 Hq32 Hkv8 D128 P16 ctx U[2048,8192] + scratch KV [16,8,8,128] bf16",
+    "tidar_causal": "TiDAR draft-block decode with a causal draft: B16 T8 Hq32 Hkv8 D128 P16 ctx U[2048,8192] "
+                    "+ scratch KV [16,8,8,128] bf16, draft token t sees scratch tokens <= t",
+    "tidar_long": "TiDAR 16-token draft in blocks of 4: B16 T16 Hq32 Hkv8 D128 P16 ctx U[2048,8192] "
+                  "+ scratch KV [16,16,8,128] bf16 (64 query rows per kv head)",
     "append": "KV-cache append of a 512-token chunk: B64 T512 Hkv8 D128 P16 ctx U[0,4096] bf16",
     "append_fp8": "KV-cache append with e4m3fn quantisation: B64 T512 Hkv2 D256 P16 ctx U[0,8192] "
                   "bf16 rows -> e4m3fn + fp32 per-token scale",
@@ -246,7 +250,10 @@ def aggregate_throughput(bytes_per_step: int, steps: int, max_elapsed_s: float, 
 def _oracle_bits(inp):
     import oracle
 
-    return oracle.as_oracle_inputs(inp.numpy_bits(), inp.spec.kv_format)
+    oi = oracle.as_oracle_inputs(inp.numpy_bits(), inp.spec.kv_format)
+    if inp.spec.draft_block is not None:
+        oi["draft_block"] = inp.spec.draft_block
+    return oi
 
 
 def _unit_rows(spec, b, g):

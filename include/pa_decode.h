@@ -49,7 +49,8 @@
  *    pa_decode_device_error().
  *
  * Supported: D in {64, 128, 256} (fp8: {128, 256}); P in {16, 32, 64, 128,
- * 256}; M = G * T <= 32 query rows per kv head; fp8 needs Hkv <= 8.
+ * 256}; M = G * T <= 64 query rows per kv head (more than 32 rows: D in {64,
+ * 128}, bf16 pages); fp8 needs Hkv <= 8.
  * Anything else returns PA_ERR_UNSUPPORTED.
  *
  * num_splits:
@@ -146,6 +147,22 @@ pa_status pa_decode_tidar(const void* q, const void* k_cache, const void* v_cach
                           const pa_shape* shape, float scale, void* out, float* lse,
                           int32_t num_splits, void* workspace, size_t workspace_bytes,
                           pa_stream_t stream);
+
+/* Block-masked draft-block (TiDAR) decode: as pa_decode_tidar, but draft
+ * token t sees only the scratch tokens t' with t' / draft_block <=
+ * t / draft_block (integer division): the first
+ * min(T, (t / draft_block + 1) * draft_block) of them. draft_block = 1 is a
+ * causal draft, draft_block >= T the unmasked pa_decode_tidar; draft_block
+ * < 1 is PA_ERR_INVALID_ARG. The paged prefix stays visible to every draft
+ * token. The ROCm blog leaves the mask inside the draft block open
+ * (introduction items 1-2: a highly configurable attention pattern); this is
+ * the block-causal family of it. */
+pa_status pa_decode_tidar_masked(const void* q, const void* k_cache, const void* v_cache,
+                                 const void* k_scratch, const void* v_scratch,
+                                 const int32_t* block_tables, const int32_t* context_lens,
+                                 const pa_shape* shape, float scale, int32_t draft_block, void* out,
+                                 float* lse, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                 pa_stream_t stream);
 
 /* Split-K combine (the MSLK page's pa_decode_reduce): for every (b, t, h),
  * M = max_s lse_s, w_s = exp(lse_s - M), out = sum_s w_s part_out_s / sum_s w_s,

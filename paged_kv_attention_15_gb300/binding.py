@@ -51,6 +51,8 @@ _SIGNATURES = {
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_tidar": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
+    "pa_decode_tidar_masked": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float,
+                                              ctypes.c_int32, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "pa_decode_reduce": (ctypes.c_int, [_P, _P, ctypes.c_int32, ctypes.POINTER(PaShape), _P, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_kv_append": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PaShape), _P, _P, _P]),
@@ -135,12 +137,15 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
            v_scale: Optional[torch.Tensor] = None, k_scratch: Optional[torch.Tensor] = None,
            v_scratch: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
            lse: Optional[torch.Tensor] = None, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
-           want_lse: bool = True, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Paged decode through pa_decode / pa_decode_fp8 / pa_decode_tidar.
+           want_lse: bool = True, stream=None, draft_block: Optional[int] = None
+           ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Paged decode through pa_decode / pa_decode_fp8 / pa_decode_tidar /
+    pa_decode_tidar_masked.
 
     The fp8 entry point is used when k_cache is uint8 (e4m3fn codes, with
-    k_scale/v_scale); the draft-block entry point when k_scratch is given.
-    out, lse and the workspace are allocated here when not passed in."""
+    k_scale/v_scale); the draft-block entry point when k_scratch is given,
+    its block-masked form when draft_block is given too. out, lse and the
+    workspace are allocated here when not passed in."""
     _need_contig(q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables, context_lens=context_lens,
                  k_scale=k_scale, v_scale=v_scale, k_scratch=k_scratch, v_scratch=v_scratch, out=out, lse=lse)
     shape = make_shape(q, k_cache, block_tables)
@@ -159,6 +164,12 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
         st = L.pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                              _ptr(block_tables), _ptr(context_lens), *tail)
         _check(st, "pa_decode_fp8")
+    elif k_scratch is not None and draft_block is not None:
+        st = L.pa_decode_tidar_masked(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scratch), _ptr(v_scratch),
+                                      _ptr(block_tables), _ptr(context_lens), ctypes.byref(shape), float(scale),
+                                      int(draft_block), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace),
+                                      ws_bytes, _stream(stream))
+        _check(st, "pa_decode_tidar_masked")
     elif k_scratch is not None:
         st = L.pa_decode_tidar(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scratch), _ptr(v_scratch),
                                _ptr(block_tables), _ptr(context_lens), *tail)
@@ -170,7 +181,10 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
 
 
 def decode_inputs(inp, **kw):
-    """decode() on a DecodeInputs bundle already on the device."""
+    """decode() on a DecodeInputs bundle already on the device (its spec's
+    draft_block selects the block-masked draft entry point)."""
+    if inp.spec.draft_block is not None and "draft_block" not in kw:
+        kw["draft_block"] = inp.spec.draft_block
     return decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale,
                   k_scale=inp.k_scale, v_scale=inp.v_scale, k_scratch=inp.k_scratch, v_scratch=inp.v_scratch,
                   **kw)

@@ -139,7 +139,8 @@ pa_status check_shape(const pa_shape* s, Kind kind) {
   }
   if (!pow2_in(s->page_size, 16, 256)) return PA_ERR_UNSUPPORTED;
   const int64_t M = (int64_t)(s->num_q_heads / s->num_kv_heads) * s->q_tokens;
-  if (M > 32) return PA_ERR_UNSUPPORTED;
+  if (M > 64) return PA_ERR_UNSUPPORTED;
+  if (M > 32 && (kind == Kind::kFp8 || D == 256)) return PA_ERR_UNSUPPORTED;  // four row tiles: D <= 128, bf16
   return PA_OK;
 }
 
@@ -167,15 +168,14 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   // With several heads per unit, a head's rows must fill whole m16 tiles or
   // share one evenly.
   if (H2 > 1 && (GT < 16 ? 16 % GT : GT % 16)) return false;
-  const int MT = (M + 15) / 16;
-  if (MT != 1 && MT != 2 && MT != 4) return false;
+  const int MT = M <= 16 ? 1 : (M <= 32 ? 2 : 4);  // rows past M are masked
   const int NGW = pa::kConsumerWarps / MT;
   const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
   if (NGW % HT) return false;
   const int NSL = NGW / HT, TS = pa::kStageRows / H2;
   if (TS % NSL) return false;
   const int TSL = TS / NSL;
-  if (TSL != 16 && TSL != 32) return false;
+  if (TSL != 16 && TSL != 32 && TSL != 64) return false;
   const SplitKernel k = pick_kernel(kind, D, MT, TSL);
   if (!k.fn) return false;
   g->GT = GT;
@@ -279,6 +279,7 @@ struct CallArgs {
   void* workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
+  int32_t draft_block = 0;  // TiDAR: 0 = no mask inside the draft block
 };
 
 pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t ev_split);
@@ -375,6 +376,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   p.num_pages = s.num_pages;
   p.num_splits = plan.balanced ? 0 : plan.splits;
   p.tidar = a.kind == Kind::kTidar ? 1 : 0;
+  p.draft_block = a.draft_block > 0 && a.draft_block < T ? a.draft_block : T;
   p.grid = plan.grid;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
   if (plan.ws_bytes) {
@@ -496,6 +498,17 @@ pa_status pa_decode_tidar(const void* q, const void* k_cache, const void* v_cach
   CallArgs a{Kind::kTidar, q, k_cache, v_cache, nullptr, nullptr, k_scratch, v_scratch, block_tables,
              context_lens, shape, scale, out, lse, num_splits, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream)};
+  return run_decode(a);
+}
+
+pa_status pa_decode_tidar_masked(const void* q, const void* k_cache, const void* v_cache, const void* k_scratch,
+                                 const void* v_scratch, const int32_t* block_tables, const int32_t* context_lens,
+                                 const pa_shape* shape, float scale, int32_t draft_block, void* out, float* lse,
+                                 int32_t num_splits, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (draft_block < 1) return PA_ERR_INVALID_ARG;
+  CallArgs a{Kind::kTidar, q, k_cache, v_cache, nullptr, nullptr, k_scratch, v_scratch, block_tables,
+             context_lens, shape, scale, out, lse, num_splits, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), draft_block};
   return run_decode(a);
 }
 

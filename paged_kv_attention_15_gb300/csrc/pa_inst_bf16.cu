@@ -14,9 +14,12 @@ static SplitKernel by_tiles(int row_tiles, int slice) {
   if (row_tiles == 1 && slice == 16) return entry<D, 1, 16>();
   if (row_tiles == 2 && slice == 16) return entry<D, 2, 16>();
   if (row_tiles == 2 && slice == 32) return entry<D, 2, 32>();
-  if constexpr (D == 128) {
+  if constexpr (D == 128 || D == 64) {
+    // four row tiles: up to 64 query rows (long draft blocks); a slice of
+    // 64 tokens when one kv head fills the tiles
     if (row_tiles == 4 && slice == 16) return entry<D, 4, 16>();
     if (row_tiles == 4 && slice == 32) return entry<D, 4, 32>();
+    if (row_tiles == 4 && slice == 64) return entry<D, 4, 64>();
   }
   return SplitKernel{nullptr, 0, 0};
 }

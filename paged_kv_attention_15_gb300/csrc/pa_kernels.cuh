@@ -78,6 +78,7 @@ struct SplitParams {
   int TP;          // scratch rows per box: T rounded up to a multiple of 8
   int num_splits;  // >= 1: explicit splits (grid = units x splits); 0: balanced (grid = CTAs)
   int tidar;       // 1: each sequence also attends to its T scratch tokens
+  int draft_block; // draft token t sees scratch tokens [0, min(T, (t / draft_block + 1) * draft_block))
   int grid;        // CTAs of a balanced launch
   float scale_log2;
 };
@@ -122,7 +123,7 @@ struct Cfg {
   static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1024 to align the dynamic base
   static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
   static_assert(MT == 1 || MT == 2 || MT == 4, "unsupported row tiles");
-  static_assert(TSL == 16 || TSL == 32, "unsupported warp slice");
+  static_assert(TSL == 16 || TSL == 32 || TSL == 64, "unsupported warp slice");
 };
 
 // ----------------------------------------------------------------- schedule
@@ -480,14 +481,21 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   const int mt = warp % MT;
   const int gi = warp / MT;
   const int hl_base = (mt * 16) / GT;
-  const int ht = GT >= 16 ? 1 : min(16 / GT, H2 - hl_base);
-  const int hl = hl_base + gi % ht;
+  const int ht = GT >= 16 ? 1 : max(1, min(16 / GT, H2 - hl_base));
+  const int hl = min(hl_base + gi % ht, H2 - 1);  // (a tile of padding rows only reads head H2-1)
   const int ts = gi / ht;
   const int r = lane >> 2;
   const int c4 = lane & 3;
   const int rho0 = mt * 16 + r, rho1 = rho0 + 8;
   const bool rok0 = rho0 < p.M && rho0 / GT == hl;  // rows this warp computes
   const bool rok1 = rho1 < p.M && rho1 / GT == hl;
+  // Scratch tokens the rows' draft tokens see (t = (rho % GT) / G): all T,
+  // or the draft-block prefix of a block-masked draft.
+  auto visible = [&](int rho) {
+    const int t = (rho % GT) / p.G;
+    return min(p.T, (t / p.draft_block + 1) * p.draft_block);
+  };
+  const int vis0 = visible(rho0), vis1 = visible(rho1);
   const float NEG_INF = -__int_as_float(0x7f800000);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* redml = reinterpret_cast<float*>(smem + C::OFF_REDML);
@@ -663,7 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               const int tok = tb + i * 8 + 2 * c4 + (e & 1);
               float f = s[i][e] * sl;
               if (FP8) f *= ksc[tok * p.Hkv + g];
-              s[i][e] = (tok < valid && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
+              const int lim = scr ? (e < 2 ? vis0 : vis1) : valid;
+              s[i][e] = (tok < lim && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
             }
           }
           float mx0 = NEG_INF, mx1 = NEG_INF;

@@ -69,6 +69,7 @@ class DecodeSpec:
     pool_pages: Optional[int] = None  # None: exactly the pages in use
     max_blocks_per_seq: Optional[int] = None  # None: from the largest context
     seed: int = 0
+    draft_block: Optional[int] = None  # block-masked draft: token t sees the scratch blocks up to its own
 
     @property
     def group(self) -> int:
@@ -95,6 +96,14 @@ SPECS = {
     "tidar": DecodeSpec("tidar", batch=16, q_tokens=8, num_q_heads=32, num_kv_heads=8,
                         head_dim=128, page_size=16, ctx_range=(2048, 8192),
                         draft_scratch=True, max_blocks_per_seq=8192 // 16, seed=4),
+    # Draft-block variants: the TiDAR workload with a causal draft, and a
+    # 16-token draft (64 query rows per kv head) in blocks of 4.
+    "tidar_causal": DecodeSpec("tidar_causal", batch=16, q_tokens=8, num_q_heads=32, num_kv_heads=8,
+                               head_dim=128, page_size=16, ctx_range=(2048, 8192), draft_scratch=True,
+                               max_blocks_per_seq=8192 // 16, seed=4, draft_block=1),
+    "tidar_long": DecodeSpec("tidar_long", batch=16, q_tokens=16, num_q_heads=32, num_kv_heads=8,
+                             head_dim=128, page_size=16, ctx_range=(2048, 8192), draft_scratch=True,
+                             max_blocks_per_seq=8192 // 16, seed=8, draft_block=4),
 }
 
 

@@ -53,7 +53,8 @@ def test_shape_validation_before_any_launch(lib):
     assert call_decode(lib, shape(head_dim=96)) == pb.PA_ERR_UNSUPPORTED
     assert call_decode(lib, shape(page_size=8)) == pb.PA_ERR_UNSUPPORTED
     assert call_decode(lib, shape(page_size=48)) == pb.PA_ERR_UNSUPPORTED
-    assert call_decode(lib, shape(num_q_heads=64, num_kv_heads=1)) == pb.PA_ERR_UNSUPPORTED  # 64 rows
+    assert call_decode(lib, shape(num_q_heads=128, num_kv_heads=1)) == pb.PA_ERR_UNSUPPORTED  # 128 rows
+    assert call_decode(lib, shape(num_q_heads=64, num_kv_heads=1, head_dim=256)) == pb.PA_ERR_UNSUPPORTED
     assert call_decode(lib, shape(q_tokens=0)) == pb.PA_ERR_INVALID_ARG
     assert call_decode(lib, shape(num_pages=0)) == pb.PA_ERR_INVALID_ARG
     assert call_decode(lib, shape(batch=-1)) == pb.PA_ERR_INVALID_ARG
@@ -84,6 +85,14 @@ def test_fp8_and_tidar_validation(lib):
                              None) == pb.PA_ERR_UNSUPPORTED  # > 8 kv heads
     assert lib.pa_decode_tidar(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, None, 1,
                                None, 0, None) == pb.PA_ERR_INVALID_ARG
+    for bs in (0, -3):
+        assert lib.pa_decode_tidar_masked(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, bs, FAKE,
+                                          None, 1, None, 0, None) == pb.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_tidar_masked(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, 2, FAKE,
+                                      None, 1, None, 0, None) == pb.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             ctypes.byref(shape(q_tokens=8, num_q_heads=16, num_kv_heads=2)), 0.1, FAKE, None, 1,
+                             None, 0, None) == pb.PA_ERR_UNSUPPORTED  # fp8: at most 32 rows
 
 
 def test_reduce_validation(lib):

@@ -28,7 +28,10 @@ def tol_of(spec):
 
 
 def ora_inputs(inp):
-    return oracle.as_oracle_inputs(inp.numpy_bits(), inp.spec.kv_format)
+    oi = oracle.as_oracle_inputs(inp.numpy_bits(), inp.spec.kv_format)
+    if inp.spec.draft_block is not None:
+        oi["draft_block"] = inp.spec.draft_block
+    return oi
 
 
 def gpu_decode(inp, num_splits=0, dev=None, **kw):
@@ -131,6 +134,44 @@ TIDAR_SWEEP = [
 @pytest.mark.parametrize("case", TIDAR_SWEEP, ids=[str(i) for i in range(len(TIDAR_SWEEP))])
 @pytest.mark.parametrize("num_splits", [0, 1, 3])
 def test_tidar_sweep(case, num_splits):
+    check_full(gen.make_inputs(spec(**case)), num_splits)
+
+
+MASKED = [
+    (dict(draft_scratch=True, q_tokens=8, num_q_heads=8, num_kv_heads=2), 1),
+    (dict(draft_scratch=True, q_tokens=8, num_q_heads=8, num_kv_heads=2), 3),
+    (dict(draft_scratch=True, q_tokens=8, num_q_heads=8, num_kv_heads=2), 4),
+    (dict(draft_scratch=True, q_tokens=5, num_q_heads=4, num_kv_heads=1, context_lens=(0, 16, 17, 250)), 2),
+    # long draft blocks: 64 rows of one kv head in four row tiles
+    (dict(draft_scratch=True, q_tokens=16, num_q_heads=8, num_kv_heads=2), 1),
+    (dict(draft_scratch=True, q_tokens=16, num_q_heads=8, num_kv_heads=2), 4),
+    (dict(draft_scratch=True, q_tokens=16, num_q_heads=8, num_kv_heads=2), 16),
+    (dict(draft_scratch=True, q_tokens=12, num_q_heads=8, num_kv_heads=2, context_lens=(3, 0, 100, 64)), 5),
+    (dict(draft_scratch=True, q_tokens=32, num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=64,
+          context_lens=(63, 64, 1, 400)), 8),
+]
+
+
+@pytest.mark.parametrize("case,bs", MASKED, ids=[str(i) for i in range(len(MASKED))])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_block_masked_draft_sweep(case, bs, num_splits):
+    inp = gen.make_inputs(spec(**case))
+    ref_out, ref_lse = oracle.decode(dict(ora_inputs(inp), draft_block=bs), inp.scale)
+    out, lse = to_np(*gpu_decode(inp, num_splits, draft_block=bs))
+    assert_match(out, lse, ref_out, ref_lse, tol_of(inp.spec))
+
+
+LONG_ROWS = [
+    dict(num_q_heads=64, num_kv_heads=1),                          # G 64
+    dict(q_tokens=10, num_q_heads=16, num_kv_heads=4),             # 40 rows, padded to four tiles
+    dict(q_tokens=16, num_q_heads=8, num_kv_heads=2, head_dim=64),
+    dict(draft_scratch=True, q_tokens=16, num_q_heads=8, num_kv_heads=2),  # unmasked long draft
+]
+
+
+@pytest.mark.parametrize("case", LONG_ROWS, ids=[str(i) for i in range(len(LONG_ROWS))])
+@pytest.mark.parametrize("num_splits", [0, 1, 5])
+def test_more_than_32_rows_per_kv_head(case, num_splits):
     check_full(gen.make_inputs(spec(**case)), num_splits)
 
 
@@ -275,7 +316,7 @@ def sample_rows(inp, n, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["gqa", "long", "fp8", "tidar"])
+@pytest.mark.parametrize("name", ["gqa", "long", "fp8", "tidar", "tidar_causal", "tidar_long"])
 def test_full_size_workload_sampled(name):
     inp = gen.make_inputs(gen.SPECS[name])
     out, lse = gpu_decode(inp, 0)
