@@ -14,6 +14,7 @@ from .pa_oracle import (  # noqa: F401
     decode_split,
     e4m3fn_table,
     e4m3fn_value,
+    f16_bits_to_f64,
     keys_values,
     split_page_ranges,
 )

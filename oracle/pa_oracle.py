@@ -33,6 +33,8 @@ changes). Readings of what the pages leave open:
     ceil(C_b / P) are never read.
   * fp8: x = value(code) * scale[page, slot, head]; the value of a code is
     the OCP e4m3fn definition (bias 7, no infinities, S.1111.111 is NaN).
+  * f16 format (the MSLK pull request's dense path is "f16/bf16"): q, the
+    caches and the scratch are IEEE binary16, widened exactly.
   * Draft-block mode: every draft token attends to the whole paged prefix
     and to all T scratch tokens of its sequence (no mask inside the block).
     With a draft-block size bs (inputs["draft_block"]), draft token t sees
@@ -66,6 +68,18 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     float32 whose upper 16 bits are the pattern and whose lower 16 are 0."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return b.view(np.float32).astype(np.float64)
+
+
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bit patterns (uint16) -> float64, exactly (1 sign, 5
+    exponent bits with bias 15, 10 mantissa bits; exponent 0 subnormal)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def widen16(bits: np.ndarray, kv_format: str) -> np.ndarray:
+    """16-bit rows of q (and of the 16-bit caches) to float64: f16 in the f16
+    format, bf16 otherwise (the fp8 format keeps a bf16 q)."""
+    return f16_bits_to_f64(bits) if kv_format == "f16" else bf16_bits_to_f64(bits)
 
 
 def e4m3fn_value(code: int) -> float:
@@ -105,8 +119,8 @@ def _paged_rows(cache: np.ndarray, scales: Optional[np.ndarray], kv_format: str,
         page = int(bt_row[j // page_size])
         n = min(page_size, ctx - j)
         raw = cache[page, :n, g, :]
-        if kv_format == "bf16":
-            out[j:j + n] = bf16_bits_to_f64(raw)
+        if kv_format in ("bf16", "f16"):
+            out[j:j + n] = widen16(raw, kv_format)
         elif kv_format == "fp8":
             out[j:j + n] = _E4M3FN[raw] * scales[page, :n, g].astype(np.float64)[:, None]
         else:
@@ -142,8 +156,8 @@ def keys_values(inputs: dict, b: int, g: int, page_range: Optional[Tuple[int, in
     vs = _paged_rows(inputs["v_cache"], inputs.get("v_scale"), kv_format, bt_row, ctx, P, g)[first:last]
     if with_scratch and inputs.get("k_scratch") is not None:
         n = inputs["k_scratch"].shape[1] if scratch_count is None else scratch_count
-        ks = np.concatenate([ks, bf16_bits_to_f64(inputs["k_scratch"][b, :n, g, :])], axis=0)
-        vs = np.concatenate([vs, bf16_bits_to_f64(inputs["v_scratch"][b, :n, g, :])], axis=0)
+        ks = np.concatenate([ks, widen16(inputs["k_scratch"][b, :n, g, :], kv_format)], axis=0)
+        vs = np.concatenate([vs, widen16(inputs["v_scratch"][b, :n, g, :], kv_format)], axis=0)
     return ks, vs
 
 
@@ -212,7 +226,7 @@ def decode(inputs: dict, scale: float,
             sel = want[(b, g)]
         for n, group in _by_key_set(inputs, sel).items():
             keys, values = keys_values(inputs, b, g, scratch_count=n)
-            q_rows = np.stack([bf16_bits_to_f64(q[b, t, h]) for (t, h) in group])
+            q_rows = np.stack([widen16(q[b, t, h], inputs["kv_format"]) for (t, h) in group])
             o, l = attend(q_rows, keys, values, scale)
             for i, (t, h) in enumerate(group):
                 out[b, t, h] = o[i]
@@ -250,7 +264,7 @@ def decode_split(inputs: dict, scale: float, num_splits: int):
                 for n, group in _by_key_set(inputs, sel).items():
                     keys, values = keys_values(inputs, b, g, page_range=(a, e),
                                                with_scratch=(s == S - 1), scratch_count=n)
-                    q_rows = np.stack([bf16_bits_to_f64(q[b, t, h]) for (t, h) in group])
+                    q_rows = np.stack([widen16(q[b, t, h], inputs["kv_format"]) for (t, h) in group])
                     o, l = attend(q_rows, keys, values, scale)
                     for i, (t, h) in enumerate(group):
                         part_out[b, t, h, s] = o[i]

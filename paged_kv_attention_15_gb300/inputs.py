@@ -64,7 +64,7 @@ class DecodeSpec:
     # Either explicit context lengths, or an inclusive uniform range.
     context_lens: Optional[Sequence[int]] = None
     ctx_range: Optional[tuple] = None
-    kv_format: str = "bf16"  # "bf16" or "fp8"
+    kv_format: str = "bf16"  # "bf16", "f16" (q, caches and out in f16) or "fp8"
     draft_scratch: bool = False  # TiDAR draft block: contiguous scratch KV
     pool_pages: Optional[int] = None  # None: exactly the pages in use
     max_blocks_per_seq: Optional[int] = None  # None: from the largest context
@@ -151,7 +151,7 @@ class DecodeInputs:
         def bits(t):
             if t is None:
                 return None
-            if t.dtype == torch.bfloat16:
+            if t.dtype in (torch.bfloat16, torch.float16):
                 return t.contiguous().view(torch.int16).numpy().view(np.uint16)
             return t.contiguous().numpy()
         return {n: bits(t) for n, t in self.tensors().items()}
@@ -190,9 +190,9 @@ def _parallel(fn, n: int) -> None:
         raise err[0]
 
 
-def _normal_bf16(shape, seed: int, stream: int, rows_per_chunk: int) -> torch.Tensor:
-    """N(0,1) float32 draws rounded to bf16 (round to nearest even), chunked on dim 0."""
-    out = torch.empty(shape, dtype=torch.bfloat16)
+def _normal_bf16(shape, seed: int, stream: int, rows_per_chunk: int, dtype=torch.bfloat16) -> torch.Tensor:
+    """N(0,1) float32 draws rounded to bf16 (or f16) by round to nearest even, chunked on dim 0."""
+    out = torch.empty(shape, dtype=dtype)
     n0 = shape[0]
     nchunks = max(1, -(-n0 // rows_per_chunk))
     row_elems = int(np.prod(shape[1:])) if len(shape) > 1 else 1
@@ -201,7 +201,7 @@ def _normal_bf16(shape, seed: int, stream: int, rows_per_chunk: int) -> torch.Te
         r0, r1 = c * rows_per_chunk, min(n0, (c + 1) * rows_per_chunk)
         buf = np.empty((r1 - r0) * row_elems, dtype=np.float32)
         _rng(seed, stream, c).standard_normal(out=buf, dtype=np.float32)
-        out[r0:r1] = torch.from_numpy(buf).view((r1 - r0,) + tuple(shape[1:])).to(torch.bfloat16)
+        out[r0:r1] = torch.from_numpy(buf).view((r1 - r0,) + tuple(shape[1:])).to(dtype)
 
     _parallel(fill, nchunks)
     return out
@@ -271,11 +271,12 @@ def make_inputs(spec: DecodeSpec, poison: bool = False) -> DecodeInputs:
 
     page_elems = P * Hkv * D
     rows_per_chunk = max(1, _CHUNK_ELEMS // page_elems)
-    q = _normal_bf16((B, T, Hq, D), spec.seed, _STREAM_Q, max(1, _CHUNK_ELEMS // (T * Hq * D)))
+    t16 = torch.float16 if spec.kv_format == "f16" else torch.bfloat16  # q, 16-bit caches, scratch
+    q = _normal_bf16((B, T, Hq, D), spec.seed, _STREAM_Q, max(1, _CHUNK_ELEMS // (T * Hq * D)), t16)
     k_scale = v_scale = None
-    if spec.kv_format == "bf16":
-        k = _normal_bf16((pool, P, Hkv, D), spec.seed, _STREAM_K, rows_per_chunk)
-        v = _normal_bf16((pool, P, Hkv, D), spec.seed, _STREAM_V, rows_per_chunk)
+    if spec.kv_format in ("bf16", "f16"):
+        k = _normal_bf16((pool, P, Hkv, D), spec.seed, _STREAM_K, rows_per_chunk, t16)
+        v = _normal_bf16((pool, P, Hkv, D), spec.seed, _STREAM_V, rows_per_chunk, t16)
     elif spec.kv_format == "fp8":
         k, k_scale = _normal_fp8((pool, P, Hkv, D), spec.seed, _STREAM_K, rows_per_chunk)
         v, v_scale = _normal_fp8((pool, P, Hkv, D), spec.seed, _STREAM_V, rows_per_chunk)
@@ -284,8 +285,8 @@ def make_inputs(spec: DecodeSpec, poison: bool = False) -> DecodeInputs:
 
     k_scr = v_scr = None
     if spec.draft_scratch:
-        k_scr = _normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_KS, B)
-        v_scr = _normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_VS, B)
+        k_scr = _normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_KS, B, t16)
+        v_scr = _normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_VS, B, t16)
 
     if poison:
         _poison(k, v, k_scale, v_scale, bt, lens, npages, pool, P)
@@ -304,7 +305,7 @@ def _poison(k, v, k_scale, v_scale, bt, lens, npages, pool, P):
     unused = torch.from_numpy(np.nonzero(~in_use)[0])
 
     def nan_fill(t, idx, slot0=None):
-        if t.dtype == torch.bfloat16:
+        if t.dtype in (torch.bfloat16, torch.float16):
             val = float("nan")
         elif t.dtype == torch.uint8:
             val = 0x7F  # e4m3fn NaN

@@ -78,6 +78,8 @@ CASES = [
     dict(kv_format="fp8", head_dim=64),                        # fp8 codes + scales
     dict(draft_scratch=True, q_tokens=4, context_lens=(20, 0, 33)),  # draft block, empty prefix
     dict(pool_pages=20, context_lens=(0, 17, 64)),             # empty context, spare pages
+    dict(kv_format="f16", q_tokens=2),                         # f16 q, caches and out
+    dict(kv_format="f16", draft_scratch=True, q_tokens=3),     # f16 draft block
 ]
 
 
@@ -111,6 +113,13 @@ def test_bf16_widening_matches_torch():
     x[:4] = torch.tensor([0.0, -0.0, float("inf"), 1e-40])
     bits = x.view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(oracle.bf16_bits_to_f64(bits), x.to(torch.float64).numpy())
+
+
+def test_f16_widening_matches_torch():
+    x = torch.randn(4096, dtype=torch.float32).to(torch.float16)
+    x[:5] = torch.tensor([0.0, -0.0, float("inf"), 6e-8, 65504.0])
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.f16_bits_to_f64(bits), x.to(torch.float64).numpy())
 
 
 def test_e4m3fn_table_matches_torch():
