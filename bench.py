@@ -58,6 +58,9 @@ WORKLOADS = {
     "long": "long-context split-K decode: B4 T1 Hq64 Hkv8 D128 P64 ctx 131072 bf16",
     "fp8": "native fp8 KV decode: B64 T1 Hq32 Hkv2 D256 P16 ctx U[1024,16384] e4m3fn KV + fp32 per-token scale",
     "tidar": "TiDAR draft-block decode: B16 T8 Hq32 Hkv8 D128 P16 ctx U[2048,8192] + scratch KV [16,8,8,128] bf16",
+    "gqa_f16": "GQA decode in f16: B32 T1 Hq32 Hkv8 D128 P16 ctx U[512,8192] f16 q/K/V/out",
+    "gqa_d64": "GQA decode, head dim 64: B32 T1 Hq32 Hkv8 D64 P16 ctx U[512,8192] bf16",
+    "gqa_d256": "GQA decode, head dim 256: B32 T1 Hq32 Hkv8 D256 P16 ctx U[512,8192] bf16",
     "tidar_causal": "TiDAR draft-block decode with a causal draft: B16 T8 Hq32 Hkv8 D128 P16 ctx U[2048,8192] "
                     "+ scratch KV [16,8,8,128] bf16, draft token t sees scratch tokens <= t",
     "tidar_long": "TiDAR 16-token draft in blocks of 4: B16 T16 Hq32 Hkv8 D128 P16 ctx U[2048,8192] "
@@ -413,7 +416,7 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8" if spec.kv_format == "fp8" else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": spec.kv_format, "data": "synthetic",
         "config": {
             "workload": WORKLOADS[args.config] + (f" (batch cut to {spec.batch})" if args.batch else ""),
             "batch": spec.batch, "q_tokens": spec.q_tokens,

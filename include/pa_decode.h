@@ -136,6 +136,15 @@ pa_status pa_decode_fp8(const void* q, const uint8_t* k_cache, const uint8_t* v_
                         int32_t num_splits, void* workspace, size_t workspace_bytes,
                         pa_stream_t stream);
 
+/* Dense f16 paged decode: as pa_decode with q, k_cache, v_cache and out in
+ * IEEE binary16 (the MSLK page's dense path takes f16 or bf16); the products
+ * run in f16 with fp32 accumulation. */
+pa_status pa_decode_f16(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        const pa_shape* shape, float scale, void* out, float* lse,
+                        int32_t num_splits, void* workspace, size_t workspace_bytes,
+                        pa_stream_t stream);
+
 /* Draft-block (TiDAR) decode: as pa_decode, plus the T scratch tokens of each
  * sequence (k_scratch, v_scratch [B, T, Hkv, D] bf16, contiguous) as extra
  * keys after the paged prefix. Every draft token attends to the whole prefix

@@ -50,6 +50,7 @@ _SIGNATURES = {
     "pa_decode_choose_splits": (ctypes.c_int32, [ctypes.POINTER(PaShape), ctypes.c_int32]),
     "pa_decode": (ctypes.c_int, [_P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
+    "pa_decode_f16": (ctypes.c_int, [_P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_tidar": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P] + _DECODE_TAIL),
     "pa_decode_tidar_masked": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float,
                                               ctypes.c_int32, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
@@ -143,7 +144,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     pa_decode_tidar_masked.
 
     The fp8 entry point is used when k_cache is uint8 (e4m3fn codes, with
-    k_scale/v_scale); the draft-block entry point when k_scratch is given,
+    k_scale/v_scale); pa_decode_f16 when q is float16 (f16 caches and out);
+    the draft-block entry point when k_scratch is given,
     its block-masked form when draft_block is given too. out, lse and the
     workspace are allocated here when not passed in."""
     _need_contig(q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables, context_lens=context_lens,
@@ -174,6 +176,9 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
         st = L.pa_decode_tidar(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scratch), _ptr(v_scratch),
                                _ptr(block_tables), _ptr(context_lens), *tail)
         _check(st, "pa_decode_tidar")
+    elif q.dtype == torch.float16:
+        st = L.pa_decode_f16(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), *tail)
+        _check(st, "pa_decode_f16")
     else:
         st = L.pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), *tail)
         _check(st, "pa_decode")

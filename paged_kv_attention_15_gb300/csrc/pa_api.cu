@@ -42,7 +42,7 @@ std::mutex g_mu;
 thread_local cudaEvent_t t_ev_start = nullptr;
 thread_local cudaEvent_t t_ev_split = nullptr;
 
-enum class Kind { kBf16, kFp8, kTidar };
+enum class Kind { kBf16, kFp8, kTidar, kF16 };
 
 pa_status device_state(DeviceState** out) {
   int dev = 0;
@@ -145,7 +145,9 @@ pa_status check_shape(const pa_shape* s, Kind kind) {
 }
 
 SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL) {
-  return kind == Kind::kFp8 ? pa::split_kernel_fp8(D, MT, TSL) : pa::split_kernel_bf16(D, MT, TSL);
+  if (kind == Kind::kFp8) return pa::split_kernel_fp8(D, MT, TSL);
+  if (kind == Kind::kF16) return pa::split_kernel_f16(D, MT, TSL);
+  return pa::split_kernel_bf16(D, MT, TSL);
 }
 
 // Work-unit geometry: H2 kv heads per CTA unit, their M = H2 * G * T query
@@ -172,11 +174,20 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   const int NGW = pa::kConsumerWarps / MT;
   const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
   if (NGW % HT) return false;
-  const int NSL = NGW / HT, TS = pa::kStageRows / H2;
-  if (TS % NSL) return false;
-  const int TSL = TS / NSL;
-  if (TSL != 16 && TSL != 32 && TSL != 64) return false;
-  const SplitKernel k = pick_kernel(kind, D, MT, TSL);
+  const int NSL = NGW / HT;
+  // Stage rows: the instance's capacity when a warp's token slice allows
+  // it, else 64.
+  const bool fp8 = kind == Kind::kFp8;
+  const int cap_rows = pa::stage_rows(D * (fp8 ? 1 : 2), fp8);
+  SplitKernel k{nullptr, 0, 0};
+  int TS = 0, TSL = 0;
+  for (int rows = cap_rows; rows >= 64 && !k.fn; rows /= 2) {
+    TS = rows / H2;
+    if (TS % NSL) continue;
+    TSL = TS / NSL;
+    if (TSL != 16 && TSL != 32 && TSL != 64) continue;
+    k = pick_kernel(kind, D, MT, TSL);
+  }
   if (!k.fn) return false;
   g->GT = GT;
   g->H2 = H2;
@@ -233,7 +244,10 @@ pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d
     const size_t smem = (size_t)k.smem_fixed + (size_t)(2 * B + 1) * 4;
     if (smem <= (size_t)d->smem_optin) {
       p.balanced = true;
-      p.grid = d->sms;
+      // One CTA per SM, but no more CTAs than the flattened pages can fill
+      // (more would only add empty shares for the reduce to skip).
+      const long long most = (long long)units * (s->max_blocks_per_seq + (kind == Kind::kTidar ? 1 : 0));
+      p.grid = most < d->sms ? (int)(most < 1 ? 1 : most) : d->sms;
       p.smem = smem;
       const size_t slots = (size_t)units + p.grid;
       p.part_lse_off = align256(slots * M * D * sizeof(float));
@@ -327,7 +341,9 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
     const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2, (uint64_t)T * Hq * D * 2};
     const uint32_t box[4] = {64u, (uint32_t)G, (uint32_t)T, 1u};
-    if (!make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, dims, str, box)) return PA_ERR_INVALID_ARG;
+    const CUtensorMapDataType qt =
+        a.kind == Kind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map(&p.tm_q, qt, a.q, dims, str, box)) return PA_ERR_INVALID_ARG;
   }
   // KV caches as 5-D (128-byte column chunk, slot, kv head, chunk index,
   // page): one box copies every chunk of BR rows of one page for the H2
@@ -338,7 +354,9 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     const uint64_t dims[5] = {128 / e, (uint64_t)P, (uint64_t)Hkv, nch, (uint64_t)s.num_pages};
     const uint64_t str[4] = {(uint64_t)Hkv * D * e, (uint64_t)D * e, 128, (uint64_t)P * Hkv * D * e};
     const uint32_t box[5] = {(uint32_t)(128 / e), (uint32_t)geo.BR, (uint32_t)geo.H2, (uint32_t)nch, 1u};
-    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : (a.kind == Kind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
     if (!make_map(&p.tm_k, dt, a.k_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
     if (!make_map(&p.tm_v, dt, a.v_cache, dims, str, box)) return PA_ERR_INVALID_ARG;
   }
@@ -414,6 +432,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     r.max_blocks = s.max_blocks_per_seq;
     r.tidar = p.tidar;
     r.num_splits = plan.balanced ? 0 : plan.splits;
+    r.out_f16 = a.kind == Kind::kF16 ? 1 : 0;
     r.grid = plan.grid;
     // Programmatic dependent launch: the reduce grid may start while the
     // split grid drains and waits (griddepcontrol.wait) for its results.
@@ -453,10 +472,10 @@ size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits) {
   }
   DeviceState* d = nullptr;
   if (device_state(&d) != PA_OK) return 0;
-  // The balanced plan does not depend on the KV format beyond the instance's
-  // fixed shared memory; take the larger of the two plans.
+  // The balanced plan depends on the kind through the instance's fixed
+  // shared memory and the draft block's extra page; take the largest plan.
   size_t best = 0;
-  for (Kind kind : {Kind::kBf16, Kind::kFp8}) {
+  for (Kind kind : {Kind::kBf16, Kind::kFp8, Kind::kTidar}) {
     if (check_shape(shape, kind) != PA_OK) continue;
     Plan plan;
     if (make_plan(shape, kind, 0, d, &plan) == PA_OK && plan.ws_bytes > best) best = plan.ws_bytes;
@@ -498,6 +517,14 @@ pa_status pa_decode_tidar(const void* q, const void* k_cache, const void* v_cach
   CallArgs a{Kind::kTidar, q, k_cache, v_cache, nullptr, nullptr, k_scratch, v_scratch, block_tables,
              context_lens, shape, scale, out, lse, num_splits, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream)};
+  return run_decode(a);
+}
+
+pa_status pa_decode_f16(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        const int32_t* context_lens, const pa_shape* shape, float scale, void* out, float* lse,
+                        int32_t num_splits, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  CallArgs a{Kind::kF16, q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, block_tables, context_lens,
+             shape, scale, out, lse, num_splits, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)};
   return run_decode(a);
 }
 

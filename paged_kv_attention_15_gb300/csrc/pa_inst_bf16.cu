@@ -1,17 +1,27 @@
-// bf16 KV instances of the split kernel.
+// 16-bit KV instances of the split kernel: bf16, or f16 when this file is
+// included by pa_inst_f16.cu with PA_INST_KV / PA_INST_FN set.
 #include "pa_launch.h"
 
 namespace pa {
 
+#ifndef PA_INST_KV
+#define PA_INST_KV kKvBf16
+#define PA_INST_FN split_kernel_bf16
+#endif
+constexpr int KVK = PA_INST_KV;
+
 template <int D, int MT, int TSL>
 static SplitKernel entry() {
   using C = Cfg<D, MT, false, TSL>;
-  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, false, TSL>), C::SMEM_FIXED, C::NS};
+  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, KVK, TSL>), C::SMEM_FIXED, C::NS};
 }
 
 template <int D>
 static SplitKernel by_tiles(int row_tiles, int slice) {
   if (row_tiles == 1 && slice == 16) return entry<D, 1, 16>();
+  if constexpr (D == 64) {  // 128-row stages: 32 tokens per warp with one row tile
+    if (row_tiles == 1 && slice == 32) return entry<D, 1, 32>();
+  }
   if (row_tiles == 2 && slice == 16) return entry<D, 2, 16>();
   if (row_tiles == 2 && slice == 32) return entry<D, 2, 32>();
   if constexpr (D == 128 || D == 64) {
@@ -24,7 +34,7 @@ static SplitKernel by_tiles(int row_tiles, int slice) {
   return SplitKernel{nullptr, 0, 0};
 }
 
-SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice) {
+SplitKernel PA_INST_FN(int head_dim, int row_tiles, int slice) {
   if (head_dim == 64) return by_tiles<64>(row_tiles, slice);
   if (head_dim == 128) return by_tiles<128>(row_tiles, slice);
   if (head_dim == 256) return by_tiles<256>(row_tiles, slice);

@@ -6,7 +6,7 @@ namespace pa {
 template <int D, int MT, int TSL>
 static SplitKernel entry() {
   using C = Cfg<D, MT, true, TSL>;
-  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, true, TSL>), C::SMEM_FIXED, C::NS};
+  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, kKvFp8, TSL>), C::SMEM_FIXED, C::NS};
 }
 
 template <int D>

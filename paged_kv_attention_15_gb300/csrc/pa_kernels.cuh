@@ -44,7 +44,11 @@ namespace pa {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStageRows = 64;  // key rows per pipeline stage (tokens x heads)
+// Capacity in key rows (tokens x heads) of a pipeline stage: 64, or 128
+// for the 128-byte rows of 16-bit D = 64, so that a stage's K tile can be
+// 16 KB and the per-stage waits and arrivals spread over as many bytes.
+// The host picks the rows a launch actually uses per stage (p.TS * H2).
+constexpr int stage_rows(int row_bytes, bool fp8) { return !fp8 && row_bytes <= 128 ? 128 : 64; }
 constexpr int kMaxHkvFp8 = 8;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -93,6 +97,7 @@ struct ReduceParams {
   int H2, NHG, GT;
   int num_splits;  // >= 1: explicit layout [B][T][Hq][S]; 0: balanced-launch slots
   int grid;        // CTAs of the balanced split launch
+  int out_f16;     // 1: out holds f16 (else bf16)
 };
 
 // Shared-memory plan of one kernel instance (TSL: tokens per warp slice).
@@ -101,8 +106,9 @@ struct Cfg {
   static constexpr int ELEM = FP8 ? 1 : 2;
   static constexpr int CE = 128 / ELEM;         // elements per 128-byte row chunk
   static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
-  static constexpr int TILE = kStageRows * D * ELEM;  // bytes of the K (or V) tile of a stage
-  static constexpr int SCALE = FP8 ? kStageRows * kMaxHkvFp8 * 4 : 0;
+  static constexpr int SROWS = stage_rows(D * ELEM, FP8);
+  static constexpr int TILE = SROWS * D * ELEM;  // bytes of the K (or V) tile of a stage
+  static constexpr int SCALE = FP8 ? SROWS * kMaxHkvFp8 * 4 : 0;
   static constexpr int STAGE = round_up(2 * TILE + 2 * SCALE, 1024);
   static constexpr int ROWS = 16 * MT;
   static constexpr int QCH = D / 64;
@@ -247,7 +253,8 @@ __device__ __forceinline__ void raise_abort(volatile int* s_abort, int* err_flag
 // benchmark" (Kernels: pa_decode_reduce, the split-K combine).
 template <typename ORow, typename LVal>
 __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_val, __nv_bfloat16* out,
-                                            float* lse_out, int lane) {
+                                            float* lse_out, int lane, bool out_f16) {
+  auto pack = [&](float lo, float hi) { return out_f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float LOG2E = 1.4426950408889634f;
   const int c0 = lane * 4, c1 = 128 + lane * 4;
@@ -284,16 +291,22 @@ __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_va
   const float inv = L > 0.f ? 1.f / L : 0.f;
   if (h0)
     *reinterpret_cast<uint2*>(out + c0) =
-        make_uint2(pack_bf16x2(a0.x * inv, a0.y * inv), pack_bf16x2(a0.z * inv, a0.w * inv));
+        make_uint2(pack(a0.x * inv, a0.y * inv), pack(a0.z * inv, a0.w * inv));
   if (h1)
     *reinterpret_cast<uint2*>(out + c1) =
-        make_uint2(pack_bf16x2(a1.x * inv, a1.y * inv), pack_bf16x2(a1.z * inv, a1.w * inv));
+        make_uint2(pack(a1.x * inv, a1.y * inv), pack(a1.z * inv, a1.w * inv));
   if (lane == 0 && lse_out) *lse_out = L > 0.f ? m + lg2(L) * kLn2 : NEG_INF;
 }
 
 // ------------------------------------------------------------ split kernel
-template <int D, int MT, bool FP8, int TSL>
+// KV element kinds of the split kernel: bf16 (q, caches, out bf16), fp8
+// (e4m3fn caches with scales; q and out bf16), f16 (q, caches, out f16).
+constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvF16 = 2;
+
+template <int D, int MT, int KV, int TSL>
 __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_constant__ SplitParams p) {
+  constexpr bool FP8 = KV == kKvFp8;
+  constexpr bool F16 = KV == kKvF16;  // 16-bit path in f16 instead of bf16
   using C = Cfg<D, MT, FP8, TSL>;
   constexpr int NS = C::NS;
   constexpr int NGW = C::NGW;
@@ -625,8 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
               for (int nb = 0; nb < NTS / 2; ++nb) {
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(krow[nb] + coff, b0, b1, b2, b3);
-                mma_bf16((kk & 1) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
-                mma_bf16((kk & 1) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
+                mma16<F16>((kk & 1) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
+                mma16<F16>((kk & 1) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
               }
             }
           } else {
@@ -731,10 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
             const uint32_t vrow = vb_ + row_base(tb + kb * 16 + ((lane >> 3) & 1) * 8 + sw);
             uint32_t pa[4];
             if (!FP8) {
-              pa[0] = pack_bf16x2(s[2 * kb][0], s[2 * kb][1]);
-              pa[1] = pack_bf16x2(s[2 * kb][2], s[2 * kb][3]);
-              pa[2] = pack_bf16x2(s[2 * kb + 1][0], s[2 * kb + 1][1]);
-              pa[3] = pack_bf16x2(s[2 * kb + 1][2], s[2 * kb + 1][3]);
+              pa[0] = pack16<F16>(s[2 * kb][0], s[2 * kb][1]);
+              pa[1] = pack16<F16>(s[2 * kb][2], s[2 * kb][3]);
+              pa[2] = pack16<F16>(s[2 * kb + 1][0], s[2 * kb + 1][1]);
+              pa[3] = pack16<F16>(s[2 * kb + 1][2], s[2 * kb + 1][3]);
 #pragma unroll
               for (int nd = 0; nd < D / 16; ++nd) {
                 const int unit = ((nd * 16) % 64) / 8 + (lane >> 4);
@@ -743,8 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
                 if (partial) {
                   b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
                 }
-                mma_bf16(acc[2 * nd], pa, b0, b1);
-                mma_bf16(acc[2 * nd + 1], pa, b2, b3);
+                mma16<F16>(acc[2 * nd], pa, b0, b1);
+                mma16<F16>(acc[2 * nd + 1], pa, b2, b3);
               }
             } else {
               // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
@@ -873,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
         if (!FP8) {
 #pragma unroll
           for (int i = 0; i < NT8; ++i)
-            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * c4) = pack_bf16x2(acc[i][2 * h2], acc[i][2 * h2 + 1]);
+            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * c4) = pack16<F16>(acc[i][2 * h2], acc[i][2 * h2 + 1]);
         } else {
 #pragma unroll
           for (int u = 0; u < D / 16; ++u)

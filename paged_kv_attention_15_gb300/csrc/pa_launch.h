@@ -17,5 +17,6 @@ struct SplitKernel {
 // fn == nullptr if that combination is not built.
 SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice);
 SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice);
+SplitKernel split_kernel_f16(int head_dim, int row_tiles, int slice);
 
 }  // namespace pa

@@ -166,6 +166,16 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The 16-bit MMA of an element type: f16 (F16) or bf16.
+template <bool F16>
+__device__ __forceinline__ void mma16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    mma_f16(d, a, b0, b1);
+  } else {
+    mma_bf16(d, a, b0, b1);
+  }
+}
+
 // ------------------------------------------------------------ SFU / packing
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -187,6 +197,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two floats -> two 16-bit values of the element type (round to nearest even).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  if constexpr (F16) {
+    return pack_f16x2(lo, hi);
+  } else {
+    return pack_bf16x2(lo, hi);
+  }
 }
 
 // Two e4m3fn codes (low byte = first) -> f16x2, exact.

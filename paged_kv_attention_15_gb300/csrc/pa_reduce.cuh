@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_cons
   const int D = p.D;
   combine_row(
       p.num_splits, D, [&](int k) { return po + (size_t)k * D; }, [&](int k) { return __ldcg(pl + k); },
-      p.out + row * D, p.lse ? p.lse + row : nullptr, lane);
+      p.out + row * D, p.lse ? p.lse + row : nullptr, lane, p.out_f16 != 0);
 }
 
 // Balanced launch: grid (units, ceil(M / 4)); warp w of CTA (u, y) combines
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_co
         const long long i = i0 + k;  // a CTA whose share is empty wrote nothing
         return (N * i / G64) < (N * (i + 1) / G64) ? __ldcg(pl + (size_t)(u + i) * M + rho) : NEG_INF;
       },
-      p.out + row * D, p.lse ? p.lse + row : nullptr, lane);
+      p.out + row * D, p.lse ? p.lse + row : nullptr, lane, p.out_f16 != 0);
 }
 
 }  // namespace pa

@@ -96,6 +96,16 @@ SPECS = {
     "tidar": DecodeSpec("tidar", batch=16, q_tokens=8, num_q_heads=32, num_kv_heads=8,
                         head_dim=128, page_size=16, ctx_range=(2048, 8192),
                         draft_scratch=True, max_blocks_per_seq=8192 // 16, seed=4),
+    # The GQA geometry in f16, and in bf16 with head dims 64 and 256.
+    "gqa_f16": DecodeSpec("gqa_f16", batch=32, q_tokens=1, num_q_heads=32, num_kv_heads=8,
+                          head_dim=128, page_size=16, ctx_range=(512, 8192), kv_format="f16",
+                          max_blocks_per_seq=8192 // 16, seed=9),
+    "gqa_d64": DecodeSpec("gqa_d64", batch=32, q_tokens=1, num_q_heads=32, num_kv_heads=8,
+                          head_dim=64, page_size=16, ctx_range=(512, 8192),
+                          max_blocks_per_seq=8192 // 16, seed=10),
+    "gqa_d256": DecodeSpec("gqa_d256", batch=32, q_tokens=1, num_q_heads=32, num_kv_heads=8,
+                           head_dim=256, page_size=16, ctx_range=(512, 8192),
+                           max_blocks_per_seq=8192 // 16, seed=11),
     # Draft-block variants: the TiDAR workload with a causal draft, and a
     # 16-token draft (64 query rows per kv head) in blocks of 4.
     "tidar_causal": DecodeSpec("tidar_causal", batch=16, q_tokens=8, num_q_heads=32, num_kv_heads=8,

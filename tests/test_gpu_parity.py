@@ -123,6 +123,21 @@ def test_fp8_sweep(case, num_splits):
     check_full(gen.make_inputs(spec(**case)), num_splits)
 
 
+F16_SWEEP = [
+    dict(kv_format="f16"),
+    dict(kv_format="f16", head_dim=64, num_q_heads=32, num_kv_heads=1),
+    dict(kv_format="f16", head_dim=256, q_tokens=2, num_q_heads=16, num_kv_heads=4, page_size=64,
+         context_lens=(64, 1, 700, 65)),
+    dict(kv_format="f16", q_tokens=16, num_q_heads=8, num_kv_heads=2, context_lens=(0, 40, 129, 16)),
+]
+
+
+@pytest.mark.parametrize("case", F16_SWEEP, ids=[str(i) for i in range(len(F16_SWEEP))])
+@pytest.mark.parametrize("num_splits", [0, 1, 4])
+def test_f16_sweep(case, num_splits):
+    check_full(gen.make_inputs(spec(**case)), num_splits)
+
+
 TIDAR_SWEEP = [
     dict(draft_scratch=True, q_tokens=8, num_q_heads=8, num_kv_heads=2),
     dict(draft_scratch=True, q_tokens=4, num_q_heads=4, num_kv_heads=1, context_lens=(0, 16, 17, 250)),
@@ -316,7 +331,8 @@ def sample_rows(inp, n, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["gqa", "long", "fp8", "tidar", "tidar_causal", "tidar_long"])
+@pytest.mark.parametrize("name", ["gqa", "long", "fp8", "tidar", "tidar_causal", "tidar_long", "gqa_f16", "gqa_d64",
+                                  "gqa_d256"])
 def test_full_size_workload_sampled(name):
     inp = gen.make_inputs(gen.SPECS[name])
     out, lse = gpu_decode(inp, 0)
