@@ -73,6 +73,7 @@ WORKLOADS = {
 APPEND_CONFIGS = ("append", "append_fp8", "append_step")
 APPEND_METRIC = "KV-cache append µs/call and achieved HBM GB/s (fraction of 8 TB/s) on 1 GB300"
 SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh"]
+APPEND_KERNEL_SOURCES = ["pa_append.cu", "pa_ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -133,21 +134,22 @@ def load_peak():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-def kernel_sha() -> str:
+def kernel_sha(config: str = DEFAULT_CONFIG) -> str:
+    """Hash of the sources of the kernel a workload's roofline is about."""
     h = hashlib.sha256()
-    for name in SPLIT_KERNEL_SOURCES:
+    for name in (APPEND_KERNEL_SOURCES if config in APPEND_CONFIGS else SPLIT_KERNEL_SOURCES):
         with open(os.path.join(ROOT, "paged_kv_attention_15_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def load_traffic(config: str):
-    """DRAM bytes per split-kernel launch from the committed ncu summary,
-    if it was taken on the current kernel source; else None."""
+    """DRAM bytes per launch of the workload's kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f).get(config)
-        if rec and rec.get("kernel_sha") == kernel_sha():
+        if rec and rec.get("kernel_sha") == kernel_sha(config):
             return int(rec["dram_bytes_per_launch"])
     except Exception:
         pass
