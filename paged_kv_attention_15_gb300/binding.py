@@ -159,6 +159,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if k_scratch is not None and q.dtype != torch.bfloat16:
+        raise ValueError("the draft-block entry points take bf16 q, caches and scratch")
     L = lib()
     tail = (ctypes.byref(shape), float(scale), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), ws_bytes,
             _stream(stream))

@@ -184,6 +184,32 @@ LONG_ROWS = [
 ]
 
 
+# Shapes whose units could hold 128 query rows (4 kv heads x 32 rows, 2 x 64):
+# the units stay at 64 rows (four tiles, one per warp)
+EIGHT_TILES = [
+    (dict(draft_scratch=True, q_tokens=8, num_q_heads=16, num_kv_heads=4), None),
+    (dict(draft_scratch=True, q_tokens=8, num_q_heads=16, num_kv_heads=4, context_lens=(0, 31, 260, 16)), 3),
+    (dict(draft_scratch=True, q_tokens=16, num_q_heads=8, num_kv_heads=4), 4),
+    (dict(q_tokens=4, num_q_heads=32, num_kv_heads=4), None),
+    (dict(draft_scratch=True, q_tokens=8, num_q_heads=32, num_kv_heads=8), 1),
+    (dict(kv_format="f16", q_tokens=4, num_q_heads=32, num_kv_heads=4), None),
+]
+
+
+@pytest.mark.parametrize("case,bs", EIGHT_TILES, ids=[str(i) for i in range(len(EIGHT_TILES))])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_units_of_up_to_four_row_tiles(case, bs, num_splits):
+    inp = gen.make_inputs(spec(**case))
+    oi = ora_inputs(inp)
+    kw = {}
+    if bs is not None:
+        oi["draft_block"] = bs
+        kw["draft_block"] = bs
+    ref_out, ref_lse = oracle.decode(oi, inp.scale)
+    out, lse = to_np(*gpu_decode(inp, num_splits, **kw))
+    assert_match(out, lse, ref_out, ref_lse, tol_of(inp.spec))
+
+
 @pytest.mark.parametrize("case", LONG_ROWS, ids=[str(i) for i in range(len(LONG_ROWS))])
 @pytest.mark.parametrize("num_splits", [0, 1, 5])
 def test_more_than_32_rows_per_kv_head(case, num_splits):
