@@ -454,15 +454,21 @@ def append_oracle_run(host, budget_s: float, start_seq: int = 0):
     from oracle import kv_append as ka
 
     bits = host.numpy_bits()
-    caches = {n: bits[n] for n in ("k_cache", "v_cache", "k_scale", "v_scale") if n in bits}
+    names = [n for n in ("k_cache", "v_cache", "k_scale", "v_scale") if n in bits]
     spec = host.spec
     done_s, done_b, n = 0.0, 0, 0
     per_seq = append_bytes(host) / spec.batch
     while done_s < budget_s and n < spec.batch:
         b = (start_seq + n) % spec.batch
+        # The oracle returns copies of the caches it is given: give it the
+        # sequence's own pages (block table renumbered), not the whole pool.
+        row = bits["block_tables"][b:b + 1]
+        pages = row[row >= 0]
+        caches = {nm: bits[nm][pages] for nm in names}
+        local = np.where(row >= 0, np.cumsum(row >= 0, axis=1) - 1, -1).astype(np.int32)
         t = time.perf_counter()
-        ka.append(caches, bits["k_new"][b:b + 1], bits["v_new"][b:b + 1], bits["block_tables"][b:b + 1],
-                  bits["context_lens"][b:b + 1], spec.page_size)
+        ka.append(caches, bits["k_new"][b:b + 1], bits["v_new"][b:b + 1], local, bits["context_lens"][b:b + 1],
+                  spec.page_size)
         done_s += time.perf_counter() - t
         done_b += per_seq
         n += 1

@@ -51,3 +51,42 @@ def test_reference_arm_prints_the_contract_line():
     assert line["metric"] == bench.METRIC and line["steps"] == 2 and line["warmup"] == 3
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_append_sample_on_own_pages_matches_whole_pool():
+    """The CPU-baseline sampler gives the append oracle one sequence's pages
+    with a renumbered block table: the rows it writes equal those of the
+    oracle's append over the whole pool."""
+    import numpy as np
+
+    from oracle import kv_append as ka
+
+    spec = gen.AppendSpec("t", batch=3, new_tokens=20, num_kv_heads=2, head_dim=64, page_size=16,
+                          context_lens=(5, 30, 0), kv_format="fp8", seed=3)
+    host = gen.make_append_inputs(spec)
+    bits = host.numpy_bits()
+    names = ("k_cache", "v_cache", "k_scale", "v_scale")
+    full = ka.append({n: bits[n] for n in names}, bits["k_new"], bits["v_new"], bits["block_tables"],
+                     bits["context_lens"], 16)
+    for b in range(3):
+        row = bits["block_tables"][b:b + 1]
+        pages = row[row >= 0]
+        local = np.where(row >= 0, np.cumsum(row >= 0, axis=1) - 1, -1).astype(np.int32)
+        own = ka.append({n: bits[n][pages] for n in names}, bits["k_new"][b:b + 1], bits["v_new"][b:b + 1], local,
+                        bits["context_lens"][b:b + 1], 16)
+        for n in names:
+            np.testing.assert_array_equal(own[n], full[n][pages])
+    secs, nbytes, desc = bench.append_oracle_run(host, 0.5)
+    assert secs > 0 and nbytes > 0 and "sequence" in desc
+
+
+def test_append_bytes_by_hand():
+    spec = gen.AppendSpec("t", batch=2, new_tokens=20, num_kv_heads=2, head_dim=64, page_size=16,
+                          context_lens=(5, 30), seed=3)
+    host = gen.make_append_inputs(spec)
+    rows = 2 * 20 * 2 * 2                       # (token, kv head) rows of K and V
+    pages = ((5 + 19) // 16 - 5 // 16 + 1) + ((30 + 19) // 16 - 30 // 16 + 1)  # 2 + 3 table entries
+    assert bench.append_bytes(host) == rows * (2 * 64 + 2 * 64) + pages * 4 + 2 * 4
+    fp8 = gen.make_append_inputs(gen.AppendSpec("t", batch=2, new_tokens=20, num_kv_heads=2, head_dim=128,
+                                                page_size=16, context_lens=(5, 30), kv_format="fp8", seed=3))
+    assert bench.append_bytes(fp8) == rows * (2 * 128 + 128 + 4) + pages * 4 + 2 * 4
