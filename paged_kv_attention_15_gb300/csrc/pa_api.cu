@@ -144,10 +144,10 @@ pa_status check_shape(const pa_shape* s, Kind kind) {
   return PA_OK;
 }
 
-SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL) {
-  if (kind == Kind::kFp8) return pa::split_kernel_fp8(D, MT, TSL);
-  if (kind == Kind::kF16) return pa::split_kernel_f16(D, MT, TSL);
-  return pa::split_kernel_bf16(D, MT, TSL);
+SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL, int CW) {
+  if (kind == Kind::kFp8) return pa::split_kernel_fp8(D, MT, TSL, CW);
+  if (kind == Kind::kF16) return pa::split_kernel_f16(D, MT, TSL, CW);
+  return pa::split_kernel_bf16(D, MT, TSL, CW);
 }
 
 // Work-unit geometry: H2 kv heads per CTA unit, their M = H2 * G * T query
@@ -171,22 +171,26 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   // share one evenly.
   if (H2 > 1 && (GT < 16 ? 16 % GT : GT % 16)) return false;
   const int MT = M <= 16 ? 1 : (M <= 32 ? 2 : 4);  // rows past M are masked
-  const int NGW = pa::kConsumerWarps / MT;
-  const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
-  if (NGW % HT) return false;
-  const int NSL = NGW / HT;
-  // Stage rows: the instance's capacity when a warp's token slice allows
-  // it, else 64.
+  // Eight consumer warps (two per row tile, splitting its tokens) where
+  // such an instance is built, else four.
   const bool fp8 = kind == Kind::kFp8;
   const int cap_rows = pa::stage_rows(D * (fp8 ? 1 : 2), fp8);
-  SplitKernel k{nullptr, 0, 0};
+  const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
+  SplitKernel k{nullptr, 0, 0, 0};
   int TS = 0, TSL = 0;
-  for (int rows = cap_rows; rows >= 64 && !k.fn; rows /= 2) {
-    TS = rows / H2;
-    if (TS % NSL) continue;
-    TSL = TS / NSL;
-    if (TSL != 16 && TSL != 32 && TSL != 64) continue;
-    k = pick_kernel(kind, D, MT, TSL);
+  for (int CW = 8; CW >= pa::kConsumerWarps && !k.fn; CW /= 2) {
+    const int NGW = CW / MT;
+    if (NGW < 1 || NGW % HT) continue;
+    const int NSL = NGW / HT;
+    // Stage rows: the instance's capacity when a warp's token slice allows
+    // it, else 64.
+    for (int rows = cap_rows; rows >= 64 && !k.fn; rows /= 2) {
+      TS = rows / H2;
+      if (TS % NSL) continue;
+      TSL = TS / NSL;
+      if (TSL != 16 && TSL != 32 && TSL != 64) continue;
+      k = pick_kernel(kind, D, MT, TSL, CW);
+    }
   }
   if (!k.fn) return false;
   g->GT = GT;
@@ -407,7 +411,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   const dim3 grid = plan.balanced ? dim3(plan.grid) : dim3(B * geo.NHG, plan.splits);
   void* args[] = {&p};
   if (ev_start && cudaEventRecord(ev_start, a.stream) != cudaSuccess) return PA_ERR_CUDA;
-  if (cudaLaunchKernel(k.fn, grid, dim3(pa::kThreads), args, plan.smem, a.stream) != cudaSuccess)
+  if (cudaLaunchKernel(k.fn, grid, dim3(k.threads), args, plan.smem, a.stream) != cudaSuccess)
     return PA_ERR_CUDA;
   if (ev_split && cudaEventRecord(ev_split, a.stream) != cudaSuccess) return PA_ERR_CUDA;
 

@@ -10,14 +10,21 @@ namespace pa {
 #endif
 constexpr int KVK = PA_INST_KV;
 
-template <int D, int MT, int TSL>
+template <int D, int MT, int TSL, int CW = kConsumerWarps>
 static SplitKernel entry() {
-  using C = Cfg<D, MT, false, TSL>;
-  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, KVK, TSL>), C::SMEM_FIXED, C::NS};
+  using C = Cfg<D, MT, false, TSL, CW>;
+  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, KVK, TSL, CW>), C::SMEM_FIXED, C::NS,
+                     C::THREADS};
 }
 
 template <int D>
-static SplitKernel by_tiles(int row_tiles, int slice) {
+static SplitKernel by_tiles(int row_tiles, int slice, int cw) {
+  if constexpr (D == 128) {
+    // eight consumer warps, two per row tile splitting its tokens: the
+    // four-tile draft-block units (64 rows of two kv heads)
+    if (cw == 8) return row_tiles == 4 && slice == 16 ? entry<D, 4, 16, 8>() : SplitKernel{nullptr, 0, 0, 0};
+  }
+  if (cw != kConsumerWarps) return SplitKernel{nullptr, 0, 0, 0};
   if (row_tiles == 1 && slice == 16) return entry<D, 1, 16>();
   if constexpr (D == 64) {  // 128-row stages: 32 tokens per warp with one row tile
     if (row_tiles == 1 && slice == 32) return entry<D, 1, 32>();
@@ -31,14 +38,14 @@ static SplitKernel by_tiles(int row_tiles, int slice) {
     if (row_tiles == 4 && slice == 32) return entry<D, 4, 32>();
     if (row_tiles == 4 && slice == 64) return entry<D, 4, 64>();
   }
-  return SplitKernel{nullptr, 0, 0};
+  return SplitKernel{nullptr, 0, 0, 0};
 }
 
-SplitKernel PA_INST_FN(int head_dim, int row_tiles, int slice) {
-  if (head_dim == 64) return by_tiles<64>(row_tiles, slice);
-  if (head_dim == 128) return by_tiles<128>(row_tiles, slice);
-  if (head_dim == 256) return by_tiles<256>(row_tiles, slice);
-  return SplitKernel{nullptr, 0, 0};
+SplitKernel PA_INST_FN(int head_dim, int row_tiles, int slice, int cw) {
+  if (head_dim == 64) return by_tiles<64>(row_tiles, slice, cw);
+  if (head_dim == 128) return by_tiles<128>(row_tiles, slice, cw);
+  if (head_dim == 256) return by_tiles<256>(row_tiles, slice, cw);
+  return SplitKernel{nullptr, 0, 0, 0};
 }
 
 }  // namespace pa

@@ -42,8 +42,7 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kConsumerWarps = 4;  // consumer warps of most instances (one per SM sub-partition)
 // Capacity in key rows (tokens x heads) of a pipeline stage: 64, or 128
 // for the 128-byte rows of 16-bit D = 64, so that a stage's K tile can be
 // 16 KB and the per-stage waits and arrivals spread over as many bytes.
@@ -100,9 +99,12 @@ struct ReduceParams {
   int out_f16;     // 1: out holds f16 (else bf16)
 };
 
-// Shared-memory plan of one kernel instance (TSL: tokens per warp slice).
-template <int D, int MT, bool FP8, int TSL>
+// Shared-memory plan of one kernel instance (TSL: tokens per warp slice;
+// CW: consumer warps, 4 or 8 -- with 8, two warps share each SM
+// sub-partition and split each row tile's tokens).
+template <int D, int MT, bool FP8, int TSL, int CW = kConsumerWarps>
 struct Cfg {
+  static constexpr int THREADS = 32 * (CW + 1);  // + the producer warp
   static constexpr int ELEM = FP8 ? 1 : 2;
   static constexpr int CE = 128 / ELEM;         // elements per 128-byte row chunk
   static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
@@ -114,7 +116,7 @@ struct Cfg {
   static constexpr int QCH = D / 64;
   static constexpr int QCHUNK = ROWS * 128;
   static constexpr int QSLOT = QCH * QCHUNK;
-  static constexpr int NGW = kConsumerWarps / MT;  // warps per row tile, each holding a partial result
+  static constexpr int NGW = CW / MT;  // warps per row tile, each holding a partial result
   static constexpr int RSTR = D + 8;               // floats per row of the merge buffer
   static constexpr int RED = (NGW - 1) * ROWS * RSTR * 4;
   static constexpr int REDML = (NGW - 1) * ROWS * 2 * 4;
@@ -130,6 +132,7 @@ struct Cfg {
   static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
   static_assert(MT == 1 || MT == 2 || MT == 4, "unsupported row tiles");
   static_assert(TSL == 16 || TSL == 32 || TSL == 64, "unsupported warp slice");
+  static_assert(CW == 4 || CW == 8, "unsupported consumer warps");
 };
 
 // ----------------------------------------------------------------- schedule
@@ -303,11 +306,13 @@ __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_va
 // (e4m3fn caches with scales; q and out bf16), f16 (q, caches, out f16).
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvF16 = 2;
 
-template <int D, int MT, int KV, int TSL>
-__global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_constant__ SplitParams p) {
+template <int D, int MT, int KV, int TSL, int CW>
+__global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
+    pa_split_kernel(const __grid_constant__ SplitParams p) {
   constexpr bool FP8 = KV == kKvFp8;
   constexpr bool F16 = KV == kKvF16;  // 16-bit path in f16 instead of bf16
-  using C = Cfg<D, MT, FP8, TSL>;
+  using C = Cfg<D, MT, FP8, TSL, CW>;
+  constexpr int kThreads = C::THREADS;
   constexpr int NS = C::NS;
   constexpr int NGW = C::NGW;
   constexpr int NCH = C::NCH;
@@ -333,11 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kConsumerWarps);
+      mbar_init(bar_empty + 8 * s, CW);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(bar_qfull + 8 * q, 1);
-      mbar_init(bar_qempty + 8 * q, kConsumerWarps);
+      mbar_init(bar_qempty + 8 * q, CW);
     }
     *s_abort = 0;
     fence_mbar_init();
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
   const int TS = p.TS;
   // Bytes per key row of all H2 heads (+ their fp8 scales) in a stage.
   const uint32_t row_bytes = H2 * D * C::ELEM + (FP8 ? p.Hkv * 4 : 0);
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ================================================================ producer
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
@@ -529,9 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
       if (s_ctx[b] != 0) continue;
       const size_t rows = (size_t)p.T * p.Hq;
       uint4* o4 = reinterpret_cast<uint4*>(p.out + (size_t)b * rows * D);
-      for (size_t i = ctid; i < rows * D / 8; i += 32 * kConsumerWarps) o4[i] = make_uint4(0, 0, 0, 0);
+      for (size_t i = ctid; i < rows * D / 8; i += 32 * CW) o4[i] = make_uint4(0, 0, 0, 0);
       if (p.lse)
-        for (size_t i = ctid; i < rows; i += 32 * kConsumerWarps) p.lse[(size_t)b * rows + i] = NEG_INF;
+        for (size_t i = ctid; i < rows; i += 32 * CW) p.lse[(size_t)b * rows + i] = NEG_INF;
     }
   }
 
@@ -578,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
             __syncwarp();
           }
         }
-        named_barrier_sync(1, 32 * kConsumerWarps);
+        named_barrier_sync(1, 32 * CW);
       }
 #pragma unroll
       for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -810,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     if (NGW > 1) {
-      named_barrier_sync(1, 32 * kConsumerWarps);
+      named_barrier_sync(1, 32 * CW);
       if (gi > 0) {
         float* rb = red + (size_t)(gi - 1) * C::ROWS * C::RSTR;
 #pragma unroll
@@ -826,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_split_kernel(const __grid_cons
           ml[2 * rho1 + 1] = l1;
         }
       }
-      named_barrier_sync(1, 32 * kConsumerWarps);
+      named_barrier_sync(1, 32 * CW);
     }
     if (gi != 0) continue;
 

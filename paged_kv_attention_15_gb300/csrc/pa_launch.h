@@ -11,12 +11,13 @@ struct SplitKernel {
   const void* fn;   // __global__ function, launched with cudaLaunchKernel
   int smem_fixed;   // dynamic shared memory without the per-sequence table
   int stages;       // pipeline depth of the instance
+  int threads;      // block size: 32 * (consumer warps + 1)
 };
 
-// Kernel instance for (head_dim, row tiles, tokens per warp slice);
-// fn == nullptr if that combination is not built.
-SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice);
-SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice);
-SplitKernel split_kernel_f16(int head_dim, int row_tiles, int slice);
+// Kernel instance for (head_dim, row tiles, tokens per warp slice,
+// consumer warps); fn == nullptr if that combination is not built.
+SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice, int consumer_warps);
+SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice, int consumer_warps);
+SplitKernel split_kernel_f16(int head_dim, int row_tiles, int slice, int consumer_warps);
 
 }  // namespace pa
