@@ -401,3 +401,37 @@ def test_graph_capture_replays_like_eager():
     assert torch.equal(got[0], eager[0]) and torch.equal(got[1], eager[1])
     ref_out, ref_lse = oracle.decode(ora_inputs(other), other.scale)
     assert_match(*to_np(*got), ref_out, ref_lse, 1e-2)
+
+
+# ----------------------------------------------------------- random shapes
+def random_case(rng):
+    """A small problem drawn from every supported axis at once."""
+    kv_format = str(rng.choice(["bf16", "bf16", "fp8", "f16"]))
+    D = int(rng.choice([128, 256] if kv_format == "fp8" else [64, 128, 256]))
+    Hkv = int(rng.choice([1, 2, 4, 8] if kv_format == "fp8" else [1, 2, 3, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+    tidar = kv_format == "bf16" and rng.random() < 0.3
+    T = int(rng.integers(1, max(2, min(8, 32 // G)) + 1))
+    while G * T > 32:
+        T -= 1
+    P = int(rng.choice([16, 32, 64, 128, 256]))
+    B = int(rng.integers(1, 6))
+    lens = [int(x) for x in rng.integers(0, 600, B)]
+    if rng.random() < 0.3:
+        lens[0] = 0
+    case = dict(batch=B, q_tokens=T, num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, page_size=P,
+                context_lens=tuple(lens), kv_format=kv_format, draft_scratch=tidar,
+                seed=int(rng.integers(1 << 30)))
+    if tidar and rng.random() < 0.5:
+        case["draft_block"] = int(rng.integers(1, T + 1))
+    return case, int(rng.choice([0, 0, 1, 2, 5]))
+
+
+@pytest.mark.parametrize("i", range(60))
+def test_random_shapes(i):
+    case, num_splits = random_case(np.random.default_rng(1000 + i))
+    inp = gen.make_inputs(spec(**case))
+    oi = ora_inputs(inp)
+    ref_out, ref_lse = oracle.decode(oi, inp.scale)
+    out, lse = to_np(*gpu_decode(inp, num_splits))
+    assert_match(out, lse, ref_out, ref_lse, tol_of(inp.spec))
