@@ -50,13 +50,16 @@
  *
  * Supported: D in {64, 128, 256} (fp8: {128, 256}); P in {16, 32, 64, 128,
  * 256}; M = G * T <= 64 query rows per kv head (more than 32 rows: D in {64,
- * 128}, bf16 pages); fp8 needs Hkv <= 8.
+ * 128}, 16-bit pages); fp8 needs Hkv <= 8.
  * Anything else returns PA_ERR_UNSUPPORTED.
  *
  * num_splits:
  *   0   auto. The flattened list of (sequence, kv head, page) work is cut into
  *       equal contiguous shares, one per CTA of a grid that fills the SMs, so
- *       sequences of any length mix are balanced. Needs the workspace of
+ *       sequences of any length mix are balanced; a dependent launch combines
+ *       the sequences split between CTAs. With so many sequences that their
+ *       table does not fit in shared memory, it runs the explicit split count
+ *       pa_decode_choose_splits() reports instead. Needs the workspace of
  *       pa_decode_workspace_size(shape, 0) (its layout is private).
  *   1   one CTA per (sequence, kv head) writes out/lse directly; no workspace.
  *   S>1 split s of sequence b covers pages [s*pps, min((s+1)*pps, n_b)),
