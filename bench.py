@@ -414,6 +414,7 @@ def run_ours(args, world, rank, local):
     achieved = nbytes / (split_mean_ms / 1e3) / 1e9
 
     e2e = run_e2e(args, host, dev, pb, nbytes, world)
+    serving = run_serving_step(args, host, dev, pb, nbytes, world)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -439,6 +440,7 @@ def run_ours(args, world, rank, local):
                      "kernel": "pa_split_kernel"},
         "clocks": clocks.summary(),
         "e2e": e2e,
+        "e2e_serving_step": serving,
         "gpu_launches": 2 * args.steps if (args.num_splits != 1) else args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -584,6 +586,81 @@ def run_append(args, world, rank, local):
         result["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                                   "sample": desc, "seconds": secs}
     return result
+
+
+def run_serving_step(args, host, dev, pb, nbytes, world):
+    """One serving decode step through the public calls, the KV cache resident
+    on the device (filled once, untimed): every step copies q, the new
+    token's K/V rows, the block table and the lengths (and the draft scratch)
+    from pinned host memory, appends the new rows at position C_b - 1
+    (quantising them for an fp8 cache), decodes over C_b tokens and reads out
+    and lse back. value = the decode's algorithmic bytes / step time."""
+    spec = host.spec
+    B, Hkv, D = spec.batch, spec.num_kv_heads, spec.head_dim
+    devset = host.to(dev)
+    gen_new = torch.Generator().manual_seed(spec.seed + 77)
+    dt = torch.float16 if spec.kv_format == "f16" else torch.bfloat16
+    if spec.kv_format == "f16":
+        return None  # the append takes bf16 rows
+    k_new = torch.randn(B, 1, Hkv, D, generator=gen_new).to(dt).pin_memory()
+    v_new = torch.randn(B, 1, Hkv, D, generator=gen_new).to(dt).pin_memory()
+    per_step = {"q": host.q, "block_tables": host.block_tables, "context_lens": host.context_lens}
+    if host.k_scratch is not None:
+        per_step.update(k_scratch=host.k_scratch, v_scratch=host.v_scratch)
+    pinned = {n: t.pin_memory() for n, t in per_step.items()}
+    pos_h = (host.context_lens - 1).clamp(min=0).to(torch.int32).pin_memory()  # append position per sequence
+    kn_d, vn_d = torch.empty_like(k_new, device=dev), torch.empty_like(v_new, device=dev)
+    pos_d = torch.empty_like(pos_h, device=dev)
+    shape = pb.make_shape(devset.q, devset.k_cache, devset.block_tables)
+    ws = torch.empty(max(pb.workspace_size(shape, args.num_splits), 1), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(devset.q)
+    lse = torch.empty(devset.q.shape[:3], dtype=torch.float32, device=dev)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(pinned.values()) + [k_new, v_new, pos_h])
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(st):
+        for name, t in pinned.items():
+            getattr(devset, name).copy_(t, non_blocking=True)
+        kn_d.copy_(k_new, non_blocking=True)
+        vn_d.copy_(v_new, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        pb.kv_append(kn_d, vn_d, devset.block_tables, pos_d, devset.k_cache, devset.v_cache,
+                     k_scale=devset.k_scale, v_scale=devset.v_scale, stream=st)
+        pb.decode_inputs(devset, out=out, lse=lse, workspace=ws, num_splits=args.num_splits, stream=st)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, min(args.warmup, 10))):
+        step(stream)
+    torch.cuda.synchronize(dev)
+    # The step (copies included) as one CUDA graph, as a serving loop issues it.
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            step(cap)
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    k = max(1, min(args.steps, 200))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with torch.cuda.stream(cap):
+        a.record(cap)
+        for _ in range(k):
+            g.replay()
+        b.record(cap)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": aggregate_throughput(nbytes, k, ms / 1e3, world), "unit": UNIT, "us_per_step": ms * 1e3 / k,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
+            "kernels": "pa_kv_append(_fp8) + pa_decode*",
+            "note": "KV cache resident; the new token's rows appended; each step one CUDA-graph replay of the "
+                    "copies, the append, the decode and the read-back"}
 
 
 def run_e2e(args, host, dev, pb, nbytes, world):
