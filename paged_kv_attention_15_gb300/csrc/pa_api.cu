@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -27,15 +28,17 @@ __device__ int g_pa_err_flags;
 constexpr int kMaxDevices = 64;
 constexpr int kKernelSlots = 16;
 
+// Per-device values looked up once; `ready` publishes them (release) to
+// threads that read it (acquire) without taking the lock.
 struct DeviceState {
-  bool ready = false;
-  int sms = 0;
-  int smem_optin = 0;
-  int* err_flags = nullptr;
-  const void* smem_set[kKernelSlots] = {};
+  std::atomic<bool> ready;
+  int sms;
+  int smem_optin;
+  int* err_flags;
+  std::atomic<const void*> smem_set[kKernelSlots];  // kernels whose shared-memory limit was raised
 };
 
-DeviceState g_dev[kMaxDevices];
+DeviceState g_dev[kMaxDevices];  // zero-initialised (static storage)
 std::mutex g_mu;
 
 // One-shot events armed by pa_decode_profile_events for this thread's next call.
@@ -49,16 +52,16 @@ pa_status device_state(DeviceState** out) {
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
   DeviceState& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PA_ERR_CUDA;
       if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return PA_ERR_CUDA;
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_pa_err_flags) != cudaSuccess) return PA_ERR_CUDA;
       d.err_flags = static_cast<int*>(ptr);
-      d.ready = true;
+      d.ready.store(true, std::memory_order_release);
     }
   }
   *out = &d;
@@ -68,14 +71,15 @@ pa_status device_state(DeviceState** out) {
 // Raises the kernel's dynamic shared-memory limit once per device.
 pa_status ensure_smem_attr(DeviceState* d, const void* fn) {
   for (int i = 0; i < kKernelSlots; ++i)
-    if (d->smem_set[i] == fn) return PA_OK;
+    if (d->smem_set[i].load(std::memory_order_acquire) == fn) return PA_OK;
   std::lock_guard<std::mutex> lock(g_mu);
   for (int i = 0; i < kKernelSlots; ++i) {
-    if (d->smem_set[i] == fn) return PA_OK;
-    if (d->smem_set[i] == nullptr) {
+    const void* cur = d->smem_set[i].load(std::memory_order_relaxed);
+    if (cur == fn) return PA_OK;
+    if (cur == nullptr) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
         return PA_ERR_CUDA;
-      d->smem_set[i] = fn;
+      d->smem_set[i].store(fn, std::memory_order_release);
       return PA_OK;
     }
   }
@@ -587,7 +591,7 @@ const char* pa_status_string(pa_status status) {
 static __device__ __align__(256) unsigned char g_pa_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
 static void* g_noalloc_ptr[kMaxDevices];
-static bool g_noalloc_ready[kMaxDevices];
+static std::atomic<bool> g_noalloc_ready[kMaxDevices];  // publishes g_noalloc_ptr (release/acquire)
 
 // Device address of this device's scratch array. In host code the array's
 // name stands for a host-side shadow, so the address must come from the
@@ -596,13 +600,13 @@ static pa_status noalloc_scratch(void** ptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
-  if (!g_noalloc_ready[dev]) {
+  if (!g_noalloc_ready[dev].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_noalloc_ready[dev]) {
+    if (!g_noalloc_ready[dev].load(std::memory_order_relaxed)) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_pa_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
       g_noalloc_ptr[dev] = p;
-      g_noalloc_ready[dev] = true;
+      g_noalloc_ready[dev].store(true, std::memory_order_release);
     }
   }
   *ptr = g_noalloc_ptr[dev];

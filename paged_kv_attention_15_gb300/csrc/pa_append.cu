@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -184,28 +185,36 @@ void magic(uint32_t d, uint32_t* m, int* l) {
   *m = (uint32_t)(((1ull << 32) * ((1ull << s) - d)) / d + 1);
 }
 
+// Per-device values cached by any thread (idempotent: a race only repeats
+// the query).
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < 64 && cached[dev]) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < 64) cached[dev] = n;
+  if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
 // Resident blocks per SM of an instance, asked of the runtime once per device.
 template <bool FP8, int D>
 int blocks_per_sm() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-  if (dev < 64 && cached[dev]) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pa_kv_append_kernel<FP8, D>, 256, 0) != cudaSuccess || n < 1)
     n = 1;
-  if (dev < 64) cached[dev] = n;
+  if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
