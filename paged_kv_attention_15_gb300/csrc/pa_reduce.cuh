@@ -1,12 +1,72 @@
-// Split-K combine kernels (included by the C-ABI unit only); the row
-// combine itself is `combine_row` in pa_kernels.cuh. Source: the MSLK pull request "[ROCm] Add FlyDSL
-// paged-attention decode backend (dense + fp8) with benchmark" (Kernels:
-// pa_decode_reduce, the split-K partial combine).
+// Split-K combine kernels (included by the C-ABI unit only). Source: the
+// MSLK pull request "[ROCm] Add FlyDSL paged-attention decode backend (dense
+// + fp8) with benchmark" (Kernels: pa_decode_reduce, the split-K partial
+// combine).
 #pragma once
 
 #include "pa_kernels.cuh"
 
 namespace pa {
+
+// ------------------------------------------------------------ row combine
+// One warp combines the pieces k = 0..np-1 of one query row: M = max_k lse_k,
+// w_k = exp(lse_k - M), out = sum_k w_k o_k / sum_k w_k, lse = M + ln sum_k w_k,
+// in one online pass (running max, sums rescaled when it grows) that keeps
+// the loads of eight pieces in flight. Pieces with lse = -inf weigh 0; a row
+// whose pieces are all empty gets out = 0, lse = -inf. o_row(k) points at
+// piece k's D (<= 256) floats in global memory, read past L1 (other CTAs of
+// the same grid may have written them); l_val(k) is its lse. Lane l owns
+// columns 4l..4l+3 and 128+4l..128+4l+3. Source: the MSLK pull request
+// "[ROCm] Add FlyDSL paged-attention decode backend (dense + fp8) with
+// benchmark" (Kernels: pa_decode_reduce, the split-K combine).
+template <typename ORow, typename LVal>
+__device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_val, __nv_bfloat16* out,
+                                            float* lse_out, int lane, bool out_f16) {
+  auto pack = [&](float lo, float hi) { return out_f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float LOG2E = 1.4426950408889634f;
+  const int c0 = lane * 4, c1 = 128 + lane * 4;
+  const bool h0 = c0 < D, h1 = c1 < D;
+  float m = NEG_INF, L = 0.f;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  for (int k0 = 0; k0 < np; k0 += 8) {
+    float lk[8];
+    float4 v0[8], v1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool in = k0 + j < np;
+      lk[j] = in ? l_val(k0 + j) : NEG_INF;
+      const float* o = in ? o_row(k0 + j) : nullptr;
+      v0[j] = in && h0 ? __ldcg(reinterpret_cast<const float4*>(o + c0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v1[j] = in && h1 ? __ldcg(reinterpret_cast<const float4*>(o + c1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float mc = fmaxf(fmaxf(fmaxf(m, fmaxf(lk[0], lk[1])), fmaxf(lk[2], lk[3])),
+                           fmaxf(fmaxf(lk[4], lk[5]), fmaxf(lk[6], lk[7])));
+    if (mc == NEG_INF) continue;
+    const float so = m == NEG_INF ? 0.f : ex2((m - mc) * LOG2E);
+    a0.x *= so; a0.y *= so; a0.z *= so; a0.w *= so;
+    a1.x *= so; a1.y *= so; a1.z *= so; a1.w *= so;
+    L *= so;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (lk[j] == NEG_INF) continue;
+      const float w = ex2((lk[j] - mc) * LOG2E);
+      a0.x += w * v0[j].x; a0.y += w * v0[j].y; a0.z += w * v0[j].z; a0.w += w * v0[j].w;
+      a1.x += w * v1[j].x; a1.y += w * v1[j].y; a1.z += w * v1[j].z; a1.w += w * v1[j].w;
+      L += w;
+    }
+    m = mc;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  if (h0)
+    *reinterpret_cast<uint2*>(out + c0) =
+        make_uint2(pack(a0.x * inv, a0.y * inv), pack(a0.z * inv, a0.w * inv));
+  if (h1)
+    *reinterpret_cast<uint2*>(out + c1) =
+        make_uint2(pack(a1.x * inv, a1.y * inv), pack(a1.z * inv, a1.w * inv));
+  if (lane == 0 && lse_out) *lse_out = L > 0.f ? m + lg2(L) * kLn2 : NEG_INF;
+}
+
 
 // Explicit splits: grid covers B*T*Hq rows, 4 rows (warps) per CTA.
 __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_constant__ ReduceParams p) {
