@@ -144,3 +144,69 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pb, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         pb.lib()
+
+
+C_PROGRAM = r"""
+#include <stdint.h>
+#include <stdio.h>
+#include "pa_decode.h"
+
+/* Stand-ins for device buffers: aligned host memory that no call below
+   reaches, since each one fails (or finishes) in its host-side checks. */
+static int32_t buf[64] __attribute__((aligned(256)));
+
+typedef void (*any_fn)(void);
+
+int main(void) {
+  void* p = buf;
+  const int32_t* ip = buf;
+  uint8_t* u8 = (uint8_t*)buf;
+  float* fp = (float*)buf;
+  pa_shape s = {2, 1, 8, 2, 128, 16, 64, 8};
+  pa_shape bad = s;
+  bad.head_dim = 96;
+  /* every entry point the header declares resolves at link time */
+  any_fn entries[] = {
+      (any_fn)pa_decode_workspace_size, (any_fn)pa_decode_choose_splits, (any_fn)pa_decode,
+      (any_fn)pa_decode_fp8, (any_fn)pa_decode_f16, (any_fn)pa_decode_tidar, (any_fn)pa_decode_tidar_masked,
+      (any_fn)pa_decode_reduce, (any_fn)pa_kv_append, (any_fn)pa_kv_append_fp8, (any_fn)pa_decode_noalloc,
+      (any_fn)pa_status_string, (any_fn)pa_decode_profile_events, (any_fn)pa_decode_device_error};
+  for (unsigned i = 0; i < sizeof entries / sizeof entries[0]; ++i)
+    if (!entries[i]) return 10;
+  if (!pa_status_string(PA_OK)[0] || !pa_status_string((pa_status)99)[0]) return 1;
+  if (pa_decode(p, p, p, ip, ip, &bad, 0.1f, p, NULL, 1, NULL, 0, NULL) != PA_ERR_UNSUPPORTED) return 2;
+  if (pa_decode(NULL, p, p, ip, ip, &s, 0.1f, p, NULL, 1, NULL, 0, NULL) != PA_ERR_INVALID_ARG) return 3;
+  if (pa_decode_workspace_size(&s, 1) != 0) return 4;
+  if (pa_decode_choose_splits(&bad, 0) != -1) return 5;
+  if (pa_kv_append(NULL, p, ip, ip, &s, p, p, NULL) != PA_ERR_INVALID_ARG) return 6;
+  if (pa_kv_append_fp8(p, p, ip, ip, &bad, u8, u8, fp, fp, NULL) != PA_ERR_UNSUPPORTED) return 7;
+  if (pa_decode_tidar_masked(p, p, p, p, p, ip, ip, &s, 0.1f, 0, p, NULL, 1, NULL, 0, NULL) != PA_ERR_INVALID_ARG)
+    return 8;
+  if (pa_decode_reduce(fp, fp, 0, &s, p, NULL, NULL) != PA_ERR_INVALID_ARG) return 9;
+  if (pa_decode_profile_events(NULL, NULL) != PA_OK) return 11;
+  printf("c abi ok %u\n", (unsigned)PA_NOALLOC_SCRATCH_BYTES);
+  return 0;
+}
+"""
+
+
+def test_header_compiles_as_c99_and_links(lib, tmp_path):
+    """A plain C program (gcc, -std=c99, no CUDA headers) includes the header,
+    links the library and gets its argument checks through the C ABI."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(pb.LIB_PATH)
+    include = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    cc = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-o", str(exe), str(src), "-I", include,
+                         "-L", libdir, "-lpadecode", "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr[-3000:]
+    res = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert res.returncode == 0, (res.returncode, res.stdout, res.stderr)
+    assert res.stdout.startswith("c abi ok")
