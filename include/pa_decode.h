@@ -50,7 +50,7 @@
  *
  * Supported: D in {64, 128, 256} (fp8: {128, 256}); P in {16, 32, 64, 128,
  * 256}; M = G * T <= 64 query rows per kv head (more than 32 rows: D in {64,
- * 128}, 16-bit pages); fp8 needs Hkv <= 8.
+ * 128}, 16-bit pages).
  * Anything else returns PA_ERR_UNSUPPORTED.
  *
  * num_splits:

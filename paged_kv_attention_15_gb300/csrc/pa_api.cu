@@ -137,7 +137,6 @@ pa_status check_shape(const pa_shape* s, Kind kind) {
   const int D = s->head_dim;
   if (kind == Kind::kFp8) {
     if (D != 128 && D != 256) return PA_ERR_UNSUPPORTED;
-    if (s->num_kv_heads > pa::kMaxHkvFp8) return PA_ERR_UNSUPPORTED;
   } else if (D != 64 && D != 128 && D != 256) {
     return PA_ERR_UNSUPPORTED;
   }
@@ -157,7 +156,7 @@ SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL, int CW) {
 // Work-unit geometry: H2 kv heads per CTA unit, their M = H2 * G * T query
 // rows in MT m16 tiles, TS = 64 / H2 tokens per stage, TSL tokens per warp.
 struct Geom {
-  int GT, H2, NHG, M, MT, TS, TSL, BR, lbr, TP;
+  int GT, H2, NHG, M, MT, TS, TSL, BR, lbr, TP, ilv;
   SplitKernel k;
 };
 
@@ -197,6 +196,18 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
     }
   }
   if (!k.fn) return false;
+  // fp8: where two slice groups would each take 16 tokens of every stage,
+  // they take all 32 tokens of every other stage instead (twice the
+  // independent MMA chains per warp, half the softmax reductions per token).
+  g->ilv = 1;
+  if (fp8 && TSL == 16 && (TS / TSL) % 2 == 0) {
+    const SplitKernel k2 = pick_kernel(kind, D, MT, 32, k.threads / 32 - 1);
+    if (k2.fn) {
+      k = k2;
+      TSL = 32;
+      g->ilv = 2;
+    }
+  }
   g->GT = GT;
   g->H2 = H2;
   g->NHG = s->num_kv_heads / H2;
@@ -395,6 +406,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   p.NHG = geo.NHG;
   p.GT = geo.GT;
   p.TS = geo.TS;
+  p.ilv = geo.ilv;
   p.BR = geo.BR;
   p.lbr = geo.lbr;
   p.TP = geo.TP;

@@ -48,7 +48,6 @@ constexpr int kConsumerWarps = 4;  // consumer warps of most instances (one per 
 // 16 KB and the per-stage waits and arrivals spread over as many bytes.
 // The host picks the rows a launch actually uses per stage (p.TS * H2).
 constexpr int stage_rows(int row_bytes, bool fp8) { return !fp8 && row_bytes <= 128 ? 128 : 64; }
-constexpr int kMaxHkvFp8 = 8;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kErrWaitTimeout = 1;
@@ -77,6 +76,7 @@ struct SplitParams {
   int NHG;         // head groups per sequence, Hkv / H2
   int GT;          // query rows per kv head, G * T
   int TS;          // tokens per stage, 64 / H2
+  int ilv;         // 1, or 2: slice group ts takes only the stages j with j % 2 == ts % 2
   int BR, lbr;     // rows of a page box, min(P, TS), and its log2
   int TP;          // scratch rows per box: T rounded up to a multiple of 8
   int num_splits;  // >= 1: explicit splits (grid = units x splits); 0: balanced (grid = CTAs)
@@ -110,8 +110,7 @@ struct Cfg {
   static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
   static constexpr int SROWS = stage_rows(D * ELEM, FP8);
   static constexpr int TILE = SROWS * D * ELEM;  // bytes of the K (or V) tile of a stage
-  static constexpr int SCALE = FP8 ? SROWS * kMaxHkvFp8 * 4 : 0;
-  static constexpr int STAGE = round_up(2 * TILE + 2 * SCALE, 1024);
+  static constexpr int STAGE = round_up(2 * TILE, 1024);
   static constexpr int ROWS = 16 * MT;
   static constexpr int QCH = D / 64;
   static constexpr int QCHUNK = ROWS * 128;
@@ -319,8 +318,8 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
   const int P = p.P;
   const int H2 = p.H2;
   const int TS = p.TS;
-  // Bytes per key row of all H2 heads (+ their fp8 scales) in a stage.
-  const uint32_t row_bytes = H2 * D * C::ELEM + (FP8 ? p.Hkv * 4 : 0);
+  // Bytes per key row of all H2 heads in a stage.
+  const uint32_t row_bytes = H2 * D * C::ELEM;
   if (warp == CW) {
     // ================================================================ producer
     const uint64_t pol_kv = l2_policy_evict_first();
@@ -371,8 +370,6 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
         const uint32_t full = bar_full + 8 * slot;
         const uint32_t kdst = sbase + slot * C::STAGE;
         const uint32_t vdst = kdst + C::TILE;
-        const uint32_t ksd = kdst + 2 * C::TILE;
-        const uint32_t vsd = ksd + C::SCALE;
         if (it.scratch && j == it.nst - 1) {
           if (lane == 0) {  // rows T..TP-1 of the box are outside the tensor: zero filled
             mbar_arrive_expect_tx(full, 2 * NCH * H2 * p.TP * 128);
@@ -389,17 +386,6 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
           ids = ids_next;
           ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
         }
-        // fp8 scales: rows [token][Hkv] of the stage's pages, one bulk copy
-        // per page and tensor. A page id outside the pool reads zero codes
-        // (tensor-map fill); its scales come from page 0 so that they stay
-        // finite and the copy stays in bounds.
-        auto copy_scales = [&](uint32_t soff, int page, int row0, int rows) {
-          const uint32_t sb = rows * p.Hkv * 4;
-          if ((unsigned)page >= (unsigned)p.num_pages) page = 0;
-          const size_t off = ((size_t)page * P + row0) * p.Hkv;
-          bulk_load(ksd + soff, p.k_scale + off, sb, full, pol_kv);
-          bulk_load(vsd + soff, p.v_scale + off, sb, full, pol_kv);
-        };
         if (P < TS) {  // whole pages: one box each
           const int npg = (valid + P - 1) / P;
           if (lane == 0) mbar_arrive_expect_tx(full, 2 * npg * P * row_bytes);
@@ -409,7 +395,6 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
               const uint32_t boff = i * NCH * H2 * P * 128;
               tma_load_5d(kdst + boff, &p.tm_k, full, 0, 0, it.hg * H2, 0, page, pol_kv);
               tma_load_5d(vdst + boff, &p.tm_v, full, 0, 0, it.hg * H2, 0, page, pol_kv);
-              if (FP8) copy_scales(i * P * p.Hkv * 4, page, 0, P);
             }
           }
         } else {  // TS rows of one page
@@ -419,7 +404,6 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
             mbar_arrive_expect_tx(full, 2 * TS * row_bytes);
             tma_load_5d(kdst, &p.tm_k, full, 0, row0, it.hg * H2, 0, page, pol_kv);
             tma_load_5d(vdst, &p.tm_v, full, 0, row0, it.hg * H2, 0, page, pol_kv);
-            if (FP8) copy_scales(0, page, row0, TS);
           }
         }
       }
@@ -444,6 +428,8 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
   const int ht = GT >= 16 ? 1 : max(1, min(16 / GT, H2 - hl_base));
   const int hl = min(hl_base + gi % ht, H2 - 1);  // (a tile of padding rows only reads head H2-1)
   const int ts = gi / ht;
+  const int ph = ts % p.ilv;          // this warp's stages: j % ilv == ph
+  const int tb = (ts / p.ilv) * TSL;  // first token of this warp's slice of a stage
   const int r = lane >> 2;
   const int c4 = lane & 3;
   const int rho0 = mt * 16 + r, rho1 = rho0 + 8;
@@ -456,6 +442,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
     return min(p.T, (t / p.draft_block + 1) * p.draft_block);
   };
   const int vis0 = visible(rho0), vis1 = visible(rho1);
+  const int lp = 31 - __clz(p.P);  // log2 of the page size (a power of two)
   const float NEG_INF = -__int_as_float(0x7f800000);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* redml = reinterpret_cast<float*>(smem + C::OFF_REDML);
@@ -530,6 +517,34 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
+      // fp8 per-token scales, read from global memory by the consumers
+      // (small copies per page through the copy engine cost more than the
+      // K/V boxes they ride with): lane l holds the K and V scale of token
+      // tb + l % TSL of a stage (0 for a token past the item's end). The
+      // loads are issued one handled stage (ilv stages) ahead of their use,
+      // the page-id lookups they depend on two handled stages ahead.
+      const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
+      const int tok_l = it.tok0 + tb + (lane & (TSL - 1));  // this lane's token in stage 0
+      auto scale_page = [&](int jj) -> int {                // page of that token in stage jj, or -1
+        const int tok = tok_l + jj * TS;
+        if (tok >= it.tok_end) return -1;
+        const int pg = __ldg(bt_row + (tok >> lp));
+        return (unsigned)pg < (unsigned)p.num_pages ? pg : 0;  // outside the pool: page 0's (finite) scales
+      };
+      auto load_scales = [&](int jj, int pg, float& ks, float& vs) {
+        ks = vs = 0.f;
+        if (pg < 0) return;
+        const size_t off = ((size_t)pg << lp | ((tok_l + jj * TS) & (P - 1))) * p.Hkv + g;
+        ks = __ldg(p.k_scale + off);
+        vs = __ldg(p.v_scale + off);
+      };
+      float ks_cur = 0.f, vs_cur = 0.f, ks_next = 0.f, vs_next = 0.f;
+      int pg_next = -1;  // page of this lane's token in the stage after the next handled one
+      if (FP8) {
+        load_scales(ph, scale_page(ph), ks_next, vs_next);
+        pg_next = scale_page(ph + p.ilv);
+      }
+
       for (int j = 0; j < it.nst; ++j) {
         const int st = stage + j;
         const int slot = st % NS;
@@ -539,8 +554,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
         }
         const bool scr = it.scratch && j == it.nst - 1;
         const int valid = scr ? p.T : min(TS, it.tok_end - (it.tok0 + j * TS));
-        const int tb = ts * TSL;  // first token of this warp's slice
-        if (ok && tb < valid) {
+        if (ok && tb < valid && ((j ^ ph) & (p.ilv - 1)) == 0) {
           // Stage tile: [box][chunk][head][box row][128 B]; a box holds the
           // rows of one page (scratch: TP rows). Every token index used below
           // is a multiple of 8 plus (lane & 7), so the 128-byte swizzle of its
@@ -555,12 +569,18 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
           };
           const uint32_t kb_ = sbase + slot * C::STAGE;
           const uint32_t vb_ = kb_ + C::TILE;
-          const float* ksc = reinterpret_cast<const float*>(smem + slot * C::STAGE + 2 * C::TILE);
-          const float* vsc = ksc + C::SCALE / 4;
           const int sw = lane & 7;
+          if (FP8) {
+            ks_cur = ks_next;
+            vs_cur = vs_next;
+            load_scales(j + p.ilv, pg_next, ks_next, vs_next);
+            pg_next = scale_page(j + 2 * p.ilv);
+          }
 
-          // ---- S = Q K^T: 16 rows x TSL tokens. Two accumulators per tile
-          // (even and odd k-steps) halve the dependent MMA chain.
+          // ---- S = Q K^T: 16 rows x TSL tokens. 16-bit pages: two
+          // accumulators per tile (even and odd k-steps) halve the dependent
+          // MMA chain. fp8: one (its register budget is spent on the D = 256
+          // output; the 8-token tiles are the independent chains).
           float s[NTS][4], s2[NTS][4];
 #pragma unroll
           for (int i = 0; i < NTS; ++i) {
@@ -610,12 +630,12 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
                 ldsm_x4(krow[nt] + coff, kr[0], kr[1], kr[2], kr[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                  mma_f16((e & 1) ? s2[nt] : s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
+                  mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
               }
             }
           }
 #pragma unroll
-          for (int i = 0; i < NTS; ++i) {
+          for (int i = 0; i < (FP8 ? 0 : NTS); ++i) {  // (fp8 keeps one accumulator per tile)
             s[i][0] += s2[i][0];
             s[i][1] += s2[i][1];
             s[i][2] += s2[i][2];
@@ -630,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
             for (int e = 0; e < 4; ++e) {
               const int tok = tb + i * 8 + 2 * c4 + (e & 1);
               float f = s[i][e] * sl;
-              if (FP8) f *= ksc[tok * p.Hkv + g];
+              if (FP8) f *= __shfl_sync(0xffffffffu, ks_cur, i * 8 + 2 * c4 + (e & 1));
               const int lim = scr ? (e < 2 ? vis0 : vis1) : valid;
               s[i][e] = (tok < lim && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
             }
@@ -709,10 +729,15 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
             } else {
               // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
               float vs[4];
-              vs[0] = t0 < valid ? vsc[t0 * p.Hkv + g] : 0.f;
-              vs[1] = t0 + 1 < valid ? vsc[(t0 + 1) * p.Hkv + g] : 0.f;
-              vs[2] = t0 + 8 < valid ? vsc[(t0 + 8) * p.Hkv + g] : 0.f;
-              vs[3] = t0 + 9 < valid ? vsc[(t0 + 9) * p.Hkv + g] : 0.f;
+              const int tl = kb * 16 + 2 * c4;  // t0 - tb: the lane holding t0's scales
+              vs[0] = __shfl_sync(0xffffffffu, vs_cur, tl);
+              vs[1] = __shfl_sync(0xffffffffu, vs_cur, tl + 1);
+              vs[2] = __shfl_sync(0xffffffffu, vs_cur, tl + 8);
+              vs[3] = __shfl_sync(0xffffffffu, vs_cur, tl + 9);
+              vs[0] = t0 < valid ? vs[0] : 0.f;
+              vs[1] = t0 + 1 < valid ? vs[1] : 0.f;
+              vs[2] = t0 + 8 < valid ? vs[2] : 0.f;
+              vs[3] = t0 + 9 < valid ? vs[3] : 0.f;
               pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
               pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
               pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);

@@ -109,16 +109,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
 // ------------------------------------------------- programmatic dependent launch
 // Lets the next kernel in the stream (launched with programmatic stream
 // serialisation) start once every CTA of this grid has executed it.

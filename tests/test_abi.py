@@ -80,9 +80,6 @@ def test_fp8_and_tidar_validation(lib):
                              None, 0, None) == pb.PA_ERR_INVALID_ARG
     assert lib.pa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(shape(head_dim=64)), 0.1,
                              FAKE, None, 1, None, 0, None) == pb.PA_ERR_UNSUPPORTED
-    assert lib.pa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
-                             ctypes.byref(shape(num_q_heads=16, num_kv_heads=16)), 0.1, FAKE, None, 1, None, 0,
-                             None) == pb.PA_ERR_UNSUPPORTED  # > 8 kv heads
     assert lib.pa_decode_tidar(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, None, 1,
                                None, 0, None) == pb.PA_ERR_INVALID_ARG
     for bs in (0, -3):
