@@ -52,6 +52,13 @@ constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kErrWaitTimeout = 1;
 constexpr float kLn2 = 0.69314718055994530942f;
+// 16-bit pages: the running row max of the online softmax moves only when a
+// score passes it by more than this (log2 units). Probabilities 2^(s - m)
+// stay below 2^8, well inside f16 and bf16, and the accumulator is rescaled
+// a few times per row instead of at every new maximum; l and the
+// accumulator share m, so the result is the same up to rounding. (fp8 keeps
+// the exact max: its P operand also carries the V scale, in f16.)
+constexpr float kMaxSlack = 8.f;
 
 constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 constexpr int clamp_int(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
@@ -665,7 +672,8 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          constexpr float slack = FP8 ? 0.f : kMaxSlack;
+          const float mn0 = mx0 > m0 + slack ? mx0 : m0, mn1 = mx1 > m1 + slack ? mx1 : m1;
           const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
           const float mu1 = mn1 == NEG_INF ? 0.f : mn1;
           // alpha = 1 exactly when the running max did not move (also for

@@ -127,6 +127,19 @@ def test_fp8_sweep(case, num_splits):
     check_full(gen.make_inputs(spec(**case)), num_splits)
 
 
+@pytest.mark.parametrize("q_scale", [4.0, 16.0])
+@pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
+def test_spread_scores_move_the_running_max(kv_format, q_scale):
+    """Queries scaled up so that scores spread over many log2 units: the
+    running row max moves often, by less and by more than the 16-bit paths'
+    slack before a rescale, and the result still matches the oracle."""
+    inp = gen.make_inputs(spec(kv_format=kv_format, num_q_heads=16, num_kv_heads=1, head_dim=128,
+                               context_lens=(700, 33, 1, 260)))
+    q = (inp.q.float() * q_scale).to(inp.q.dtype)
+    check_full(dataclasses.replace(inp, q=q), 0)
+    check_full(dataclasses.replace(inp, q=q), 3)
+
+
 F16_SWEEP = [
     dict(kv_format="f16"),
     dict(kv_format="f16", head_dim=64, num_q_heads=32, num_kv_heads=1),
