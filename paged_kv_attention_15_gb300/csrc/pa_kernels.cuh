@@ -17,15 +17,17 @@
 // e4m3fn KV with symmetric per-token scale, split-K partial combine).
 //
 // GB300 design. One CTA per SM (persistent) or per (sequence, head group,
-// split). Warp 4 produces: it walks the block table and issues one TMA box
-// per page and stage (every column chunk of the page's rows of H2 kv heads;
-// for fp8 also the page's per-token scales by bulk copy) into a ring of NS
-// shared-memory stages of 64 key rows (64/H2 tokens x H2 heads), each
-// guarded by a pair of mbarriers (full: bytes landed; empty: consumers
-// done). H2 is chosen so a 16-row page still makes a large box: small
-// boxes cannot keep enough bytes in flight per SM. Warps 0-3 consume the
-// ring in order: warp w takes row tile w % MT and, inside it, one kv head
-// and one token slice of every stage, keeping its own online-softmax state.
+// split). The last warp produces: it walks the block table and issues one
+// TMA box per page and stage (every column chunk of the page's rows of H2
+// kv heads) into a ring of NS shared-memory stages of 64 key rows (64/H2
+// tokens x H2 heads), each guarded by a pair of mbarriers (full: bytes
+// landed; empty: consumers done). H2 is chosen so a 16-row page still makes
+// a large box: small boxes cannot keep enough bytes in flight per SM. The
+// other warps consume the ring in order: warp w takes row tile w % MT and,
+// inside it, one kv head and one token slice of every stage (or of every
+// other stage), keeping its own online-softmax state. fp8 consumers also
+// copy their tokens' scales into a small per-warp ring themselves, a few
+// stages ahead (4-byte asynchronous copies).
 // QK^T and PV run as mma.sync m16n8k16 with fp32 accumulators; the score
 // fragment becomes the P operand in registers; K is read with ldmatrix and
 // V with ldmatrix.trans from 128-byte-swizzled tiles (conflict-free). At
@@ -59,6 +61,10 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // accumulator share m, so the result is the same up to rounding. (fp8 keeps
 // the exact max: its P operand also carries the V scale, in f16.)
 constexpr float kMaxSlack = 8.f;
+// fp8: a consumer warp copies the scales of a stage this many handled
+// stages before it uses them (and keeps one more slot for the stage in use).
+constexpr int kScaleAhead = 2;
+constexpr int kScaleRing = kScaleAhead + 1;
 
 constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 constexpr int clamp_int(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
@@ -127,12 +133,16 @@ struct Cfg {
   static constexpr int RED = (NGW - 1) * ROWS * RSTR * 4;
   static constexpr int REDML = (NGW - 1) * ROWS * 2 * 4;
   static constexpr int BARS = 256;
-  static constexpr int FIXED = 2 * QSLOT + round_up(RED + REDML, 1024) + BARS;
+  // fp8: per consumer warp a ring of kScaleRing handled stages' K and V
+  // scales, one float per lane each.
+  static constexpr int SRING = FP8 ? CW * kScaleRing * 2 * 32 * 4 : 0;
+  static constexpr int FIXED = 2 * QSLOT + round_up(RED + REDML + SRING, 1024) + BARS;
   static constexpr int NS = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
   static constexpr int OFF_Q = NS * STAGE;
   static constexpr int OFF_RED = OFF_Q + 2 * QSLOT;
   static constexpr int OFF_REDML = OFF_RED + RED;
-  static constexpr int OFF_BAR = round_up(OFF_REDML + REDML, 1024);
+  static constexpr int OFF_SRING = OFF_REDML + REDML;
+  static constexpr int OFF_BAR = round_up(OFF_SRING + SRING, 1024);
   static constexpr int OFF_PREFIX = OFF_BAR + BARS;
   static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1024 to align the dynamic base
   static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
@@ -450,6 +460,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
   };
   const int vis0 = visible(rho0), vis1 = visible(rho1);
   const int lp = 31 - __clz(p.P);  // log2 of the page size (a power of two)
+  const uint64_t pol_scale = l2_policy_evict_first();
   const float NEG_INF = -__int_as_float(0x7f800000);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* redml = reinterpret_cast<float*>(smem + C::OFF_REDML);
@@ -524,32 +535,33 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-      // fp8 per-token scales, read from global memory by the consumers
-      // (small copies per page through the copy engine cost more than the
-      // K/V boxes they ride with): lane l holds the K and V scale of token
-      // tb + l % TSL of a stage (0 for a token past the item's end). The
-      // loads are issued one handled stage (ilv stages) ahead of their use,
-      // the page-id lookups they depend on two handled stages ahead.
+      // fp8 per-token scales, copied by the consumers themselves (small
+      // copies per page through the tensor-copy engine cost more than the
+      // K/V boxes they ride with): for the n-th stage this warp handles,
+      // lane l copies the K and V scale of token tb + l % TSL into slot
+      // n % kScaleRing of the warp's ring, kScaleAhead handled stages ahead,
+      // by 4-byte asynchronous copies (one commit group per stage).
       const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
       const int tok_l = it.tok0 + tb + (lane & (TSL - 1));  // this lane's token in stage 0
-      auto scale_page = [&](int jj) -> int {                // page of that token in stage jj, or -1
+      const uint32_t ring = sbase + C::OFF_SRING + warp * (kScaleRing * 2 * 32 * 4);
+      auto copy_scales = [&](int jj, int n) {  // stage jj, the warp's n-th handled stage
         const int tok = tok_l + jj * TS;
-        if (tok >= it.tok_end) return -1;
-        const int pg = __ldg(bt_row + (tok >> lp));
-        return (unsigned)pg < (unsigned)p.num_pages ? pg : 0;  // outside the pool: page 0's (finite) scales
+        if (tok < it.tok_end) {
+          int pg = __ldg(bt_row + (tok >> lp));
+          pg = (unsigned)pg < (unsigned)p.num_pages ? pg : 0;  // outside the pool: page 0's (finite) scales
+          const size_t off = ((size_t)pg << lp | (tok & (P - 1))) * p.Hkv + g;
+          const uint32_t dst = ring + (n % kScaleRing) * 256 + (lane & (TSL - 1)) * 4;
+          if (lane < TSL) {
+            cp_async4(dst, p.k_scale + off, pol_scale);
+            cp_async4(dst + 128, p.v_scale + off, pol_scale);
+          }
+        }
+        cp_async_commit();
       };
-      auto load_scales = [&](int jj, int pg, float& ks, float& vs) {
-        ks = vs = 0.f;
-        if (pg < 0) return;
-        const size_t off = ((size_t)pg << lp | ((tok_l + jj * TS) & (P - 1))) * p.Hkv + g;
-        ks = __ldg(p.k_scale + off);
-        vs = __ldg(p.v_scale + off);
-      };
-      float ks_cur = 0.f, vs_cur = 0.f, ks_next = 0.f, vs_next = 0.f;
-      int pg_next = -1;  // page of this lane's token in the stage after the next handled one
+      int nh = 0;  // stages this warp handled in this item
       if (FP8) {
-        load_scales(ph, scale_page(ph), ks_next, vs_next);
-        pg_next = scale_page(ph + p.ilv);
+#pragma unroll
+        for (int a = 0; a < kScaleAhead; ++a) copy_scales(ph + a * p.ilv, a);
       }
 
       for (int j = 0; j < it.nst; ++j) {
@@ -577,11 +589,14 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
           const uint32_t kb_ = sbase + slot * C::STAGE;
           const uint32_t vb_ = kb_ + C::TILE;
           const int sw = lane & 7;
+          const float* ksc = reinterpret_cast<const float*>(smem + C::OFF_SRING) +
+                             warp * (kScaleRing * 2 * 32) + (nh % kScaleRing) * 64;  // [token - tb]
+          const float* vsc = ksc + 32;
           if (FP8) {
-            ks_cur = ks_next;
-            vs_cur = vs_next;
-            load_scales(j + p.ilv, pg_next, ks_next, vs_next);
-            pg_next = scale_page(j + 2 * p.ilv);
+            copy_scales(j + kScaleAhead * p.ilv, nh + kScaleAhead);
+            cp_async_wait<kScaleAhead>();  // this stage's group has landed
+            __syncwarp();                  // ... for every lane's copies
+            ++nh;
           }
 
           // ---- S = Q K^T: 16 rows x TSL tokens. 16-bit pages: two
@@ -657,7 +672,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
             for (int e = 0; e < 4; ++e) {
               const int tok = tb + i * 8 + 2 * c4 + (e & 1);
               float f = s[i][e] * sl;
-              if (FP8) f *= __shfl_sync(0xffffffffu, ks_cur, i * 8 + 2 * c4 + (e & 1));
+              if (FP8) f *= ksc[tok - tb];
               const int lim = scr ? (e < 2 ? vis0 : vis1) : valid;
               s[i][e] = (tok < lim && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
             }
@@ -737,15 +752,11 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
             } else {
               // P~ = p * v_scale[token] in f16; masked tokens exactly 0.
               float vs[4];
-              const int tl = kb * 16 + 2 * c4;  // t0 - tb: the lane holding t0's scales
-              vs[0] = __shfl_sync(0xffffffffu, vs_cur, tl);
-              vs[1] = __shfl_sync(0xffffffffu, vs_cur, tl + 1);
-              vs[2] = __shfl_sync(0xffffffffu, vs_cur, tl + 8);
-              vs[3] = __shfl_sync(0xffffffffu, vs_cur, tl + 9);
-              vs[0] = t0 < valid ? vs[0] : 0.f;
-              vs[1] = t0 + 1 < valid ? vs[1] : 0.f;
-              vs[2] = t0 + 8 < valid ? vs[2] : 0.f;
-              vs[3] = t0 + 9 < valid ? vs[3] : 0.f;
+              const int tl = kb * 16 + 2 * c4;  // t0 - tb
+              vs[0] = t0 < valid ? vsc[tl] : 0.f;
+              vs[1] = t0 + 1 < valid ? vsc[tl + 1] : 0.f;
+              vs[2] = t0 + 8 < valid ? vsc[tl + 8] : 0.f;
+              vs[3] = t0 + 9 < valid ? vsc[tl + 9] : 0.f;
               pa[0] = pack_f16x2(s[2 * kb][0] * vs[0], s[2 * kb][1] * vs[1]);
               pa[1] = pack_f16x2(s[2 * kb][2] * vs[0], s[2 * kb][3] * vs[1]);
               pa[2] = pack_f16x2(s[2 * kb + 1][0] * vs[2], s[2 * kb + 1][1] * vs[3]);
@@ -893,6 +904,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
       }
     }
   }
+  if (FP8) cp_async_wait<0>();  // no scale copy may still be landing when the CTA exits
   launch_dependents();
 }
 

@@ -1,5 +1,6 @@
-// Inline-PTX building blocks for sm_103a: mbarriers, TMA tile and bulk
-// copies, ldmatrix, warp-level MMA, exp2/log2 and fp8 conversion.
+// Inline-PTX building blocks for sm_103a: mbarriers, TMA tile copies,
+// 4-byte asynchronous copies, ldmatrix, warp-level MMA, exp2/log2 and fp8
+// conversion.
 #pragma once
 
 #include <cstdint>
@@ -82,6 +83,22 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// 4-byte asynchronous copy global -> shared through L1 (no register
+// round trip), with an L2 eviction-priority policy; completion is tracked
+// per thread by commit groups.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
