@@ -599,10 +599,11 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
             ++nh;
           }
 
-          // ---- S = Q K^T: 16 rows x TSL tokens. 16-bit pages: two
-          // accumulators per tile (even and odd k-steps) halve the dependent
-          // MMA chain. fp8: one (its register budget is spent on the D = 256
-          // output; the 8-token tiles are the independent chains).
+          // ---- S = Q K^T: 16 rows x TSL tokens. Slices of 16 tokens on
+          // 16-bit pages: two accumulators per 8-token tile (even and odd
+          // k-steps) halve the dependent MMA chain. Longer slices and fp8:
+          // one (the slice's four or more tiles are the independent chains;
+          // the registers go to the output).
           float s[NTS][4], s2[NTS][4];
 #pragma unroll
           for (int i = 0; i < NTS; ++i) {
@@ -627,8 +628,8 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
               for (int nb = 0; nb < NTS / 2; ++nb) {
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(krow[nb] + coff, b0, b1, b2, b3);
-                mma16<F16>((kk & 1) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
-                mma16<F16>((kk & 1) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
+                mma16<F16>((NTS <= 2 && (kk & 1)) ? s2[2 * nb] : s[2 * nb], qa, b0, b1);
+                mma16<F16>((NTS <= 2 && (kk & 1)) ? s2[2 * nb + 1] : s[2 * nb + 1], qa, b2, b3);
               }
             }
           } else {
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
             }
           }
 #pragma unroll
-          for (int i = 0; i < (FP8 ? 0 : NTS); ++i) {  // (fp8 keeps one accumulator per tile)
+          for (int i = 0; i < (FP8 || NTS > 2 ? 0 : NTS); ++i) {  // (only 16-token 16-bit slices use s2)
             s[i][0] += s2[i][0];
             s[i][1] += s2[i][1];
             s[i][2] += s2[i][2];
