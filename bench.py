@@ -9,14 +9,19 @@ that no step finds its KV in the 129 MB L2. The append workloads
 decode instead: one step = one pa_kv_append(_fp8) call.
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--config gqa|long|fp8|tidar|append|append_fp8|append_step]
+                    [--config long|gqa|fp8|tidar|tiny|... (see WORKLOADS)]
                     [--impl ours|reference]
+
+The default workload is the long-context split-K decode (B4, 64/8 heads,
+D128, P64, 131072 keys per sequence: 2.15 GB per call), the largest of the
+problem statement's workloads that fits one GPU.
 
 Prints one JSON line on rank 0. `value` is the achieved algorithmic HBM
 bandwidth in GB/s (bytes a decode must move, see algorithmic_bytes, over
 the device time of a call), summed over ranks; `ms_per_step` is the time
-of one call. `--impl reference` times the fp64 CPU oracle on host cores on
-a bounded sample of the same workload.
+of one call. `--impl reference` times the fp64 CPU oracle on all host cores
+(one single-threaded process per core, spawned) on a bounded sample of the
+same workload; `cpu_baseline` reports that run and a one-core run.
 """
 
 from __future__ import annotations
@@ -50,7 +55,7 @@ METRIC = "paged decode µs/call and achieved HBM GB/s (fraction of 8 TB/s) on 1 
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_CONFIG = "gqa"
+DEFAULT_CONFIG = "long"
 
 WORKLOADS = {
     "tiny": "tiny paged decode: B2 T1 Hq4 Hkv1 D64 P16 ctx {37,100} bf16",
@@ -222,6 +227,19 @@ class ClockSampler:
                 "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
 
 
+def merge_clocks(timed: dict, kernel_pass: dict) -> dict:
+    """Clock record of the timed replays together with the kernel-only pass
+    that follows it (the GPU is busy in both)."""
+    out = dict(timed)
+    out["kernel_pass"] = kernel_pass
+    mhz = [x for x in (timed.get("sm_mhz"), kernel_pass.get("sm_mhz")) if x]
+    out["samples"] = (timed.get("samples") or 0) + (kernel_pass.get("samples") or 0)
+    out["reasons"] = sorted(set(timed.get("reasons") or []) | set(kernel_pass.get("reasons") or []))
+    if not timed.get("sm_mhz") and mhz:
+        out["sm_mhz"] = mhz[0]
+    return out
+
+
 # --------------------------------------------------------------------------- ranks
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -281,22 +299,18 @@ def oracle_seconds_per_key(inp) -> float:
     return max((time.perf_counter() - t) / max(probe, 1), 1e-9)
 
 
-def oracle_sample_run(inp, budget_s: float, start_unit: int = 0, per_key: float = None):
-    """Runs the oracle, as it stands, on whole (sequence, kv head) units (a
-    context prefix for the first unit when one unit alone exceeds the
-    budget). Returns (seconds, algorithmic bytes, description)."""
+def oracle_units_run(spec, bits, units, budget_s: float, per_key: float):
+    """Runs the oracle, as it stands, on the (sequence, kv head) units in
+    order until the budget is spent (whole units; a context prefix of the
+    first unit when it alone exceeds the budget). Returns (seconds,
+    algorithmic bytes, units done, prefix keys or None)."""
     import oracle
 
-    spec = inp.spec
-    bits = _oracle_bits(inp)
     ctx = bits["context_lens"].astype(np.int64)
-    units = [(b, g) for b in range(spec.batch) for g in range(spec.num_kv_heads)]
-    if per_key is None:
-        per_key = oracle_seconds_per_key(inp)
     done_s, done_bytes, n_units, prefix = 0.0, 0, 0, None
-    i = start_unit
-    while done_s < budget_s and n_units < len(units):
-        b, g = units[i % len(units)]
+    for (b, g) in units:
+        if done_s >= budget_s:
+            break
         c = int(ctx[b])
         run = dict(bits)
         if per_key * c > budget_s - done_s and n_units == 0:
@@ -311,11 +325,131 @@ def oracle_sample_run(inp, budget_s: float, start_unit: int = 0, per_key: float 
         done_s += time.perf_counter() - t
         done_bytes += unit_bytes(spec, c)
         n_units += 1
-        i += 1
+    return done_s, done_bytes, n_units, prefix
+
+
+def _all_units(spec, start_unit: int):
+    units = [(b, g) for b in range(spec.batch) for g in range(spec.num_kv_heads)]
+    k = start_unit % len(units)
+    return units[k:] + units[:k]
+
+
+def oracle_sample_run(inp, budget_s: float, start_unit: int = 0, per_key: float = None):
+    """The oracle on one core: whole (sequence, kv head) units from
+    start_unit on until the budget is spent. Returns (seconds, algorithmic
+    bytes, description)."""
+    spec = inp.spec
+    if per_key is None:
+        per_key = oracle_seconds_per_key(inp)
+    secs, nbytes, n_units, prefix = oracle_units_run(spec, _oracle_bits(inp), _all_units(spec, start_unit),
+                                                     budget_s, per_key)
     desc = f"{n_units} (sequence, kv head) unit(s) of the {spec.name} workload"
     if prefix is not None:
         desc += f", the first one cut to its first {prefix} keys"
-    return done_s, done_bytes, desc
+    return secs, nbytes, desc
+
+
+# The oracle on all host cores: one single-threaded process per core
+# (spawned, so safe next to CUDA), the workload's arrays shared with them
+# through shared memory (attached, not copied).
+_POOL_STATE = {}
+
+
+def _pool_init(meta, spec):
+    from multiprocessing import shared_memory
+
+    # (spawned children share the parent's resource tracker; the parent
+    # unlinks the blocks when the pool closes)
+    arrays, keep = {}, []
+    for name, (shm_name, shape, dtype) in meta["arrays"].items():
+        shm = shared_memory.SharedMemory(name=shm_name)
+        keep.append(shm)
+        arrays[name] = np.ndarray(shape, dtype=np.dtype(dtype), buffer=shm.buf)
+    arrays.update(meta["scalars"])
+    _POOL_STATE.update(bits=arrays, spec=spec, keep=keep)
+
+
+def _pool_task(units, budget_s, per_key):
+    st = _POOL_STATE
+    return oracle_units_run(st["spec"], st["bits"], units, budget_s, per_key)
+
+
+def _pool_ready(_):
+    return os.getpid()
+
+
+class OraclePool:
+    """A pool of `workers` spawned processes running the oracle on disjoint
+    units of one workload at once; run() returns the wall time of the whole
+    sample, so value = bytes / wall is the throughput of all cores."""
+
+    def __init__(self, inp, workers: int):
+        import concurrent.futures
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+
+        self.spec = inp.spec
+        self.workers = max(1, int(workers))
+        bits = _oracle_bits(inp)
+        self._shms, meta = [], {"arrays": {}, "scalars": {}}
+        for name, v in bits.items():
+            if isinstance(v, np.ndarray) and v.nbytes > 0:
+                shm = shared_memory.SharedMemory(create=True, size=v.nbytes)
+                np.ndarray(v.shape, dtype=v.dtype, buffer=shm.buf)[...] = v
+                self._shms.append(shm)
+                meta["arrays"][name] = (shm.name, v.shape, v.dtype.str)
+            else:
+                meta["scalars"][name] = v
+        self._ex = None
+        try:
+            self._ex = concurrent.futures.ProcessPoolExecutor(
+                max_workers=self.workers, mp_context=mp.get_context("spawn"), initializer=_pool_init,
+                initargs=(meta, self.spec))
+            # every worker started and attached before anything is timed
+            list(self._ex.map(_pool_ready, range(4 * self.workers)))
+        except BaseException:
+            self.close()
+            raise
+
+    def run(self, budget_s: float, per_key: float, start_unit: int = 0):
+        units = _all_units(self.spec, start_unit)
+        W = self.workers
+        shares = [units[w::W] for w in range(W)]
+        t = time.perf_counter()
+        res = list(self._ex.map(_pool_task, shares, [budget_s] * W, [per_key] * W))
+        wall = time.perf_counter() - t
+        nbytes = sum(r[1] for r in res)
+        n_units = sum(r[2] for r in res)
+        cut = sum(1 for r in res if r[3] is not None)
+        desc = (f"{n_units} (sequence, kv head) unit(s) of the {self.spec.name} workload over {W} processes"
+                + (f", {cut} of them a context prefix" if cut else ""))
+        return wall, nbytes, desc
+
+    def close(self):
+        if self._ex is not None:
+            self._ex.shutdown(wait=True)
+            self._ex = None
+        for shm in self._shms:
+            shm.close()
+            shm.unlink()
+        self._shms = []
+
+
+def cpu_baseline(inp, budget_s: float, workers: int = 0):
+    """The oracle timed on one core and on all host cores (os.cpu_count()
+    processes, or `workers`). The all-cores run is the reported value."""
+    per_key = oracle_seconds_per_key(inp)
+    s1, b1, d1 = oracle_sample_run(inp, budget_s, per_key=per_key)
+    W = workers or os.cpu_count() or 1
+    pool = OraclePool(inp, W)
+    try:
+        wall, bw, dw = pool.run(budget_s, per_key)
+    finally:
+        pool.close()
+    return {"value": bw / wall / 1e9, "unit": UNIT, "cores": W, "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": dw, "seconds": wall,
+            "one_core": {"value": b1 / s1 / 1e9, "unit": UNIT, "cores": 1, "sample": d1, "seconds": s1},
+            "threads_per_process": 1}
 
 
 # --------------------------------------------------------------------------- arms
@@ -389,20 +523,26 @@ def run_ours(args, world, rank, local):
     elapsed_ms = t0.elapsed_time(t1)
     assert pb.device_error() == 0
 
-    # ---- the split kernel alone: CUDA events around its launch (eager calls)
-    kcalls = max(1, min(args.steps, args.kernel_steps))
+    # ---- the split kernel alone: CUDA events around its launch (eager calls),
+    # at least --kernel-steps calls whatever --steps is, clocks sampled
+    # across them as well
+    kcalls = max(1, args.kernel_steps)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kcalls)]
     for a, b in ev:  # torch creates the CUDA event handles on first record
         a.record(stream)
         b.record(stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
+    kclocks = ClockSampler(local)
+    kclocks.start()
     e0.record(stream)
     for i in range(kcalls):
         pb.arm_profile_events(ev[i][0], ev[i][1])
         step(i)
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    kclocks.stop()
+    assert pb.device_error() == 0
     split_ms = [a.elapsed_time(b) for a, b in ev]
     eager_ms_per_call = e0.elapsed_time(e1) / kcalls
 
@@ -410,8 +550,9 @@ def run_ours(args, world, rank, local):
     ms_per_step = max_ms / args.steps
     value = aggregate_throughput(nbytes, args.steps, max_ms / 1e3, world)
     split_mean_ms = sum(split_ms) / len(split_ms)
+    split_median_ms = statistics.median(split_ms)
     peak, peak_src = load_peak()
-    achieved = nbytes / (split_mean_ms / 1e3) / 1e9
+    achieved = nbytes / (split_median_ms / 1e3) / 1e9
 
     e2e = run_e2e(args, host, dev, pb, nbytes, world)
     serving = run_serving_step(args, host, dev, pb, nbytes, world)
@@ -431,22 +572,21 @@ def run_ours(args, world, rank, local):
         },
         "us_per_call": ms_per_step * 1e3,
         "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
-        "kernels_us": {"split": split_mean_ms * 1e3, "reduce_and_gaps": (ms_per_step - split_mean_ms) * 1e3,
+        "kernels_us": {"split": split_median_ms * 1e3, "split_mean": split_mean_ms * 1e3,
+                       "split_calls": kcalls, "reduce_and_gaps": (ms_per_step - split_median_ms) * 1e3,
                        "eager_call": eager_ms_per_call * 1e3},
-        "timing": "CUDA-graph replays (one graph per input set, alternated); split kernel from CUDA events "
-                  "around its launch in a separate eager pass",
+        "timing": "CUDA-graph replays (one graph per input set, alternated); split kernel: median of CUDA-event "
+                  f"durations around its launch over {kcalls} eager calls (input sets alternated)",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": load_traffic(args.config), "peak_source": peak_src,
                      "kernel": "pa_split_kernel"},
-        "clocks": clocks.summary(),
+        "clocks": merge_clocks(clocks.summary(), kclocks.summary()),
         "e2e": e2e,
         "e2e_serving_step": serving,
         "gpu_launches": 2 * args.steps if (args.num_splits != 1) else args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs, b, desc = oracle_sample_run(host, args.cpu_budget)
-        result["cpu_baseline"] = {"value": b / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                  "sample": desc, "seconds": secs}
+        result["cpu_baseline"] = cpu_baseline(host, args.cpu_budget, args.cpu_workers)
     return result
 
 
@@ -526,15 +666,19 @@ def run_append(args, world, rank, local):
     max_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_per_step = max_ms / args.steps
 
-    # the append kernel alone: CUDA events around eager calls (one launch each)
-    kcalls = max(1, min(args.steps, args.kernel_steps))
+    # the append kernel alone: CUDA events around eager calls (one launch
+    # each), at least --kernel-steps of them, clocks sampled across them
+    kcalls = max(1, args.kernel_steps)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kcalls)]
     torch.cuda.synchronize(dev)
+    kclocks = ClockSampler(local)
+    kclocks.start()
     for i in range(kcalls):
         ev[i][0].record(stream)
         call(sets[i & 1], stream)
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    kclocks.stop()
     kern_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
     peak, peak_src = load_peak()
     achieved = nbytes / (kern_ms / 1e3) / 1e9
@@ -570,12 +714,12 @@ def run_append(args, world, rank, local):
         },
         "us_per_call": ms_per_step * 1e3,
         "frac_of_8tbs": aggregate_throughput(nbytes, args.steps, max_ms / 1e3, world) / world / NOMINAL_HBM_GBS,
-        "kernels_us": {"append": kern_ms * 1e3},
+        "kernels_us": {"append": kern_ms * 1e3, "append_calls": kcalls},
         "timing": "CUDA-graph replays (one graph per input set, alternated); the append kernel from CUDA "
                   "events around eager calls",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": load_traffic(args.config), "peak_source": peak_src, "kernel": "pa_kv_append_kernel"},
-        "clocks": clocks.summary(),
+        "clocks": merge_clocks(clocks.summary(), kclocks.summary()),
         "e2e": {"value": nbytes * world / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": 0, "steps": k, "ms_per_step": e2e_ms,
                 "note": "the appended rows stay in the device cache; nothing is read back"},
@@ -583,8 +727,9 @@ def run_append(args, world, rank, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, nb, desc = append_oracle_run(host, args.cpu_budget)
-        result["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                  "sample": desc, "seconds": secs}
+        result["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": UNIT, "cores": 1, "nproc": os.cpu_count(),
+                                  "kind": "oracle", "sample": desc, "seconds": secs,
+                                  "note": "one core: the append oracle is timed single-threaded"}
     return result
 
 
@@ -735,23 +880,26 @@ def run_reference(args):
     host = gen.make_inputs(spec)
     budget = max(0.002, args.reference_seconds / (args.steps + args.warmup))
     per_key = oracle_seconds_per_key(host)
-    for w in range(args.warmup):
-        oracle_sample_run(host, budget, start_unit=w, per_key=per_key)
-    secs, nbytes, desc = 0.0, 0, None
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        s, b, d = oracle_sample_run(host, budget, start_unit=args.warmup + i, per_key=per_key)
-        secs += s
-        nbytes += b
-        desc = desc or d
-    wall = time.perf_counter() - t0
+    W = args.cpu_workers or os.cpu_count() or 1
+    pool = OraclePool(host, W)
+    try:
+        for w in range(args.warmup):
+            pool.run(budget, per_key, start_unit=w)
+        secs, nbytes, desc = 0.0, 0, None
+        for i in range(args.steps):
+            s, b, d = pool.run(budget, per_key, start_unit=args.warmup + i)
+            secs += s
+            nbytes += b
+            desc = desc or d
+    finally:
+        pool.close()
     value = nbytes / secs / 1e9
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": WORKLOADS[args.config], "num_splits": args.num_splits},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"per step: {desc}"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": W, "nproc": os.cpu_count(), "kind": "oracle",
+                             "threads_per_process": 1, "sample": f"per step: {desc}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -766,7 +914,9 @@ def main(argv=None):
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--kernel-steps", type=int, default=200, help="eager calls timed for the split kernel alone")
+    ap.add_argument("--kernel-steps", type=int, default=300,
+                    help="eager calls timed for the dominant kernel alone (independent of --steps)")
+    ap.add_argument("--cpu-workers", type=int, default=0, help="oracle processes for the all-cores run (0: all)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -45,8 +45,10 @@
  *    (out, lse and the workspace are untouched). PA_ERR_CUDA reports a
  *    launch failure (cudaGetLastError). Nothing aborts or throws across the
  *    ABI. A device-side wait that runs out of time (a bug, never expected)
- *    makes the kernel stop early and set a flag read by
- *    pa_decode_device_error().
+ *    makes the kernel stop early: every query row whose work was cut short
+ *    gets NaN in out and lse (also through the split-K combine), so no part
+ *    of an aborted call can pass as a result, and a flag is set that
+ *    pa_decode_device_error() reads.
  *
  * Supported: D in {64, 128, 256} (fp8: {128, 256}); P in {16, 32, 64, 128,
  * 256}; M = G * T <= 64 query rows per kv head (more than 32 rows: D in {64,
@@ -102,8 +104,11 @@ typedef struct pa_shape {
 } pa_shape;
 
 /* Bytes of workspace pa_decode* needs for this shape and num_splits (0 for
- * num_splits == 1). For num_splits == 0 the size depends on the current
- * device's SM count. Returns 0 as well for an invalid shape. */
+ * num_splits == 1). For num_splits == 0 the size is the largest over every
+ * decode entry point (bf16, f16, fp8, draft block) and depends on the
+ * current device's SM count: size it on the device that will run the call
+ * (another GPU model may need more and would return PA_ERR_WORKSPACE).
+ * Returns 0 as well for an invalid shape. */
 size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits);
 
 /* What num_splits == 0 resolves to on the current device, for this shape and
@@ -182,9 +187,17 @@ pa_status pa_decode_tidar_masked(const void* q, const void* k_cache, const void*
  * part_out float [B][T][Hq][num_splits][D], part_lse float [B][T][Hq][num_splits]
  * (the layout pa_decode writes for num_splits > 1). out bf16 [B][T][Hq][D];
  * lse may be NULL. num_splits >= 1. Only batch, q_tokens, num_q_heads and
- * head_dim of shape are used (head_dim a multiple of 4, <= 1024). */
+ * head_dim of shape are used (head_dim a multiple of 4, <= 1024). A split
+ * whose lse is NaN makes its row NaN. */
 pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t num_splits,
                            const pa_shape* shape, void* out, float* lse, pa_stream_t stream);
+
+/* pa_decode_reduce with out in IEEE binary16: the combine for callers of
+ * pa_decode_f16 that run explicit splits and combine the partials
+ * themselves (the MSLK page's dense path is f16 or bf16). Arguments, layouts
+ * and errors as pa_decode_reduce. */
+pa_status pa_decode_reduce_f16(const float* part_out, const float* part_lse, int32_t num_splits,
+                               const pa_shape* shape, void* out, float* lse, pa_stream_t stream);
 
 /* KV-cache append, the step before a decode: writes the T = shape->q_tokens
  * new tokens of every sequence into its pages (the ROCm blog's paged cache,
@@ -228,8 +241,11 @@ pa_status pa_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* 
  * keeps the split-K partials in a fixed scratch array that the library
  * reserves statically on every GPU that loads it (held until the process
  * exits): PA_NOALLOC_SCRATCH_BYTES bytes. It allocates nothing.
- *  - Calls whose partials need more than that (pa_decode_workspace_size()
- *    above the limit) return PA_ERR_WORKSPACE before any launch.
+ *  - The limit applies to the partials pa_decode itself uses for this shape
+ *    and num_splits on this device. pa_decode_workspace_size(shape, S) is
+ *    that size for S >= 1; for S = 0 it is the largest over every decode
+ *    format, so it may exceed what this bf16 call needs. Calls over the
+ *    limit return PA_ERR_WORKSPACE before any launch.
  *  - The first call on a device looks up the scratch array's device address
  *    (once per device, with that device current); make that first call
  *    before any stream capture.

@@ -55,6 +55,7 @@ _SIGNATURES = {
     "pa_decode_tidar_masked": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float,
                                               ctypes.c_int32, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "pa_decode_reduce": (ctypes.c_int, [_P, _P, ctypes.c_int32, ctypes.POINTER(PaShape), _P, _P, _P]),
+    "pa_decode_reduce_f16": (ctypes.c_int, [_P, _P, ctypes.c_int32, ctypes.POINTER(PaShape), _P, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_kv_append": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PaShape), _P, _P, _P]),
     "pa_kv_append_fp8": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
@@ -247,18 +248,22 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
 
 
 def decode_reduce(part_out: torch.Tensor, part_lse: torch.Tensor, *, out: Optional[torch.Tensor] = None,
-                  lse: Optional[torch.Tensor] = None, stream=None):
-    """pa_decode_reduce: combine part_out [B,T,Hq,S,D] by part_lse [B,T,Hq,S]."""
+                  lse: Optional[torch.Tensor] = None, stream=None, out_dtype=torch.bfloat16):
+    """pa_decode_reduce (bf16 out) or pa_decode_reduce_f16 (out_dtype
+    torch.float16): combine part_out [B,T,Hq,S,D] by part_lse [B,T,Hq,S]."""
     _need_contig(part_out=part_out, part_lse=part_lse)
     B, T, Hq, S, D = part_out.shape
     shape = PaShape(B, T, Hq, 1, D, 16, 1, 1)
     if out is None:
-        out = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=part_out.device)
+        out = torch.empty((B, T, Hq, D), dtype=out_dtype, device=part_out.device)
     if lse is None:
         lse = torch.empty((B, T, Hq), dtype=torch.float32, device=part_out.device)
-    st = lib().pa_decode_reduce(_ptr(part_out), _ptr(part_lse), S, ctypes.byref(shape), _ptr(out), _ptr(lse),
-                                _stream(stream))
-    _check(st, "pa_decode_reduce")
+    if out.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("out must be bf16 or f16")
+    name = "pa_decode_reduce_f16" if out.dtype == torch.float16 else "pa_decode_reduce"
+    st = getattr(lib(), name)(_ptr(part_out), _ptr(part_lse), S, ctypes.byref(shape), _ptr(out), _ptr(lse),
+                              _stream(stream))
+    _check(st, name)
     return out, lse
 
 

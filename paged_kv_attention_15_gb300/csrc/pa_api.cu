@@ -493,9 +493,10 @@ size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits) {
   DeviceState* d = nullptr;
   if (device_state(&d) != PA_OK) return 0;
   // The balanced plan depends on the kind through the instance's fixed
-  // shared memory and the draft block's extra page; take the largest plan.
+  // shared memory and the draft block's extra page; take the largest plan
+  // over every decode entry point.
   size_t best = 0;
-  for (Kind kind : {Kind::kBf16, Kind::kFp8, Kind::kTidar}) {
+  for (Kind kind : {Kind::kBf16, Kind::kF16, Kind::kFp8, Kind::kTidar}) {
     if (check_shape(shape, kind) != PA_OK) continue;
     Plan plan;
     if (make_plan(shape, kind, 0, d, &plan) == PA_OK && plan.ws_bytes > best) best = plan.ws_bytes;
@@ -559,8 +560,12 @@ pa_status pa_decode_tidar_masked(const void* q, const void* k_cache, const void*
   return run_decode(a);
 }
 
-pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t num_splits, const pa_shape* shape,
-                           void* out, float* lse, pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+pa_status run_reduce(const float* part_out, const float* part_lse, int32_t num_splits, const pa_shape* shape,
+                     void* out, float* lse, pa_stream_t stream, bool out_f16) {
   if (!shape || !part_out || !part_lse || !out || num_splits < 1) return PA_ERR_INVALID_ARG;
   if (shape->batch < 0 || shape->q_tokens < 1 || shape->num_q_heads < 1 || shape->head_dim < 4 ||
       shape->head_dim % 4 || shape->head_dim > 1024)
@@ -579,12 +584,27 @@ pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t
   r.Hq = shape->num_q_heads;
   r.D = shape->head_dim;
   r.num_splits = num_splits;
+  r.out_f16 = out_f16 ? 1 : 0;
   const size_t rows = (size_t)r.B * r.T * r.Hq;
   void* rargs[] = {&r};
   if (cudaLaunchKernel(reinterpret_cast<const void*>(&pa::pa_reduce_splits_kernel), dim3((unsigned)((rows + 3) / 4)),
                        dim3(128), rargs, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode_reduce(const float* part_out, const float* part_lse, int32_t num_splits, const pa_shape* shape,
+                           void* out, float* lse, pa_stream_t stream) {
+  return run_reduce(part_out, part_lse, num_splits, shape, out, lse, stream, false);
+}
+
+pa_status pa_decode_reduce_f16(const float* part_out, const float* part_lse, int32_t num_splits,
+                               const pa_shape* shape, void* out, float* lse, pa_stream_t stream) {
+  return run_reduce(part_out, part_lse, num_splits, shape, out, lse, stream, true);
 }
 
 const char* pa_status_string(pa_status status) {

@@ -860,8 +860,16 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
       acc[i][2] = a2 * inv1;
       acc[i][3] = a3 * inv1;
     }
-    const float lse0 = L0 > 0.f ? (M0 + lg2(L0)) * kLn2 : NEG_INF;
-    const float lse1 = L1 > 0.f ? (M1 + lg2(L1)) * kLn2 : NEG_INF;
+    float lse0 = L0 > 0.f ? (M0 + lg2(L0)) * kLn2 : NEG_INF;
+    float lse1 = L1 > 0.f ? (M1 + lg2(L1)) * kLn2 : NEG_INF;
+    // An item cut short by a timed-out wait (in this warp or another role of
+    // the CTA) is written as NaN, so that no part of it passes as a result.
+    if (__any_sync(0xffffffffu, !ok || *s_abort)) {
+      const float NaN = __int_as_float(0x7fffffff);
+#pragma unroll
+      for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = NaN;
+      lse0 = lse1 = NaN;
+    }
 
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {

@@ -13,12 +13,13 @@ namespace pa {
 // w_k = exp(lse_k - M), out = sum_k w_k o_k / sum_k w_k, lse = M + ln sum_k w_k,
 // in one online pass (running max, sums rescaled when it grows) that keeps
 // the loads of eight pieces in flight. Pieces with lse = -inf weigh 0; a row
-// whose pieces are all empty gets out = 0, lse = -inf. o_row(k) points at
-// piece k's D (<= 256) floats in global memory, read past L1 (other CTAs of
-// the same grid may have written them); l_val(k) is its lse. Lane l owns
-// columns 4l..4l+3 and 128+4l..128+4l+3. Source: the MSLK pull request
-// "[ROCm] Add FlyDSL paged-attention decode backend (dense + fp8) with
-// benchmark" (Kernels: pa_decode_reduce, the split-K combine).
+// whose pieces are all empty gets out = 0, lse = -inf; a piece whose lse is
+// NaN (its work was cut short by a timed-out wait) makes the row NaN.
+// o_row(k) points at piece k's D (<= 256) floats in global memory, read
+// past L1 (other CTAs of the same grid may have written them); l_val(k) is
+// its lse. Lane l owns columns 4l..4l+3 and 128+4l..128+4l+3. Source: the
+// MSLK pull request "[ROCm] Add FlyDSL paged-attention decode backend (dense
+// + fp8) with benchmark" (Kernels: pa_decode_reduce, the split-K combine).
 template <typename ORow, typename LVal>
 __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_val, __nv_bfloat16* out,
                                             float* lse_out, int lane, bool out_f16) {
@@ -28,6 +29,7 @@ __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_va
   const int c0 = lane * 4, c1 = 128 + lane * 4;
   const bool h0 = c0 < D, h1 = c1 < D;
   float m = NEG_INF, L = 0.f;
+  bool poisoned = false;
   float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
   for (int k0 = 0; k0 < np; k0 += 8) {
     float lk[8];
@@ -36,6 +38,7 @@ __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_va
     for (int j = 0; j < 8; ++j) {
       const bool in = k0 + j < np;
       lk[j] = in ? l_val(k0 + j) : NEG_INF;
+      poisoned |= lk[j] != lk[j];
       const float* o = in ? o_row(k0 + j) : nullptr;
       v0[j] = in && h0 ? __ldcg(reinterpret_cast<const float4*>(o + c0)) : make_float4(0.f, 0.f, 0.f, 0.f);
       v1[j] = in && h1 ? __ldcg(reinterpret_cast<const float4*>(o + c1)) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -57,14 +60,26 @@ __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_va
     }
     m = mc;
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float NaN = __int_as_float(0x7fffffff);
+  const float inv = poisoned ? NaN : (L > 0.f ? 1.f / L : 0.f);
   if (h0)
     *reinterpret_cast<uint2*>(out + c0) =
         make_uint2(pack(a0.x * inv, a0.y * inv), pack(a0.z * inv, a0.w * inv));
   if (h1)
     *reinterpret_cast<uint2*>(out + c1) =
         make_uint2(pack(a1.x * inv, a1.y * inv), pack(a1.z * inv, a1.w * inv));
-  if (lane == 0 && lse_out) *lse_out = L > 0.f ? m + lg2(L) * kLn2 : NEG_INF;
+  if (lane == 0 && lse_out) *lse_out = poisoned ? NaN : (L > 0.f ? m + lg2(L) * kLn2 : NEG_INF);
+}
+
+// combine_row over a row of any D (a multiple of 4): 256 columns at a time
+// (the weights are recomputed per chunk; they are the same every time).
+template <typename ORow, typename LVal>
+__device__ __forceinline__ void combine_row_any(int np, int D, ORow o_row, LVal l_val, __nv_bfloat16* out,
+                                                float* lse_out, int lane, bool out_f16) {
+  for (int c = 0; c < D; c += 256)
+    combine_row(
+        np, D - c < 256 ? D - c : 256, [&](int k) { return o_row(k) + c; }, l_val, out + c,
+        c == 0 ? lse_out : nullptr, lane, out_f16);
 }
 
 
@@ -79,7 +94,7 @@ __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_cons
   const float* po = p.part_o + base * p.D;
   const float* pl = p.part_lse + base;
   const int D = p.D;
-  combine_row(
+  combine_row_any(
       p.num_splits, D, [&](int k) { return po + (size_t)k * D; }, [&](int k) { return __ldcg(pl + k); },
       p.out + row * D, p.lse ? p.lse + row : nullptr, lane, p.out_f16 != 0);
 }

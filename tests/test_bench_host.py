@@ -49,7 +49,8 @@ def test_reference_arm_prints_the_contract_line():
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["metric"] == bench.METRIC and line["steps"] == 2 and line["warmup"] == 3
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["nproc"] >= 1 and line["cpu_baseline"]["threads_per_process"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
 
 
@@ -90,3 +91,21 @@ def test_append_bytes_by_hand():
     fp8 = gen.make_append_inputs(gen.AppendSpec("t", batch=2, new_tokens=20, num_kv_heads=2, head_dim=128,
                                                 page_size=16, context_lens=(5, 30), kv_format="fp8", seed=3))
     assert bench.append_bytes(fp8) == rows * (2 * 128 + 128 + 4) + pages * 4 + 2 * 4
+
+
+def test_all_cores_oracle_pool_covers_every_unit_once():
+    """The all-cores CPU baseline: two spawned processes share the workload
+    through shared memory and split its units; with a large budget they do
+    every unit exactly once, so their bytes equal the one-core run's."""
+    spec = gen.custom_spec(batch=3, q_tokens=1, num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=16,
+                           context_lens=(37, 100, 5), seed=2)
+    inp = gen.make_inputs(spec)
+    per_key = bench.oracle_seconds_per_key(inp)
+    s1, b1, _ = bench.oracle_sample_run(inp, 60.0, per_key=per_key)
+    pool = bench.OraclePool(inp, 2)
+    try:
+        wall, b2, desc = pool.run(60.0, per_key)
+    finally:
+        pool.close()
+    assert b2 == b1 == sum(bench.unit_bytes(spec, c) for c in (37, 100, 5) for _ in range(2))
+    assert wall > 0 and "6 (sequence, kv head) unit(s)" in desc and "2 processes" in desc

@@ -331,6 +331,44 @@ def test_reduce_entry_point_against_oracle_combine():
     assert_match(o, l, ref_o, ref_l, 1e-2)
 
 
+@pytest.mark.parametrize("D", [64, 256, 320, 1024])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+def test_reduce_entry_point_head_dims_and_f16(D, out_dtype):
+    """The standalone combine for head dims up to 1024 (rows wider than one
+    warp's 256 columns are combined in chunks), with bf16 or f16 out."""
+    rng = np.random.default_rng(D)
+    B, T, Hq, S = 2, 1, 3, 5
+    po = rng.standard_normal((B, T, Hq, S, D)).astype(np.float32)
+    pl = (rng.standard_normal((B, T, Hq, S)) * 3).astype(np.float32)
+    pl[1, 0, 1, 1:] = -np.inf
+    ref_o, ref_l = oracle.combine(po.astype(np.float64), pl.astype(np.float64))
+    out = torch.full((B, T, Hq, D), 5.0, dtype=out_dtype, device="cuda")
+    out, lse = pb.decode_reduce(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda(), out=out)
+    torch.cuda.synchronize()
+    assert out.dtype == out_dtype
+    assert_match(*to_np(out, lse), ref_o, ref_l, 1e-2)
+
+
+def test_reduce_propagates_a_nan_split():
+    """A split whose lse is NaN (work cut short) makes its row NaN; the other
+    rows are unaffected."""
+    rng = np.random.default_rng(3)
+    B, T, Hq, S, D = 2, 1, 2, 4, 128
+    po = rng.standard_normal((B, T, Hq, S, D)).astype(np.float32)
+    pl = rng.standard_normal((B, T, Hq, S)).astype(np.float32)
+    pl[0, 0, 1, 2] = np.nan
+    po[0, 0, 1, 2] = np.nan
+    out, lse = pb.decode_reduce(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda())
+    torch.cuda.synchronize()
+    o, l = to_np(out, lse)
+    assert np.all(np.isnan(o[0, 0, 1])) and np.isnan(l[0, 0, 1])
+    mask = np.ones((B, T, Hq), dtype=bool)
+    mask[0, 0, 1] = False
+    ref_o, ref_l = oracle.combine(po.astype(np.float64), pl.astype(np.float64))
+    assert np.all(np.abs(o[mask] - ref_o[mask]) <= 1e-2 + 1e-2 * np.abs(ref_o[mask]))
+    assert np.all(np.abs(l[mask] - ref_l[mask]) <= LSE_TOL)
+
+
 def test_split_counts_beyond_pages_and_single_page():
     inp = gen.make_inputs(spec(context_lens=(16, 1, 17, 40)))
     for S in (1, 2, 3, 4, 9, 100):
@@ -376,14 +414,20 @@ def sample_rows(inp, n, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["gqa", "long", "fp8", "tidar", "tidar_causal", "tidar_long", "gqa_f16", "gqa_d64",
-                                  "gqa_d256"])
-def test_full_size_workload_sampled(name):
+# The five workloads of the problem statement are compared on every output
+# row (the oracle takes a few seconds each); the extension workloads on
+# sampled rows.
+FULL_ROWS = ("tiny", "gqa", "long", "fp8", "tidar")
+
+
+@pytest.mark.parametrize("name", ["tiny", "gqa", "long", "fp8", "tidar", "tidar_causal", "tidar_long", "gqa_f16",
+                                  "gqa_d64", "gqa_d256"])
+def test_full_size_workload(name):
     inp = gen.make_inputs(gen.SPECS[name])
     out, lse = gpu_decode(inp, 0)
     out_np, lse_np = to_np(out, lse)
     assert np.all(np.isfinite(out_np)) and np.all(np.isfinite(lse_np))
-    rows = sample_rows(inp, 48, seed=len(name))
+    rows = None if name in FULL_ROWS else sample_rows(inp, 48, seed=len(name))
     ref_out, ref_lse = oracle.decode(ora_inputs(inp), inp.scale, rows=rows)
     assert_match(out_np, lse_np, ref_out, ref_lse, tol_of(inp.spec), rows=rows)
     # Explicit splits agree with the balanced launch at full size as well.

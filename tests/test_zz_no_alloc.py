@@ -54,8 +54,19 @@ def test_noalloc_matches_pa_decode_on_consecutive_calls(num_splits):
 def test_noalloc_rejects_partials_beyond_the_static_scratch():
     torch.cuda.set_device(0)
     # 64 sequences x 32 heads x 1024 splits x 129 floats: far above the limit.
-    shape = pb.PaShape(64, 1, 32, 8, 128, 16, 1024, 1024)
+    # Real buffers of the declared shape (zero lengths, valid page ids), so
+    # that even a call that wrongly went ahead would only compute.
+    B, T, Hq, Hkv, D, P, pages = 64, 1, 32, 8, 128, 16, 1024
+    shape = pb.PaShape(B, T, Hq, Hkv, D, P, pages, pages)
     assert pb.workspace_size(shape, 1024) > (8 << 20)
-    fake = 1 << 20
-    st = pb.lib().pa_decode_noalloc(fake, fake, fake, fake, fake, ctypes.byref(shape), 0.1, fake, None, 1024, None)
+    q = torch.zeros(B, T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(pages, P, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    bt = torch.zeros(B, pages, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(B, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, 7.0)
+    st = pb.lib().pa_decode_noalloc(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), lens.data_ptr(),
+                                    ctypes.byref(shape), 0.1, out.data_ptr(), None, 1024, None)
     assert st == pb.PA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()), "a rejected call must leave out untouched"
