@@ -78,6 +78,8 @@ WORKLOADS = {
 APPEND_CONFIGS = ("append", "append_fp8", "append_step")
 APPEND_METRIC = "KV-cache append µs/call and achieved HBM GB/s (fraction of 8 TB/s) on 1 GB300"
 SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh"]
+UMMA_KERNEL_SOURCES = ["pa_umma.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
+KERNEL_NAMES = {1: "pa_split_kernel", 2: "pa_umma_kernel"}
 APPEND_KERNEL_SOURCES = ["pa_append.cu", "pa_ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -139,22 +141,25 @@ def load_peak():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-def kernel_sha(config: str = DEFAULT_CONFIG) -> str:
+def kernel_sha(config: str = DEFAULT_CONFIG, kernel: str = "pa_split_kernel") -> str:
     """Hash of the sources of the kernel a workload's roofline is about."""
     h = hashlib.sha256()
-    for name in (APPEND_KERNEL_SOURCES if config in APPEND_CONFIGS else SPLIT_KERNEL_SOURCES):
+    srcs = APPEND_KERNEL_SOURCES if config in APPEND_CONFIGS else (
+        UMMA_KERNEL_SOURCES if kernel == "pa_umma_kernel" else SPLIT_KERNEL_SOURCES)
+    for name in srcs:
         with open(os.path.join(ROOT, "paged_kv_attention_15_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic(config: str):
+def load_traffic(config: str, kernel: str = "pa_split_kernel"):
     """DRAM bytes per launch of the workload's kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+    summary, if it was taken on the current source of that kernel; else
+    None."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f).get(config)
-        if rec and rec.get("kernel_sha") == kernel_sha(config):
+        if rec and rec.get("kernel", "pa_split_kernel") == kernel and rec.get("kernel_sha") == kernel_sha(config, kernel):
             return int(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -470,7 +475,9 @@ def run_ours(args, world, rank, local):
     spec = workload_spec(args)
     host = gen.make_inputs(spec)
     pb.lib()
+    pb.set_kernel_path({"auto": pb.KERNEL_AUTO, "warp": pb.KERNEL_WARP_MMA, "tcgen05": pb.KERNEL_TCGEN05}[args.kernel_path])
     sets = [host.to(dev), host.to(dev)]  # alternated: each step reads KV not in L2
+    kname = KERNEL_NAMES[pb.kernel_for_inputs(sets[0])]
     shape = pb.make_shape(sets[0].q, sets[0].k_cache, sets[0].block_tables)
     ws_bytes = pb.workspace_size(shape, args.num_splits)
     wss = [torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) for _ in sets]
@@ -566,6 +573,7 @@ def run_ours(args, world, rank, local):
             "batch": spec.batch, "q_tokens": spec.q_tokens,
             "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
             "page_size": spec.page_size, "num_splits": args.num_splits, "seed": spec.seed,
+            "split_kernel": kname, "kernel_path": args.kernel_path,
             "algorithmic_bytes_per_step": nbytes,
             "l2": f"inputs larger than L2: two device copies of {nbytes / 1e6:.0f} MB alternated",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -578,8 +586,8 @@ def run_ours(args, world, rank, local):
         "timing": "CUDA-graph replays (one graph per input set, alternated); split kernel: median of CUDA-event "
                   f"durations around its launch over {kcalls} eager calls (input sets alternated)",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": load_traffic(args.config), "peak_source": peak_src,
-                     "kernel": "pa_split_kernel"},
+                     "frac": achieved / peak, "traffic": load_traffic(args.config, kname), "peak_source": peak_src,
+                     "kernel": kname},
         "clocks": merge_clocks(clocks.summary(), kclocks.summary()),
         "e2e": e2e,
         "e2e_serving_step": serving,
@@ -917,6 +925,8 @@ def main(argv=None):
     ap.add_argument("--kernel-steps", type=int, default=300,
                     help="eager calls timed for the dominant kernel alone (independent of --steps)")
     ap.add_argument("--cpu-workers", type=int, default=0, help="oracle processes for the all-cores run (0: all)")
+    ap.add_argument("--kernel-path", default="auto", choices=["auto", "warp", "tcgen05"],
+                    help="split kernel: automatic choice, the warp-level MMA kernel, or the tcgen05 kernel")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

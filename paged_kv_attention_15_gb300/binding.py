@@ -61,6 +61,8 @@ _SIGNATURES = {
     "pa_kv_append_fp8": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(PaShape), _P, _P, _P, _P, _P]),
     "pa_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32)]),
     "pa_decode_profile_events": (ctypes.c_int, [_P, _P]),
+    "pa_decode_set_kernel_path": (ctypes.c_int, [ctypes.c_int32]),
+    "pa_decode_kernel_for": (ctypes.c_int32, [ctypes.POINTER(PaShape), ctypes.c_int32]),
     "pa_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float, _P, _P,
                                          ctypes.c_int32, _P]),
 }
@@ -279,3 +281,26 @@ def device_error() -> int:
     v = ctypes.c_int32(0)
     _check(lib().pa_decode_device_error(ctypes.byref(v)), "pa_decode_device_error")
     return int(v.value)
+
+
+KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05 = 0, 1, 2
+_FORMATS = {"bf16": 0, "fp8": 1, "f16": 2, "draft": 3}
+
+
+def set_kernel_path(path: int) -> None:
+    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_WARP_MMA or KERNEL_TCGEN05
+    (see pa_decode_set_kernel_path)."""
+    _check(lib().pa_decode_set_kernel_path(int(path)), "pa_decode_set_kernel_path")
+
+
+def kernel_for(shape: PaShape, fmt: str) -> int:
+    """1 (warp-level MMA kernel) or 2 (tcgen05 kernel) for a decode of this
+    shape and format ('bf16', 'fp8', 'f16', 'draft'); -1 if unsupported."""
+    return int(lib().pa_decode_kernel_for(ctypes.byref(shape), _FORMATS[fmt]))
+
+
+def kernel_for_inputs(inp) -> int:
+    """kernel_for() of a DecodeInputs bundle."""
+    s = inp.spec
+    fmt = "draft" if s.draft_scratch else s.kv_format
+    return kernel_for(make_shape(inp.q, inp.k_cache, inp.block_tables), fmt)

@@ -155,10 +155,16 @@ SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL, int CW) {
 
 // Work-unit geometry: H2 kv heads per CTA unit, their M = H2 * G * T query
 // rows in MT m16 tiles, TS = 64 / H2 tokens per stage, TSL tokens per warp.
+// tcgen05 kernel (umma): M = N rows, TS = 128 / H2 tokens per stage.
 struct Geom {
   int GT, H2, NHG, M, MT, TS, TSL, BR, lbr, TP, ilv;
+  bool umma;
   SplitKernel k;
 };
+
+// Which decode kernel a call may use: 0 automatic, 1 the warp-level MMA
+// kernel only, 2 the tcgen05 kernel wherever an instance exists.
+std::atomic<int> g_kernel_path{0};
 
 int ilog2(int x) {
   int l = 0;
@@ -212,6 +218,7 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   g->H2 = H2;
   g->NHG = s->num_kv_heads / H2;
   g->M = M;
+  g->umma = false;
   g->MT = MT;
   g->TS = TS;
   g->TSL = TSL;
@@ -222,10 +229,52 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   return true;
 }
 
+// tcgen05 kernel geometry: G * T query rows per kv head (16 or 32), the
+// most kv heads per unit (up to 4) whose N = H2 * G * T rows have an
+// instance; a stage holds TS = 128 / H2 tokens of each head.
+bool geom_umma(const pa_shape* s, Kind kind, Geom* g) {
+  const int G = s->num_q_heads / s->num_kv_heads, T = s->q_tokens, P = s->page_size, D = s->head_dim;
+  const int GT = G * T;
+  if (GT != 16 && GT != 32) return false;
+  for (int H2 = 4; H2 >= 1; H2 /= 2) {
+    const int N = H2 * GT;
+    if (s->num_kv_heads % H2 || N > 64) continue;
+    const int TS = 128 / H2, TP = (T + 7) / 8 * 8;
+    if (kind == Kind::kTidar && TP > TS) continue;
+    const SplitKernel k = kind == Kind::kFp8 ? pa::umma_kernel_fp8(D, GT, N)
+                                             : pa::umma_kernel_16(D, kind == Kind::kF16, GT, N);
+    if (!k.fn) continue;
+    g->GT = GT;
+    g->H2 = H2;
+    g->NHG = s->num_kv_heads / H2;
+    g->M = N;
+    g->MT = 0;
+    g->TS = TS;
+    g->TSL = 0;
+    g->BR = P < TS ? P : TS;
+    g->lbr = ilog2(g->BR);
+    g->TP = TP;
+    g->ilv = 1;
+    g->umma = true;
+    g->k = k;
+    return true;
+  }
+  return false;
+}
+
+// Automatic choice: the warp-level kernel (measured faster on every
+// workload so far); the tcgen05 kernel on request.
+bool want_umma(const pa_shape* s, Kind kind) {
+  (void)s;
+  (void)kind;
+  return g_kernel_path.load(std::memory_order_relaxed) == 2;
+}
+
 // One kv head per unit, or more while a page's box stays under 16 KB: a
 // 16-row page of one head is a 4 KB copy, too small to keep enough bytes in
 // flight per SM.
 pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out) {
+  if (want_umma(s, kind) && geom_umma(s, kind, out)) return PA_OK;
   Geom best;
   if (!geom_for(s, kind, 1, &best)) return PA_ERR_UNSUPPORTED;
   const int e = kind == Kind::kFp8 ? 1 : 2;
@@ -664,6 +713,21 @@ pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
   if (need > 0 && (st = noalloc_scratch(&ws)) != PA_OK) return st;
   return pa_decode(q, k_cache, v_cache, block_tables, context_lens, shape, scale, out, lse, num_splits, ws, need,
                    stream);
+}
+
+pa_status pa_decode_set_kernel_path(int32_t path) {
+  if (path < 0 || path > 2) return PA_ERR_INVALID_ARG;
+  g_kernel_path.store(path, std::memory_order_relaxed);
+  return PA_OK;
+}
+
+int32_t pa_decode_kernel_for(const pa_shape* shape, int32_t format) {
+  if (format < 0 || format > 3) return -1;
+  const Kind kind = format == 1 ? Kind::kFp8 : format == 2 ? Kind::kF16 : format == 3 ? Kind::kTidar : Kind::kBf16;
+  if (check_shape(shape, kind) != PA_OK) return -1;
+  Geom g;
+  if (pick_geometry(shape, kind, &g) != PA_OK) return -1;
+  return g.umma ? 2 : 1;
 }
 
 pa_status pa_decode_profile_events(void* start_event, void* split_done_event) {

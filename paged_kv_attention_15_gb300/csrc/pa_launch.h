@@ -20,4 +20,9 @@ SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice, int consum
 SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice, int consumer_warps);
 SplitKernel split_kernel_f16(int head_dim, int row_tiles, int slice, int consumer_warps);
 
+// Instance of the tcgen05 kernel for (head_dim, query rows per kv head GT,
+// rows per work unit N = kv heads per unit * GT); fn == nullptr if not built.
+SplitKernel umma_kernel_fp8(int head_dim, int GT, int N);
+SplitKernel umma_kernel_16(int head_dim, bool f16, int GT, int N);
+
 }  // namespace pa
