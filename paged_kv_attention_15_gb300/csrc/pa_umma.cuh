@@ -51,8 +51,10 @@ namespace pa {
 constexpr int kUThreads = 512;
 constexpr int kUKConvWarp0 = 4;
 constexpr int kUVConvWarp0 = 8;
-constexpr int kUProducerWarp = 12;
+constexpr int kUProducerWarp = 12;   // K pages, Q, page-id table
 constexpr int kUMmaWarp = 13;
+constexpr int kUVProducerWarp = 14;  // V pages
+constexpr int kUPvWarp = 15;         // issues the P V products
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA
 // Registers per thread after the split (launched with 65536 / 512 = 128):
 // softmax 200, converters 104, producer/MMA warpgroup 96;
@@ -74,8 +76,15 @@ struct UCfg {
   static constexpr int NKP = D / 64;           // K operand pieces per stage (64 columns, 16 KB)
   static constexpr int KPB = 16384;
   static constexpr int NKPS = 2;               // K piece slots
-  static constexpr int NVT = D / 128;          // V operand tiles per stage (128 columns, 32 KB)
-  static constexpr int VTB = 32768;
+  static constexpr int NVT = D / 128;          // 128-column tiles of the V^T operand
+  // V^T operand sub-tile: one 128-column tile of SUBR key rows of one head,
+  // [2 chunks of 64 columns][SUBR rows][128 B]; a ring of two, so the V
+  // converters fill one while the MMAs read the other.
+  static constexpr int SUBR = TSK < 64 ? TSK : 64;
+  static constexpr int NKH = TSK / SUBR;  // sub-tiles per head and tile
+  static constexpr int SUBB = SUBR * 256;
+  static constexpr int NVS = 2;
+  static constexpr int VTB = NVS * SUBB;
   static constexpr int QB = N * D * 2;         // Q operand tile
   static constexpr int PSW = GT * 2;           // bytes of a P^T row (the swizzle width)
   static constexpr int PH = TSK * PSW;         // P^T bytes of one head
@@ -84,17 +93,20 @@ struct UCfg {
   static constexpr int OFF_VT = OFF_KP + NKPS * KPB;
   static constexpr int OFF_Q = OFF_VT + VTB;
   static constexpr int OFF_PT = OFF_Q + round_up(QB, 1024);
-  static constexpr int REST = 1024 + 3 * 256 + 256 + 64 + 128 + (FP8 ? 1024 : 0);  // exchange arrays, barriers, ids, scales
+  static constexpr int REST = 1024 + 3 * 256 + 512 + 64 + 128 + (FP8 ? 4096 : 0);  // exchange arrays, barriers, ids, scales
   static constexpr int NPT = OFF_PT + 2 * PB + REST + 1024 + 1024 <= kSmemLimit ? 2 : 1;
   static constexpr int OFF_RED = OFF_PT + NPT * PB;  // [4 warps][64] floats
   static constexpr int OFF_ALPHA = OFF_RED + 1024;   // [N] floats
   static constexpr int OFF_COLL = OFF_ALPHA + 256;   // [N] floats
   static constexpr int OFF_COLM = OFF_COLL + 256;    // [N] floats
-  static constexpr int OFF_BAR = OFF_COLM + 256;     // 32 mbarriers
-  static constexpr int OFF_MISC = OFF_BAR + 256;     // tensor-memory base, abort flag
+  static constexpr int OFF_BAR = OFF_COLM + 256;     // 64 mbarrier slots
+  static constexpr int OFF_MISC = OFF_BAR + 512;     // tensor-memory base, abort flag
   static constexpr int OFF_IDS = OFF_MISC + 64;      // page ids of a stage: [4][8] ints
-  static constexpr int OFF_KSS = OFF_IDS + 128;      // fp8: scale_log2 * K scale per key row: [2][128] floats
-  static constexpr int OFF_TABLE = OFF_KSS + (FP8 ? 1024 : 0);  // balanced mode: per-sequence lengths, starts
+  // fp8 per-row scales of a stage, a ring of four stages: the K converters
+  // can run two stages ahead of the softmax that reads them
+  static constexpr int OFF_KSS = OFF_IDS + 128;      // fp8: scale_log2 * K scale per key row: [4][128] floats
+  static constexpr int OFF_VSS = OFF_KSS + (FP8 ? 2048 : 0);  // fp8: V scale per key row: [4][128] floats
+  static constexpr int OFF_TABLE = OFF_VSS + (FP8 ? 2048 : 0);  // balanced mode: per-sequence lengths, starts
   static constexpr int SMEM_FIXED = OFF_TABLE + 1024;  // + 1024 to align the dynamic base
   // tensor-memory columns: S^T [2][N], then O^T [2 items][NVT][N]
   static constexpr int TM_O = 2 * N;
@@ -118,8 +130,8 @@ enum UBar {
   kBRawVEmpty = 6,  // [2] converters done with them (4 warps)
   kBKpFull = 8,     // [2] K piece written (4 warps)
   kBKpEmpty = 10,   // [2] K piece read by its MMAs (commit)
-  kBVtFull = 12,    // V tile written (4 warps)
-  kBVtEmpty = 13,   // V tile read (commit)
+  kBVtFull = 12,    // [2] V sub-tile written (4 warps)
+  kBVtEmpty = 32,   // [2] V sub-tile read (commit)
   kBSFull = 14,     // [2] S^T computed (commit)
   kBSEmpty = 16,    // [2] S^T read by the softmax (4 warps)
   kBPFull = 18,     // [2] P^T written (4 warps)
@@ -129,9 +141,9 @@ enum UBar {
   kBQFull = 26,     // Q landed (tx bytes)
   kBQReady = 27,    // fp8: Q converted to f16 (4 warps)
   kBQEmpty = 28,    // Q no longer read (commit)
-  kBDone = 29,      // every MMA of the CTA complete (commit)
-  kBKssFull = 30,   // [2] fp8: a stage's K scales written (4 warps)
-  kBCount = 32
+  kBDone = 29,      // every MMA of the CTA complete (a commit by each issuer)
+  kBKssFull = 34,   // [4] fp8: a stage's K and V scales written (4 warps)
+  kBCount = 38
 };
 
 // Max or sum of GT values over the 32 lanes of a warp, by halving exchange:
@@ -167,6 +179,13 @@ __device__ __forceinline__ int reduced_col0(int lane) {
   return GT == 16 ? (lane >> 1) : (GT == 32 ? lane : 2 * lane);
 }
 
+// Maximum of x over the 32 lanes of the warp, in every lane.
+__device__ __forceinline__ float redux_max(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 template <int R>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
@@ -176,11 +195,6 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
 
 template <int D, int KV, int GT, int N>
 __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_constant__ SplitParams p) {
@@ -192,8 +206,14 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
   constexpr int NVT = C::NVT;
   constexpr int NPT = C::NPT;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // (pointer arithmetic on the shared array, so that accesses through smem
+  // stay shared-memory accesses)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
+  // 16-byte shared loads and stores by shared address, as ordinary C++
+  // accesses (the compiler may overlap them; mbarrier waits order them)
+  auto lds = [&](uint32_t a) { return *reinterpret_cast<const uint4*>(smem + (a - sbase)); };
+  auto sts = [&](uint32_t a, uint4 v) { *reinterpret_cast<uint4*>(smem + (a - sbase)) = v; };
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -220,14 +240,15 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
       mbar_init(bar(kBOFull + s), 1);
       mbar_init(bar(kBOEmpty + s), 4);
     }
-    mbar_init(bar(kBVtFull), 4);
-    mbar_init(bar(kBVtEmpty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBVtFull + s), 4);
+      mbar_init(bar(kBVtEmpty + s), 1);
+    }
     mbar_init(bar(kBQFull), 1);
     mbar_init(bar(kBQReady), 4);
     mbar_init(bar(kBQEmpty), 1);
-    mbar_init(bar(kBDone), 1);
-    mbar_init(bar(kBKssFull), 4);
-    mbar_init(bar(kBKssFull + 1), 4);
+    mbar_init(bar(kBDone), 2);
+    for (int s = 0; s < 4; ++s) mbar_init(bar(kBKssFull + s), 4);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -273,23 +294,27 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
 
   if (wg == 3) {
    regs_dec<kRegOther>();
-   if (warp == kUProducerWarp) {
-    // ================================================================ producer
+   if (warp == kUProducerWarp || warp == kUVProducerWarp) {
+    // ================================================================ producers
+    // Two warps: one copies the K pages (and Q, and publishes the page
+    // ids), the other the V pages, so that neither waits behind the other's
+    // ring (V slots are released later than K slots).
+    const int kv = warp == kUVProducerWarp ? 1 : 0;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
     if (lane == 0) {
-      prefetch_tensormap(&p.tm_q);
-      prefetch_tensormap(&p.tm_k);
-      prefetch_tensormap(&p.tm_v);
+      if (kv == 0) prefetch_tensormap(&p.tm_q);
+      prefetch_tensormap(kv ? &p.tm_v : &p.tm_k);
     }
     int stage = 0, qn = 0;
     uint32_t filled = 0, fill_parity = 0;
     const uint32_t row_bytes = (uint32_t)(H2 * D * C::E);
     while (ok && next_item(p, s_ctx, s_start, cur, it)) {
       if (it.nst == 0) continue;
-      if (qn >= 1) ok = __all_sync(0xffffffffu, mbar_wait(bar(kBQEmpty), (qn - 1) & 1, kWaitLimitNs, s_abort));
+      if (kv == 0 && qn >= 1)
+        ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(kBQEmpty), (qn - 1) & 1, kWaitLimitNs, s_abort));
       if (!ok) break;
-      if (lane == 0) {
+      if (kv == 0 && lane == 0) {
         const uint32_t qdst = sbase + C::OFF_Q;
         mbar_arrive_expect_tx(bar(kBQFull), C::QB);
         for (int hl = 0; hl < H2; ++hl)
@@ -319,12 +344,9 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
         const int npg = scr ? 0 : (P < TSK ? (valid + P - 1) / P : 1);
         filled |= 1u << slot;
         fill_parity = (fill_parity & ~(1u << slot)) | (uint32_t((stage >> 1) & 1) << slot);
-        // K boxes when the slot's K half is free, then V boxes when its V
-        // half is (the converters release K earlier than V)
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
+        {
           if (stage >= 2) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar((kv ? kBRawVEmpty : kBRawKEmpty) + slot),
+            ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar((kv ? kBRawVEmpty : kBRawKEmpty) + slot),
                                                    ((stage >> 1) - 1) & 1, kWaitLimitNs, s_abort));
             if (!ok) break;
           }
@@ -367,111 +389,121 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
       const int zero = 0;
       const volatile int* no_abort = &zero;
       for (int s2 = 0; s2 < 2; ++s2)
-        if (filled >> s2 & 1) {
-          mbar_wait(bar(kBRawKFull + s2), fill_parity >> s2 & 1, kWaitLimitNs, no_abort);
-          mbar_wait(bar(kBRawVFull + s2), fill_parity >> s2 & 1, kWaitLimitNs, no_abort);
-        }
-      if (qn > 0) mbar_wait(bar(kBQFull), (qn - 1) & 1, kWaitLimitNs, no_abort);
+        if (filled >> s2 & 1)
+          mbar_wait(bar((kv ? kBRawVFull : kBRawKFull) + s2), fill_parity >> s2 & 1, kWaitLimitNs, no_abort);
+      if (kv == 0 && qn > 0) mbar_wait(bar(kBQFull), (qn - 1) & 1, kWaitLimitNs, no_abort);
     }
-   } else if (warp == kUMmaWarp) {
-    // ================================================================ MMA issuer
+   } else if (warp == kUMmaWarp || warp == kUPvWarp) {
+    // ================================================================ MMA issuers
+    // Two threads issue the MMAs, one per product, so that neither waits
+    // behind the other's operands: lane 0 of warp 13 computes S^T = K Q^T
+    // stage by stage, lane 0 of warp 15 the P V products. They write
+    // different tensor-memory columns and meet only through the softmax
+    // (S -> P, and the rescale of O). Each shares its SM sub-partition with
+    // busy warps, so an MMA is one add to a precomputed descriptor and the
+    // loops over pieces, k-steps, heads and tiles are unrolled. tcgen05
+    // fences follow only the waits that hand tensor memory between threads
+    // (the S and O buffers); operands in shared memory are ordered by the
+    // writers' proxy fences and the mbarriers.
     if (lane == 0) {
       constexpr bool BF = C::BF16;
-      constexpr uint32_t idS = idesc_f16(128, N, BF, false, false);
-      constexpr uint32_t idPV = idesc_f16(128, GT, BF, true, true);
-      const uint32_t kp0 = sbase + C::OFF_KP, vt0 = sbase + C::OFF_VT, q0 = sbase + C::OFF_Q;
-      const uint32_t pt0 = sbase + C::OFF_PT;
-      int st = 0, kpi = 0, vti = 0, qn = 0, oi = 0;
-      // a stage whose P V product is still to issue (issued after the next
-      // stage's S, so that the tensor core works while the softmax runs)
-      bool pend = false;
-      int pst = 0, pob = 0, poi = 0;
-      bool pfirst = false, plast = false;
-      auto issue_pv = [&]() {
-        if (ok && pfirst && poi >= 2) {
-          ok = mbar_wait(bar(kBOEmpty + pob), ((poi >> 1) - 1) & 1, kWaitLimitNs, s_abort);
-          if (!ok) raise_abort(s_abort, p.err_flags);
-        }
-        const int pb = pst % NPT;
-        if (ok) {
-          ok = mbar_wait(bar(kBPFull + pb), (pst / NPT) & 1, kWaitLimitNs, s_abort);
-          if (!ok) raise_abort(s_abort, p.err_flags);
-        }
-        tc_fence_after();
-        for (int tt = 0; tt < NVT; ++tt, ++vti) {
+      int st = 0, qn = 0, oi = 0;
+      if (warp == kUMmaWarp) {
+        constexpr uint32_t idS = idesc_f16(128, N, BF, false, false);
+        const uint64_t dK0 = smem_desc(sbase + C::OFF_KP, 16, 1024, kSwz128);
+        const uint64_t dQ0 = smem_desc(sbase + C::OFF_Q, 16, 1024, kSwz128);
+        int kpi = 0;
+        while (next_item(p, s_ctx, s_start, cur, it)) {
+          if (it.nst == 0) continue;
           if (ok) {
-            ok = mbar_wait(bar(kBVtFull), vti & 1, kWaitLimitNs, s_abort);
+            ok = mbar_wait_sleep(bar(FP8 ? kBQReady : kBQFull), qn & 1, kWaitLimitNs, s_abort);
             if (!ok) raise_abort(s_abort, p.err_flags);
           }
-          tc_fence_after();
-          if (ok) {
-#pragma unroll
-            for (int h = 0; h < H2; ++h) {
-              const uint32_t d_tm = tm + C::TM_O + (uint32_t)((pob * NVT + tt) * N + h * GT);
-#pragma unroll
-              for (int ks = 0; ks < TSK / 16; ++ks) {
-                const uint64_t ad = smem_desc(vt0 + (h * TSK + 16 * ks) * 128, 16384, 1024, kSwz128);
-                const uint64_t bd = smem_desc(pt0 + pb * C::PB + h * C::PH + ks * 16 * C::PSW, C::PH, 8 * C::PSW,
-                                              C::PSWZ);
-                umma_f16(d_tm, ad, bd, idPV, (pfirst && ks == 0) ? 0u : 1u);
-              }
-            }
-          }
-          umma_commit(bar(kBVtEmpty));
-        }
-        umma_commit(bar(kBPEmpty + pb));
-        if (plast) umma_commit(bar(kBOFull + pob));
-        pend = false;
-      };
-      while (next_item(p, s_ctx, s_start, cur, it)) {
-        if (it.nst == 0) continue;
-        if (ok) {
-          ok = mbar_wait(bar(FP8 ? kBQReady : kBQFull), qn & 1, kWaitLimitNs, s_abort);
-          if (!ok) raise_abort(s_abort, p.err_flags);
-        }
-        ++qn;
-        for (int j = 0; j < it.nst; ++j, ++st) {
-          const int sb = st & 1;
-          if (ok && st >= 2) {
-            ok = mbar_wait(bar(kBSEmpty + sb), ((st >> 1) - 1) & 1, kWaitLimitNs, s_abort);
-            if (!ok) raise_abort(s_abort, p.err_flags);
-          }
-          tc_fence_after();
-          for (int c = 0; c < C::NKP; ++c, ++kpi) {
-            const int ks = kpi & 1;
-            if (ok) {
-              ok = mbar_wait(bar(kBKpFull + ks), (kpi >> 1) & 1, kWaitLimitNs, s_abort);
+          ++qn;
+          for (int j = 0; j < it.nst; ++j, ++st) {
+            const int sb = st & 1;
+            if (ok && st >= 2) {
+              ok = mbar_wait_sleep(bar(kBSEmpty + sb), ((st >> 1) - 1) & 1, kWaitLimitNs, s_abort);
               if (!ok) raise_abort(s_abort, p.err_flags);
             }
             tc_fence_after();
-            if (ok) {
+            const uint32_t d_s = tm + (uint32_t)(sb * N);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = smem_desc(kp0 + ks * C::KPB + k * 32, 16, 1024, kSwz128);
-                const uint64_t bd = smem_desc(q0 + c * (N * 128) + k * 32, 16, 1024, kSwz128);
-                umma_f16(tm + (uint32_t)(sb * N), ad, bd, idS, (c | k) ? 1u : 0u);
+            for (int c = 0; c < C::NKP; ++c, ++kpi) {
+              const int ks = kpi & 1;
+              if (ok) {
+                ok = mbar_wait_sleep(bar(kBKpFull + ks), (kpi >> 1) & 1, kWaitLimitNs, s_abort);
+                if (!ok) raise_abort(s_abort, p.err_flags);
+              }
+              if (ok) {
+                const uint64_t dK = dK0 + (uint64_t)(ks * (C::KPB >> 4));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  umma_f16(d_s, dK + 2 * k, dQ0 + (uint64_t)(((c * N * 128) >> 4) + 2 * k), idS,
+                           (c | k) ? 1u : 0u);
+              }
+              umma_commit(bar(kBKpEmpty + ks));
+            }
+            umma_commit(bar(kBSFull + sb));
+            if (j == it.nst - 1) umma_commit(bar(kBQEmpty));
+          }
+        }
+      } else {
+        constexpr uint32_t idPV = idesc_f16(128, GT, BF, true, true);
+        const uint64_t dV0 = smem_desc(sbase + C::OFF_VT, C::SUBR * 128, 1024, kSwz128);
+        const uint64_t dP0 = smem_desc(sbase + C::OFF_PT, C::PH, 8 * C::PSW, C::PSWZ);
+        int vti = 0;
+        while (next_item(p, s_ctx, s_start, cur, it)) {
+          if (it.nst == 0) continue;
+          const int ob = oi & 1;
+          for (int j = 0; j < it.nst; ++j, ++st) {
+            if (ok && j == 0 && oi >= 2) {  // the epilogue of item oi - 2 has read this O buffer
+              ok = mbar_wait_sleep(bar(kBOEmpty + ob), ((oi >> 1) - 1) & 1, kWaitLimitNs, s_abort);
+              if (!ok) raise_abort(s_abort, p.err_flags);
+            }
+            const int pb = st % NPT;
+            if (ok) {
+              ok = mbar_wait_sleep(bar(kBPFull + pb), (st / NPT) & 1, kWaitLimitNs, s_abort);
+              if (!ok) raise_abort(s_abort, p.err_flags);
+            }
+            tc_fence_after();
+            const uint64_t dP = dP0 + (uint64_t)((pb * C::PB) >> 4);
+            const uint32_t acc0 = j == 0 ? 0u : 1u;
+#pragma unroll
+            for (int tt = 0; tt < NVT; ++tt) {
+#pragma unroll
+              for (int hk = 0; hk < H2 * C::NKH; ++hk, ++vti) {
+                const int h = hk / C::NKH, kh = hk % C::NKH;
+                const int vsl = vti & 1;
+                if (ok) {
+                  ok = mbar_wait_sleep(bar(kBVtFull + vsl), (vti >> 1) & 1, kWaitLimitNs, s_abort);
+                  if (!ok) raise_abort(s_abort, p.err_flags);
+                }
+                if (ok) {
+                  const uint32_t d_tm = tm + C::TM_O + (uint32_t)((ob * NVT + tt) * N + h * GT);
+                  const uint64_t dV = dV0 + (uint64_t)((vsl * C::SUBB) >> 4);
+#pragma unroll
+                  for (int ks = 0; ks < C::SUBR / 16; ++ks)
+                    umma_f16(d_tm, dV + (uint64_t)((ks * 16 * 128) >> 4),
+                             dP + (uint64_t)((h * C::PH + (kh * C::SUBR + ks * 16) * C::PSW) >> 4), idPV,
+                             (kh == 0 && ks == 0) ? acc0 : 1u);
+                }
+                umma_commit(bar(kBVtEmpty + vsl));
               }
             }
-            umma_commit(bar(kBKpEmpty + ks));
+            umma_commit(bar(kBPEmpty + pb));
+            if (j == it.nst - 1) umma_commit(bar(kBOFull + ob));
           }
-          umma_commit(bar(kBSFull + sb));
-          if (j == it.nst - 1) umma_commit(bar(kBQEmpty));
-          if (pend) issue_pv();
-          pend = true;
-          pst = st;
-          pob = oi & 1;
-          poi = oi;
-          pfirst = j == 0;
-          plast = j == it.nst - 1;
+          ++oi;
         }
-        ++oi;
       }
-      if (pend) issue_pv();
-      // every MMA complete before the tensor memory is released
+      // every MMA of this thread complete before the tensor memory is released
       umma_commit(bar(kBDone));
-      const int zero = 0;
-      const volatile int* no_abort = &zero;
-      mbar_wait(bar(kBDone), 0, kWaitLimitNs, no_abort);
+      if (warp == kUMmaWarp) {
+        const int zero = 0;
+        const volatile int* no_abort = &zero;
+        mbar_wait(bar(kBDone), 0, kWaitLimitNs, no_abort);
+      }
     }
     __syncwarp();
    }
@@ -487,13 +519,14 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
     int stage = 0, qn = 0, kpi = 0, vti = 0;
     const uint32_t kp0 = sbase + C::OFF_KP, vt0 = sbase + C::OFF_VT;
     float* s_kss = reinterpret_cast<float*>(smem + C::OFF_KSS);
+    float* s_vss = reinterpret_cast<float*>(smem + C::OFF_VSS);
     const float sl = p.scale_log2;
     while (next_item(p, s_ctx, s_start, cur, it)) {
       if (it.nst == 0) continue;
       const int g = it.hg * H2 + h;
       if (FP8 && isK) {  // Q: bf16 as copied -> f16 in place (the MMA takes both operands in f16)
         if (ok) {
-          ok = mbar_wait(bar(kBQFull), qn & 1, kWaitLimitNs, s_abort);
+          ok = mbar_wait_sleep(bar(kBQFull), qn & 1, kWaitLimitNs, s_abort);
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
         if (ok) {
@@ -524,107 +557,116 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
                                   : (uint32_t)((t >> p.lbr) * box_bytes + h * p.BR * 128 + (t & (p.BR - 1)) * 128);
         const uint32_t cs = scr ? scr_cstride : cstride;
         if (ok) {
-          ok = mbar_wait(bar((isK ? kBRawKFull : kBRawVFull) + slot), (st >> 1) & 1, kWaitLimitNs, s_abort);
+          ok = mbar_wait_sleep(bar((isK ? kBRawKFull : kBRawVFull) + slot), (st >> 1) & 1, kWaitLimitNs, s_abort);
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
-        // fp8: this token's scale (its page id from the producer's table);
-        // loaded now, used after the conversions (K) or by them (V)
-        float sc = 0.f;
-        if (FP8 && ok && in_ctx) {
+        // fp8, K converters: this token's K and V scales (its page id from
+        // the producer's table); loaded now, published after the K pieces
+        float ksc = 0.f, vsc_f = 0.f;
+        if (FP8 && isK && ok && in_ctx) {
           const int tok = t_first + t;
           int pg = s_ids[(st & 3) * 8 + (P < TSK ? (t >> lp) : 0)];
-          pg = (unsigned)pg < (unsigned)p.num_pages ? pg : 0;  // outside the pool: page 0's (finite) scale
-          sc = __ldg((isK ? p.k_scale : p.v_scale) + ((size_t)pg * P + (tok & (P - 1))) * p.Hkv + g);
+          pg = (unsigned)pg < (unsigned)p.num_pages ? pg : 0;  // outside the pool: page 0's (finite) scales
+          const size_t off = ((size_t)pg * P + (tok & (P - 1))) * p.Hkv + g;
+          ksc = __ldg(p.k_scale + off);
+          vsc_f = __ldg(p.v_scale + off);
         }
         const uint32_t rbase = sbase + slot * C::RAW + (isK ? 0 : C::RAWT);
         if (isK) {
           for (int c = 0; c < C::NKP; ++c, ++kpi) {
             const int ks = kpi & 1;
             if (ok && kpi >= 2) {
-              ok = mbar_wait(bar(kBKpEmpty + ks), ((kpi >> 1) - 1) & 1, kWaitLimitNs, s_abort);
+              ok = mbar_wait_sleep(bar(kBKpEmpty + ks), ((kpi >> 1) - 1) & 1, kWaitLimitNs, s_abort);
               if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
             }
             if (ok) {
               const uint32_t dst = kp0 + ks * C::KPB + kr * 128;
               if (!has_src) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) st_shared_v4(dst + ((u ^ sw) << 4), make_uint4(0, 0, 0, 0));
+                for (int u = 0; u < 8; ++u) sts(dst + ((u ^ sw) << 4), make_uint4(0, 0, 0, 0));
               } else if (FP8) {
                 const uint32_t src = rbase + roff + (c >> 1) * cs;
+                uint4 v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[i] = lds(src + (((4 * (c & 1) + i) ^ sw) << 4));
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  const int jl = 4 * (c & 1) + i;
-                  const uint4 v = ld_shared_v4(src + ((jl ^ sw) << 4));
-                  st_shared_v4(dst + (((2 * i) ^ sw) << 4),
-                               make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
-                                          e4m3x2_to_f16x2(v.y >> 16)));
-                  st_shared_v4(dst + (((2 * i + 1) ^ sw) << 4),
-                               make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
-                                          e4m3x2_to_f16x2(v.w >> 16)));
+                  sts(dst + (((2 * i) ^ sw) << 4),
+                      make_uint4(e4m3x2_to_f16x2(v[i].x), e4m3x2_to_f16x2(v[i].x >> 16), e4m3x2_to_f16x2(v[i].y),
+                                 e4m3x2_to_f16x2(v[i].y >> 16)));
+                  sts(dst + (((2 * i + 1) ^ sw) << 4),
+                      make_uint4(e4m3x2_to_f16x2(v[i].z), e4m3x2_to_f16x2(v[i].z >> 16), e4m3x2_to_f16x2(v[i].w),
+                                 e4m3x2_to_f16x2(v[i].w >> 16)));
                 }
               } else {
                 const uint32_t src = rbase + roff + c * cs;
+                uint4 v[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {  // both rows have the same swizzle phase: copy units as
-                  const int pu = u ^ sw;       // stored, each lane of an 8-row phase on its own banks
-                  st_shared_v4(dst + pu * 16, ld_shared_v4(src + pu * 16));
-                }
+                for (int u = 0; u < 8; ++u) v[u] = lds(src + ((u ^ sw) << 4));  // both rows have the same
+#pragma unroll                                                                      // swizzle phase: copy units
+                for (int u = 0; u < 8; ++u) sts(dst + ((u ^ sw) << 4), v[u]);  // as stored, a bank group each
               }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBKpFull + ks));
           }
-          if (FP8) {  // the softmax's per-row factor scale_log2 * K scale of the stage
-            s_kss[(st & 1) * 128 + kr] = sl * sc;
+          if (FP8) {  // for the softmax: scale_log2 * K scale, and the V scale
+            s_kss[(st & 3) * 128 + kr] = sl * ksc;
+            s_vss[(st & 3) * 128 + kr] = vsc_f;
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBKssFull + (st & 1)));
+            if (lane == 0) mbar_arrive(bar(kBKssFull + (st & 3)));
           }
         } else {
-          uint32_t vsc = 0;
-          if (FP8) {
-            const __half2 h2 = __float2half2_rn(sc);
-            vsc = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          for (int tt = 0; tt < NVT; ++tt, ++vti) {
-            if (ok && vti >= 1) {
-              ok = mbar_wait(bar(kBVtEmpty), (vti - 1) & 1, kWaitLimitNs, s_abort);
-              if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
-            }
-            if (ok) {
+          // V^T sub-tiles (tt, head hv): this thread writes pieces of row
+          // r = kr % TSK (token r of head hv): 32 bytes of output each, PPT
+          // of the row's 8 pieces starting at part * PPT.
+          constexpr int SUBR = C::SUBR;
+          constexpr int PPT = SUBR / 16;
+          const int r0 = kr % SUBR, part = kr / SUBR;
+          const int swr = r0 & 7;
+          for (int tt = 0; tt < NVT; ++tt) {
+            for (int hk = 0; hk < H2 * C::NKH; ++hk, ++vti) {
+              const int hv = hk / C::NKH;
+              const int r = (hk % C::NKH) * SUBR + r0;  // token of head hv
+              const bool r_ok = scr ? r < p.T : r < valid;
+              const int vsl = vti & 1;
+              if (ok && vti >= 2) {
+                ok = mbar_wait_sleep(bar(kBVtEmpty + vsl), ((vti >> 1) - 1) & 1, kWaitLimitNs, s_abort);
+                if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
+              }
+              if (ok) {
+                const uint32_t srow = rbase + (scr ? (uint32_t)(hv * p.TP * 128 + r * 128)
+                                                   : (uint32_t)((r >> p.lbr) * box_bytes + hv * p.BR * 128 +
+                                                                (r & (p.BR - 1)) * 128));
+                const uint32_t drow = vt0 + vsl * C::SUBB + r0 * 128;
 #pragma unroll
-              for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * tt + cc;  // 64-column chunk of the row
-                const uint32_t dst = vt0 + cc * 16384 + kr * 128;
-                if (!in_ctx) {  // past the stage's valid tokens: zero (the product must see no NaN)
-#pragma unroll
-                  for (int u = 0; u < 8; ++u) st_shared_v4(dst + ((u ^ sw) << 4), make_uint4(0, 0, 0, 0));
-                } else if (FP8) {
-                  const uint32_t src = rbase + roff + (c >> 1) * cs;
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    const int jl = 4 * (c & 1) + i;
-                    const uint4 v = ld_shared_v4(src + ((jl ^ sw) << 4));
-                    st_shared_v4(dst + (((2 * i) ^ sw) << 4),
-                                 make_uint4(hmul2(e4m3x2_to_f16x2(v.x), vsc), hmul2(e4m3x2_to_f16x2(v.x >> 16), vsc),
-                                            hmul2(e4m3x2_to_f16x2(v.y), vsc), hmul2(e4m3x2_to_f16x2(v.y >> 16), vsc)));
-                    st_shared_v4(dst + (((2 * i + 1) ^ sw) << 4),
-                                 make_uint4(hmul2(e4m3x2_to_f16x2(v.z), vsc), hmul2(e4m3x2_to_f16x2(v.z >> 16), vsc),
-                                            hmul2(e4m3x2_to_f16x2(v.w), vsc), hmul2(e4m3x2_to_f16x2(v.w >> 16), vsc)));
+                for (int q0 = 0; q0 < PPT; ++q0) {
+                  const int q = part * PPT + q0;  // piece: chunk cc = q / 4 of the tile, pair i = q % 4
+                  const int cc = q >> 2, i = q & 3;
+                  const int c = 2 * tt + cc;      // 64-column chunk of the row
+                  const uint32_t dst = drow + cc * (SUBR * 128);
+                  uint4 lo, hi;
+                  if (!r_ok) {  // past the stage's valid tokens: zero (the product must see no NaN)
+                    lo = hi = make_uint4(0, 0, 0, 0);
+                  } else if (FP8) {
+                    const uint4 v = lds(srow + (c >> 1) * cs + (((4 * (c & 1) + i) ^ swr) << 4));
+                    lo = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                                    e4m3x2_to_f16x2(v.y >> 16));
+                    hi = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                                    e4m3x2_to_f16x2(v.w >> 16));
+                  } else {
+                    lo = lds(srow + c * cs + (((2 * i) ^ swr) << 4));
+                    hi = lds(srow + c * cs + (((2 * i + 1) ^ swr) << 4));
                   }
-                } else {
-                  const uint32_t src = rbase + roff + c * cs;
-#pragma unroll
-                  for (int u = 0; u < 8; ++u) {
-                    const int pu = u ^ sw;
-                    st_shared_v4(dst + pu * 16, ld_shared_v4(src + pu * 16));
-                  }
+                  sts(dst + (((2 * i) ^ swr) << 4), lo);
+                  sts(dst + (((2 * i + 1) ^ swr) << 4), hi);
                 }
               }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(kBVtFull + vsl));
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBVtFull));
           }
         }
         __syncwarp();
@@ -645,7 +687,10 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
     float* colL = reinterpret_cast<float*>(smem + C::OFF_COLL);
     float* colM = reinterpret_cast<float*>(smem + C::OFF_COLM);
     const uint32_t pt0 = sbase + C::OFF_PT;
-    constexpr float slack = kMaxSlack;
+    // The running max moves only past this slack, so p = 2^(s - m) <= 2^slack.
+    // fp8: P also carries the token's V scale, p * v_scale in f16; a slack of
+    // 4 keeps it finite for V scales up to 4095 (|v| up to 1.8e6).
+    constexpr float slack = FP8 ? 4.f : kMaxSlack;
     const float sl = p.scale_log2;
     int stage = 0, oi = 0;
 
@@ -681,13 +726,14 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
         }
       }
       const float* s_kss = reinterpret_cast<const float*>(smem + C::OFF_KSS);
+      const float* s_vss = reinterpret_cast<const float*>(smem + C::OFF_VSS);
       const int ob = oi & 1;
 
       for (int j = 0; j < it.nst; ++j) {
         const int st = stage + j, sb = st & 1;
         float s[GT];
         if (ok) {
-          ok = mbar_wait(bar(kBSFull + sb), (st >> 1) & 1, kWaitLimitNs, s_abort);
+          ok = mbar_wait_sleep(bar(kBSFull + sb), (st >> 1) & 1, kWaitLimitNs, s_abort);
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
         tc_fence_after();
@@ -697,15 +743,16 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
 #pragma unroll
           for (int i = 0; i < GT; ++i) s[i] = 0.f;
         }
-        // fp8: this row's scale_log2 * K scale, read before the S buffer is
-        // released (the K converters rewrite the slot two stages on)
-        float kss = sl;
+        // fp8: this row's scale_log2 * K scale and V scale (slot st % 4: the
+        // K converters run at most two stages ahead of this read)
+        float kss = sl, vsr = 1.f;
         if (FP8) {
           if (ok) {
-            ok = mbar_wait(bar(kBKssFull + sb), (st >> 1) & 1, kWaitLimitNs, s_abort);
+            ok = mbar_wait_sleep(bar(kBKssFull + (st & 3)), (st >> 2) & 1, kWaitLimitNs, s_abort);
             if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
           }
-          kss = s_kss[sb * 128 + kr];
+          kss = s_kss[(st & 3) * 128 + kr];
+          vsr = s_vss[(st & 3) * 128 + kr];
         }
         tc_fence_before();
         __syncwarp();
@@ -713,41 +760,45 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
         // scale (and the K scale of this row's token), mask
         const bool scr = it.scratch && j == it.nst - 1;
         const int valid = scr ? p.T : min(TSK, it.tok_end - (it.tok0 + j * TSK));
-        const uint64_t vis = scr ? vis_bits : (t < valid ? ~0ull : 0ull);
+        if (scr) {
 #pragma unroll
-        for (int i = 0; i < GT; ++i) s[i] = (vis >> i) & 1 ? s[i] * kss : NEG_INF;
-        // stage max of every column over the head's tokens (mn first holds
-        // the warp's reduction, then the new running max)
+          for (int i = 0; i < GT; ++i) s[i] = (vis_bits >> i) & 1 ? s[i] * kss : NEG_INF;
+        } else {
+          const bool tv = t < valid;
+#pragma unroll
+          for (int i = 0; i < GT; ++i) s[i] = tv ? s[i] * kss : NEG_INF;
+        }
+        // stage max of every column over the head's tokens: the warp's by
+        // one reduction per column, then across the head's warps through
+        // shared memory (mn holds the maxima, then the new running max)
         float mn[GT];
 #pragma unroll
-        for (int i = 0; i < GT; ++i) mn[i] = s[i];
-        warp_columns_reduce<GT, true>(mn, lane);
-        {
-          const int c0 = reduced_col0<GT>(lane);
-          if (GT != 16 || (lane & 1) == 0) {
+        for (int i = 0; i < GT; ++i) mn[i] = redux_max(s[i]);
+        if (nwh > 1) {
+          if (lane == 0) {
 #pragma unroll
-            for (int r = 0; r < (GT > 32 ? GT / 32 : 1); ++r) red[warp * 64 + c0 + r] = mn[r];
+            for (int i = 0; i < GT; i += 4)
+              *reinterpret_cast<float4*>(red + warp * 64 + i) = make_float4(mn[i], mn[i + 1], mn[i + 2], mn[i + 3]);
+          }
+          named_barrier_sync(1, 128);
+#pragma unroll
+          for (int w2 = 0; w2 < nwh; ++w2) {
+            if (wh0 + w2 == warp) continue;
+#pragma unroll
+            for (int i = 0; i < GT; i += 4) {
+              const float4 x = *reinterpret_cast<const float4*>(red + (wh0 + w2) * 64 + i);
+              mn[i] = fmaxf(mn[i], x.x);
+              mn[i + 1] = fmaxf(mn[i + 1], x.y);
+              mn[i + 2] = fmaxf(mn[i + 2], x.z);
+              mn[i + 3] = fmaxf(mn[i + 3], x.w);
+            }
           }
         }
-        named_barrier_sync(1, 128);
         bool need_o = false;
 #pragma unroll
-        for (int i = 0; i < GT; i += 4) {
-          float4 M = *reinterpret_cast<const float4*>(red + wh0 * 64 + i);
-#pragma unroll
-          for (int w2 = 1; w2 < nwh; ++w2) {
-            const float4 x = *reinterpret_cast<const float4*>(red + (wh0 + w2) * 64 + i);
-            M.x = fmaxf(M.x, x.x);
-            M.y = fmaxf(M.y, x.y);
-            M.z = fmaxf(M.z, x.z);
-            M.w = fmaxf(M.w, x.w);
-          }
-          const float Mv[4] = {M.x, M.y, M.z, M.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            mn[i + e] = Mv[e] > m[i + e] + slack ? Mv[e] : m[i + e];
-            need_o |= (m[i + e] != NEG_INF) && (mn[i + e] != m[i + e]);
-          }
+        for (int i = 0; i < GT; ++i) {
+          mn[i] = mn[i] > m[i] + slack ? mn[i] : m[i];
+          need_o |= (m[i] != NEG_INF) && (mn[i] != m[i]);
         }
         if (named_barrier_or(2, 128, need_o)) {
           // A running max moved: rescale l and the O^T columns (all heads:
@@ -761,7 +812,7 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
           named_barrier_sync(1, 128);
           if (j > 0) {
             if (ok) {
-              ok = mbar_wait(bar(kBPEmpty + (st - 1) % NPT), ((st - 1) / NPT) & 1, kWaitLimitNs, s_abort);
+              ok = mbar_wait_sleep(bar(kBPEmpty + (st - 1) % NPT), ((st - 1) / NPT) & 1, kWaitLimitNs, s_abort);
               if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
             }
             tc_fence_after();
@@ -795,13 +846,13 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
           const float p0 = ex2(s[i] - mu0), p1 = ex2(s[i + 1] - mu1);
           l[i] += p0;
           l[i + 1] += p1;
-          pk[i / 2] = pack16<!C::BF16>(p0, p1);
+          pk[i / 2] = FP8 ? pack16<true>(p0 * vsr, p1 * vsr) : pack16<!C::BF16>(p0, p1);
         }
         // P^T row of this token: wait until the product that last read the
         // buffer is done
         const int pb = st % NPT;
         if (ok && st >= NPT) {
-          ok = mbar_wait(bar(kBPEmpty + pb), ((st - NPT) / NPT) & 1, kWaitLimitNs, s_abort);
+          ok = mbar_wait_sleep(bar(kBPEmpty + pb), ((st - NPT) / NPT) & 1, kWaitLimitNs, s_abort);
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
         {
@@ -809,7 +860,7 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
           const int swp = (t & 7) >> C::PSHIFT;
 #pragma unroll
           for (int u = 0; u < C::PSW / 16; ++u)
-            st_shared_v4(rowa + ((u ^ swp) << 4), make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+            sts(rowa + ((u ^ swp) << 4), make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -844,7 +895,7 @@ __global__ void __launch_bounds__(kUThreads, 1) pa_umma_kernel(const __grid_cons
       const float NaN = __int_as_float(0x7fffffff);
       if (it.nst > 0) {
         if (ok) {
-          ok = mbar_wait(bar(kBOFull + ob), (oi >> 1) & 1, kWaitLimitNs, s_abort);
+          ok = mbar_wait_sleep(bar(kBOFull + ob), (oi >> 1) & 1, kWaitLimitNs, s_abort);
           if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
         }
         tc_fence_after();
