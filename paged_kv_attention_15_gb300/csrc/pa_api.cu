@@ -35,7 +35,7 @@ struct DeviceState {
   int sms;
   int smem_optin;
   int* err_flags;
-  std::atomic<const void*> smem_set[kKernelSlots];  // kernels whose shared-memory limit was raised
+  std::atomic<const void*> smem_set[kKernelSlots];  // kernels prepared for launch (setup_kernel)
 };
 
 DeviceState g_dev[kMaxDevices];  // zero-initialised (static storage)
@@ -68,24 +68,36 @@ pa_status device_state(DeviceState** out) {
   return PA_OK;
 }
 
-// Raises the kernel's dynamic shared-memory limit once per device.
-pa_status ensure_smem_attr(DeviceState* d, const void* fn) {
+// Prepares a kernel for launch, once per device: raises its dynamic
+// shared-memory limit and, for a kernel that moves registers between its
+// warpgroups, checks that it was built with the launch registers its split
+// draws on (with fewer, a setmaxnreg.inc would wait for registers that never
+// come; the call is refused instead).
+pa_status setup_kernel(DeviceState* d, const SplitKernel& k) {
+  if (k.launch_regs > 0) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, k.fn) != cudaSuccess) return PA_ERR_CUDA;
+    if (a.numRegs < k.launch_regs) return PA_ERR_UNSUPPORTED;
+  }
+  return cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status ensure_kernel_ready(DeviceState* d, const SplitKernel& k) {
   for (int i = 0; i < kKernelSlots; ++i)
-    if (d->smem_set[i].load(std::memory_order_acquire) == fn) return PA_OK;
+    if (d->smem_set[i].load(std::memory_order_acquire) == k.fn) return PA_OK;
   std::lock_guard<std::mutex> lock(g_mu);
   for (int i = 0; i < kKernelSlots; ++i) {
     const void* cur = d->smem_set[i].load(std::memory_order_relaxed);
-    if (cur == fn) return PA_OK;
+    if (cur == k.fn) return PA_OK;
     if (cur == nullptr) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
-        return PA_ERR_CUDA;
-      d->smem_set[i].store(fn, std::memory_order_release);
-      return PA_OK;
+      const pa_status st = setup_kernel(d, k);
+      if (st == PA_OK) d->smem_set[i].store(k.fn, std::memory_order_release);
+      return st;
     }
   }
-  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) == cudaSuccess
-             ? PA_OK
-             : PA_ERR_CUDA;
+  return setup_kernel(d, k);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -186,7 +198,7 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   const int cap_rows = pa::stage_rows(D * (fp8 ? 1 : 2), fp8);
   const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
   SplitKernel k{nullptr, 0, 0, 0};
-  int TS = 0, TSL = 0;
+  int TS = 0, TSL = 0, ilv = 1;
   for (int CW = 8; CW >= pa::kConsumerWarps && !k.fn; CW /= 2) {
     const int NGW = CW / MT;
     if (NGW < 1 || NGW % HT) continue;
@@ -196,24 +208,21 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
     for (int rows = cap_rows; rows >= 64 && !k.fn; rows /= 2) {
       TS = rows / H2;
       if (TS % NSL) continue;
-      TSL = TS / NSL;
-      if (TSL != 16 && TSL != 32 && TSL != 64) continue;
-      k = pick_kernel(kind, D, MT, TSL, CW);
+      const int base = TS / NSL;  // tokens per warp if every slice group took every stage
+      // Slice groups take 32 (else `base`) tokens of every ilv-th stage
+      // where such an instance is built (more independent MMA chains per
+      // warp, fewer softmax reductions per token); NSL / ilv slices per stage.
+      for (TSL = base < 32 ? 32 : base; TSL >= base; TSL /= 2) {
+        ilv = TSL / base;
+        if (TSL != 16 && TSL != 32 && TSL != 64) continue;
+        if (ilv > NSL || NSL % ilv) continue;
+        k = pick_kernel(kind, D, MT, TSL, CW);
+        if (k.fn) break;
+      }
     }
   }
   if (!k.fn) return false;
-  // fp8: where two slice groups would each take 16 tokens of every stage,
-  // they take all 32 tokens of every other stage instead (twice the
-  // independent MMA chains per warp, half the softmax reductions per token).
-  g->ilv = 1;
-  if (fp8 && TSL == 16 && (TS / TSL) % 2 == 0) {
-    const SplitKernel k2 = pick_kernel(kind, D, MT, 32, k.threads / 32 - 1);
-    if (k2.fn) {
-      k = k2;
-      TSL = 32;
-      g->ilv = 2;
-    }
-  }
+  g->ilv = ilv;
   g->GT = GT;
   g->H2 = H2;
   g->NHG = s->num_kv_heads / H2;
@@ -472,7 +481,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   }
 
   const SplitKernel k = geo.k;
-  if ((st = ensure_smem_attr(d, k.fn)) != PA_OK) return st;
+  if ((st = ensure_kernel_ready(d, k)) != PA_OK) return st;
   const dim3 grid = plan.balanced ? dim3(plan.grid) : dim3(B * geo.NHG, plan.splits);
   void* args[] = {&p};
   if (ev_start && cudaEventRecord(ev_start, a.stream) != cudaSuccess) return PA_ERR_CUDA;

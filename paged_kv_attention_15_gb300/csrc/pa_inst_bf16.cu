@@ -14,15 +14,20 @@ template <int D, int MT, int TSL, int CW = kConsumerWarps>
 static SplitKernel entry() {
   using C = Cfg<D, MT, false, TSL, CW>;
   return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, KVK, TSL, CW>), C::SMEM_FIXED, C::NS,
-                     C::THREADS};
+                     C::THREADS, C::REGSPLIT ? kSplitLaunchRegs : 0};
 }
 
 template <int D>
 static SplitKernel by_tiles(int row_tiles, int slice, int cw) {
   if constexpr (D == 128) {
-    // eight consumer warps, two per row tile splitting its tokens: the
-    // four-tile draft-block units (64 rows of two kv heads)
-    if (cw == 8) return row_tiles == 4 && slice == 16 ? entry<D, 4, 16, 8>() : SplitKernel{nullptr, 0, 0, 0};
+    // eight consumer warps, two per row tile: the four-tile draft-block
+    // units (64 query rows of one or two kv heads), in 16-token slices or
+    // (with the register split) 32-token slices
+    if (cw == 8) {
+      if (row_tiles == 4 && slice == 16) return entry<D, 4, 16, 8>();
+      if (row_tiles == 4 && slice == 32) return entry<D, 4, 32, 8>();
+      return SplitKernel{nullptr, 0, 0, 0};
+    }
   }
   if (cw != kConsumerWarps) return SplitKernel{nullptr, 0, 0, 0};
   if (row_tiles == 1 && slice == 16) return entry<D, 1, 16>();

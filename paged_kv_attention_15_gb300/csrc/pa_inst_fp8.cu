@@ -3,11 +3,11 @@
 
 namespace pa {
 
-template <int D, int MT, int TSL>
+template <int D, int MT, int TSL, int CW = kConsumerWarps>
 static SplitKernel entry() {
-  using C = Cfg<D, MT, true, TSL>;
-  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, kKvFp8, TSL, kConsumerWarps>),
-                     C::SMEM_FIXED, C::NS, C::THREADS};
+  using C = Cfg<D, MT, true, TSL, CW>;
+  return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, kKvFp8, TSL, CW>), C::SMEM_FIXED, C::NS,
+                     C::THREADS, C::REGSPLIT ? kSplitLaunchRegs : 0};
 }
 
 template <int D>

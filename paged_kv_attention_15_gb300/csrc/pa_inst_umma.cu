@@ -11,7 +11,7 @@ static SplitKernel uentry() {
   using C = UCfg<D, KV, GT, N>;
   if constexpr (C::FITS) {
     return SplitKernel{reinterpret_cast<const void*>(&pa_umma_kernel<D, KV, GT, N>), C::SMEM_FIXED, C::NRAW,
-                       kUThreads};
+                       kUThreads, kULaunchRegs};
   } else {
     return SplitKernel{nullptr, 0, 0, 0};
   }

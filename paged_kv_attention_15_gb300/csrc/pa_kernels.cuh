@@ -65,6 +65,15 @@ constexpr float kMaxSlack = 8.f;
 // stages before it uses them (and keeps one more slot for the stage in use).
 constexpr int kScaleAhead = 2;
 constexpr int kScaleRing = kScaleAhead + 1;
+// Eight consumer warps with long slices (or fp8): 12 warps launch at 168
+// registers (the limit of three warps on one SM sub-partition); the
+// producer's warpgroup (the producer and three idle warps) drops to 40 and
+// the two consumer warpgroups rise to 232, room for a 32-token score slice
+// next to the output rows with two consumer warps per sub-partition:
+// 2 x 128 x 232 + 128 x 40 = 384 x 168.
+constexpr int kSplitLaunchRegs = 168, kSplitConsumerRegs = 232, kSplitProducerRegs = 40;
+static_assert(2 * 128 * kSplitConsumerRegs + 128 * kSplitProducerRegs <= 384 * kSplitLaunchRegs,
+              "register split exceeds the launch pool");
 
 constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 constexpr int clamp_int(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
@@ -89,7 +98,7 @@ struct SplitParams {
   int NHG;         // head groups per sequence, Hkv / H2
   int GT;          // query rows per kv head, G * T
   int TS;          // tokens per stage, 64 / H2
-  int ilv;         // 1, or 2: slice group ts takes only the stages j with j % 2 == ts % 2
+  int ilv;         // 1, 2 or 4: slice group ts takes only the stages j with j % ilv == ts % ilv
   int BR, lbr;     // rows of a page box, min(P, TS), and its log2
   int TP;          // scratch rows per box: T rounded up to a multiple of 8
   int num_splits;  // >= 1: explicit splits (grid = units x splits); 0: balanced (grid = CTAs)
@@ -117,7 +126,8 @@ struct ReduceParams {
 // sub-partition and split each row tile's tokens).
 template <int D, int MT, bool FP8, int TSL, int CW = kConsumerWarps>
 struct Cfg {
-  static constexpr int THREADS = 32 * (CW + 1);  // + the producer warp
+  static constexpr bool REGSPLIT = CW == 8 && (FP8 || TSL >= 32);  // setmaxnreg layout (kSplitLaunchRegs)
+  static constexpr int THREADS = 32 * (CW + (REGSPLIT ? 4 : 1));  // + the producer warp (warpgroup)
   static constexpr int ELEM = FP8 ? 1 : 2;
   static constexpr int CE = 128 / ELEM;         // elements per 128-byte row chunk
   static constexpr int NCH = D * ELEM / 128;    // row chunks per KV row
@@ -129,7 +139,8 @@ struct Cfg {
   static constexpr int QCHUNK = ROWS * 128;
   static constexpr int QSLOT = QCH * QCHUNK;
   static constexpr int NGW = CW / MT;  // warps per row tile, each holding a partial result
-  static constexpr int RSTR = D + 8;               // floats per row of the merge buffer
+  static constexpr int CHW = D <= 128 ? D : 64;    // output columns per merge round
+  static constexpr int RSTR = CHW + 8;             // floats per row of the merge buffer
   static constexpr int RED = (NGW - 1) * ROWS * RSTR * 4;
   static constexpr int REDML = (NGW - 1) * ROWS * 2 * 4;
   static constexpr int BARS = 256;
@@ -337,7 +348,11 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
   const int TS = p.TS;
   // Bytes per key row of all H2 heads in a stage.
   const uint32_t row_bytes = H2 * D * C::ELEM;
-  if (warp == CW) {
+  if (warp >= CW) {
+    if constexpr (C::REGSPLIT) {
+      regs_dec<kSplitProducerRegs>();
+      if (warp != CW) return;  // the idle warps of the producer's warpgroup
+    }
     // ================================================================ producer
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
@@ -435,6 +450,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
   }
 
   // ================================================================ consumers
+  if constexpr (C::REGSPLIT) regs_inc<kSplitConsumerRegs>();
   // Warp w: row tile mt = w % MT; among the NGW warps of that tile, gi picks
   // the kv head hl (when a tile holds several heads' rows) and the token
   // slice ts of every stage (TSL tokens).
@@ -647,14 +663,16 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
               }
               const int unit = 4 * kq + (lane >> 3);  // 16-byte unit = k-step
               const uint32_t coff = (unit / 8) * cstride + (((unit % 8) ^ sw) << 4);
+              uint32_t kr[NTS][4];
 #pragma unroll
-              for (int nt = 0; nt < NTS; ++nt) {
-                uint32_t kr[4];
-                ldsm_x4(krow[nt] + coff, kr[0], kr[1], kr[2], kr[3]);
+              for (int nt = 0; nt < NTS; ++nt) ldsm_x4(krow[nt] + coff, kr[nt][0], kr[nt][1], kr[nt][2], kr[nt][3]);
+              // Consecutive MMAs go to different score tiles: NTS independent
+              // accumulation chains in flight instead of one.
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[e]), e4m3x2_to_f16x2(kr[e] >> 16));
-              }
+              for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int nt = 0; nt < NTS; ++nt)
+                  mma_f16(s[nt], qa[e], e4m3x2_to_f16x2(kr[nt][e]), e4m3x2_to_f16x2(kr[nt][e] >> 16));
             }
           }
 #pragma unroll
@@ -801,65 +819,86 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (NGW > 1) {
-      named_barrier_sync(1, 32 * CW);
-      if (gi > 0) {
-        float* rb = red + (size_t)(gi - 1) * C::ROWS * C::RSTR;
+    // Rounds of CHW output columns: the other warps of the tile write their
+    // columns (and, in the first round, their m and l), warp gi = 0 folds
+    // them into its own, each weighted by 2^(m_warp - M) / L.
+    float M0 = m0, M1 = m1, L0 = 0.f, L1 = 0.f, w00 = 1.f, w01 = 1.f, inv0 = 0.f, inv1 = 0.f;
+    float wq0[NGW > 1 ? NGW - 1 : 1], wq1[NGW > 1 ? NGW - 1 : 1];
+    auto merge_weights = [&]() {
 #pragma unroll
-        for (int i = 0; i < NT8; ++i) {
-          *reinterpret_cast<float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][0], acc[i][1]);
-          *reinterpret_cast<float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[i][2], acc[i][3]);
+      for (int q = 0; q < NGW - 1; ++q) {
+        M0 = fmaxf(M0, redml[(q * C::ROWS + rho0) * 2]);
+        M1 = fmaxf(M1, redml[(q * C::ROWS + rho1) * 2]);
+      }
+      const float Mu0 = M0 == NEG_INF ? 0.f : M0;
+      const float Mu1 = M1 == NEG_INF ? 0.f : M1;
+      w00 = ex2(m0 - Mu0);
+      w01 = ex2(m1 - Mu1);
+      L0 = w00 * l0;
+      L1 = w01 * l1;
+#pragma unroll
+      for (int q = 0; q < NGW - 1; ++q) {
+        wq0[q] = ex2(redml[(q * C::ROWS + rho0) * 2] - Mu0);
+        wq1[q] = ex2(redml[(q * C::ROWS + rho1) * 2] - Mu1);
+        L0 += wq0[q] * redml[(q * C::ROWS + rho0) * 2 + 1];
+        L1 += wq1[q] * redml[(q * C::ROWS + rho1) * 2 + 1];
+      }
+      inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
+      inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+    };
+    auto merge_columns = [&](int i0, int i1) {  // n8 tiles [i0, i1) of this round
+#pragma unroll
+      for (int i = i0; i < i1; ++i) {
+        float a0 = acc[i][0] * w00, a1 = acc[i][1] * w00, a2 = acc[i][2] * w01, a3 = acc[i][3] * w01;
+#pragma unroll
+        for (int q = 0; q < NGW - 1; ++q) {
+          const float* rb = red + (size_t)q * C::ROWS * C::RSTR + (i - i0) * 8 + 2 * c4;
+          const float2 x = *reinterpret_cast<const float2*>(rb + rho0 * C::RSTR);
+          const float2 y = *reinterpret_cast<const float2*>(rb + rho1 * C::RSTR);
+          a0 += wq0[q] * x.x;
+          a1 += wq0[q] * x.y;
+          a2 += wq1[q] * y.x;
+          a3 += wq1[q] * y.y;
         }
-        if (c4 == 0) {
-          float* ml = redml + (size_t)(gi - 1) * C::ROWS * 2;
-          ml[2 * rho0] = m0;
-          ml[2 * rho0 + 1] = l0;
-          ml[2 * rho1] = m1;
-          ml[2 * rho1 + 1] = l1;
+        acc[i][0] = a0 * inv0;
+        acc[i][1] = a1 * inv0;
+        acc[i][2] = a2 * inv1;
+        acc[i][3] = a3 * inv1;
+      }
+    };
+    if constexpr (NGW > 1) {
+#pragma unroll
+      for (int ck = 0; ck < D / C::CHW; ++ck) {
+        constexpr int NCT = C::CHW / 8;  // n8 tiles per round
+        named_barrier_sync(1, 32 * CW);  // the previous round's (or item's) reads are done
+        if (gi > 0) {
+          float* rb = red + (size_t)(gi - 1) * C::ROWS * C::RSTR;
+#pragma unroll
+          for (int i = 0; i < NCT; ++i) {
+            const int ia = ck * NCT + i;
+            *reinterpret_cast<float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[ia][0], acc[ia][1]);
+            *reinterpret_cast<float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4) = make_float2(acc[ia][2], acc[ia][3]);
+          }
+          if (ck == 0 && c4 == 0) {
+            float* ml = redml + (size_t)(gi - 1) * C::ROWS * 2;
+            ml[2 * rho0] = m0;
+            ml[2 * rho0 + 1] = l0;
+            ml[2 * rho1] = m1;
+            ml[2 * rho1 + 1] = l1;
+          }
+        }
+        named_barrier_sync(1, 32 * CW);
+        if (gi == 0) {
+          if (ck == 0) merge_weights();
+          merge_columns(ck * NCT, (ck + 1) * NCT);
         }
       }
-      named_barrier_sync(1, 32 * CW);
+    } else {
+      merge_weights();
+      merge_columns(0, NT8);
     }
     if (gi != 0) continue;
 
-    float M0 = m0, M1 = m1;
-#pragma unroll
-    for (int q = 0; q < NGW - 1; ++q) {
-      M0 = fmaxf(M0, redml[(q * C::ROWS + rho0) * 2]);
-      M1 = fmaxf(M1, redml[(q * C::ROWS + rho1) * 2]);
-    }
-    const float Mu0 = M0 == NEG_INF ? 0.f : M0;
-    const float Mu1 = M1 == NEG_INF ? 0.f : M1;
-    const float w00 = ex2(m0 - Mu0), w01 = ex2(m1 - Mu1);
-    float L0 = w00 * l0, L1 = w01 * l1;
-    float wq0[NGW > 1 ? NGW - 1 : 1], wq1[NGW > 1 ? NGW - 1 : 1];
-#pragma unroll
-    for (int q = 0; q < NGW - 1; ++q) {
-      wq0[q] = ex2(redml[(q * C::ROWS + rho0) * 2] - Mu0);
-      wq1[q] = ex2(redml[(q * C::ROWS + rho1) * 2] - Mu1);
-      L0 += wq0[q] * redml[(q * C::ROWS + rho0) * 2 + 1];
-      L1 += wq1[q] * redml[(q * C::ROWS + rho1) * 2 + 1];
-    }
-    const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
-    const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
-#pragma unroll
-    for (int i = 0; i < NT8; ++i) {
-      float a0 = acc[i][0] * w00, a1 = acc[i][1] * w00, a2 = acc[i][2] * w01, a3 = acc[i][3] * w01;
-#pragma unroll
-      for (int q = 0; q < NGW - 1; ++q) {
-        const float* rb = red + (size_t)q * C::ROWS * C::RSTR;
-        const float2 x = *reinterpret_cast<const float2*>(rb + rho0 * C::RSTR + i * 8 + 2 * c4);
-        const float2 y = *reinterpret_cast<const float2*>(rb + rho1 * C::RSTR + i * 8 + 2 * c4);
-        a0 += wq0[q] * x.x;
-        a1 += wq0[q] * x.y;
-        a2 += wq1[q] * y.x;
-        a3 += wq1[q] * y.y;
-      }
-      acc[i][0] = a0 * inv0;
-      acc[i][1] = a1 * inv0;
-      acc[i][2] = a2 * inv1;
-      acc[i][3] = a3 * inv1;
-    }
     float lse0 = L0 > 0.f ? (M0 + lg2(L0)) * kLn2 : NEG_INF;
     float lse1 = L1 > 0.f ? (M1 + lg2(L1)) * kLn2 : NEG_INF;
     // An item cut short by a timed-out wait (in this warp or another role of

@@ -11,7 +11,9 @@ struct SplitKernel {
   const void* fn;   // __global__ function, launched with cudaLaunchKernel
   int smem_fixed;   // dynamic shared memory without the per-sequence table
   int stages;       // pipeline depth of the instance
-  int threads;      // block size: 32 * (consumer warps + 1)
+  int threads;      // block size: 32 * (consumer warps + 1), or whole warpgroups
+  int launch_regs;  // kernels that move registers between warpgroups (setmaxnreg):
+                    // the registers per thread their split needs at launch; 0 otherwise
 };
 
 // Kernel instance for (head_dim, row tiles, tokens per warp slice,

@@ -101,6 +101,19 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, u
   }
 }
 
+// Per-thread register limit of the executing warpgroup (every warp of the
+// warpgroup executes the same one): inc waits until the CTA's pool, fixed at
+// launch as threads x launch registers, has the registers that another
+// warpgroup's dec returned.
+template <int R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

@@ -60,7 +60,8 @@ constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA
 // softmax 200, converters 104, producer/MMA warpgroup 96;
 // 200 * 128 + 104 * 256 + 96 * 128 = 64512 <= 65536.
 constexpr int kRegSoftmax = 200, kRegConv = 104, kRegOther = 96;
-static_assert(kRegSoftmax * 128 + kRegConv * 256 + kRegOther * 128 <= 65536, "register split");
+constexpr int kULaunchRegs = 65536 / kUThreads;  // registers per thread at launch (the pool the split draws on)
+static_assert(kRegSoftmax * 128 + kRegConv * 256 + kRegOther * 128 <= kUThreads * kULaunchRegs, "register split");
 
 template <int D, int KV, int GT, int N>
 struct UCfg {
@@ -184,15 +185,6 @@ __device__ __forceinline__ float redux_max(float x) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
   return r;
-}
-
-template <int R>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
-}
-template <int R>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
 
