@@ -79,7 +79,10 @@ APPEND_CONFIGS = ("append", "append_fp8", "append_step")
 APPEND_METRIC = "KV-cache append µs/call and achieved HBM GB/s (fraction of 8 TB/s) on 1 GB300"
 SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh"]
 UMMA_KERNEL_SOURCES = ["pa_umma.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
-KERNEL_NAMES = {1: "pa_split_kernel", 2: "pa_umma_kernel"}
+QROW_KERNEL_SOURCES = ["pa_qrow.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
+KERNEL_NAMES = {1: "pa_split_kernel", 2: "pa_umma_kernel", 3: "pa_qrow_kernel"}
+KERNEL_SOURCES = {"pa_split_kernel": SPLIT_KERNEL_SOURCES, "pa_umma_kernel": UMMA_KERNEL_SOURCES,
+                  "pa_qrow_kernel": QROW_KERNEL_SOURCES}
 APPEND_KERNEL_SOURCES = ["pa_append.cu", "pa_ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -144,8 +147,7 @@ def load_peak():
 def kernel_sha(config: str = DEFAULT_CONFIG, kernel: str = "pa_split_kernel") -> str:
     """Hash of the sources of the kernel a workload's roofline is about."""
     h = hashlib.sha256()
-    srcs = APPEND_KERNEL_SOURCES if config in APPEND_CONFIGS else (
-        UMMA_KERNEL_SOURCES if kernel == "pa_umma_kernel" else SPLIT_KERNEL_SOURCES)
+    srcs = APPEND_KERNEL_SOURCES if config in APPEND_CONFIGS else KERNEL_SOURCES[kernel]
     for name in srcs:
         with open(os.path.join(ROOT, "paged_kv_attention_15_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
@@ -475,7 +477,8 @@ def run_ours(args, world, rank, local):
     spec = workload_spec(args)
     host = gen.make_inputs(spec)
     pb.lib()
-    pb.set_kernel_path({"auto": pb.KERNEL_AUTO, "warp": pb.KERNEL_WARP_MMA, "tcgen05": pb.KERNEL_TCGEN05}[args.kernel_path])
+    pb.set_kernel_path({"auto": pb.KERNEL_AUTO, "warp": pb.KERNEL_WARP_MMA, "tcgen05": pb.KERNEL_TCGEN05,
+                        "tcgen05-qrow": pb.KERNEL_TCGEN05_QROW}[args.kernel_path])
     sets = [host.to(dev), host.to(dev)]  # alternated: each step reads KV not in L2
     kname = KERNEL_NAMES[pb.kernel_for_inputs(sets[0])]
     shape = pb.make_shape(sets[0].q, sets[0].k_cache, sets[0].block_tables)
@@ -925,8 +928,9 @@ def main(argv=None):
     ap.add_argument("--kernel-steps", type=int, default=300,
                     help="eager calls timed for the dominant kernel alone (independent of --steps)")
     ap.add_argument("--cpu-workers", type=int, default=0, help="oracle processes for the all-cores run (0: all)")
-    ap.add_argument("--kernel-path", default="auto", choices=["auto", "warp", "tcgen05"],
-                    help="split kernel: automatic choice, the warp-level MMA kernel, or the tcgen05 kernel")
+    ap.add_argument("--kernel-path", default="auto", choices=["auto", "warp", "tcgen05", "tcgen05-qrow"],
+                    help="split kernel: automatic choice, the warp-level MMA kernel, or one of the tcgen05 "
+                         "kernels (token-major, query-row-major)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -283,19 +283,22 @@ def device_error() -> int:
     return int(v.value)
 
 
-KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05 = 0, 1, 2
+# Decode kernels: automatic, the warp-level MMA kernel, the token-major
+# tcgen05 kernel, the query-row-major tcgen05 kernel (16-bit, 64-row units).
+KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05, KERNEL_TCGEN05_QROW = 0, 1, 2, 3
 _FORMATS = {"bf16": 0, "fp8": 1, "f16": 2, "draft": 3}
 
 
 def set_kernel_path(path: int) -> None:
-    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_WARP_MMA or KERNEL_TCGEN05
-    (see pa_decode_set_kernel_path)."""
+    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05
+    or KERNEL_TCGEN05_QROW (see pa_decode_set_kernel_path)."""
     _check(lib().pa_decode_set_kernel_path(int(path)), "pa_decode_set_kernel_path")
 
 
 def kernel_for(shape: PaShape, fmt: str) -> int:
-    """1 (warp-level MMA kernel) or 2 (tcgen05 kernel) for a decode of this
-    shape and format ('bf16', 'fp8', 'f16', 'draft'); -1 if unsupported."""
+    """The kernel (KERNEL_WARP_MMA, KERNEL_TCGEN05 or KERNEL_TCGEN05_QROW) a
+    decode of this shape and format ('bf16', 'fp8', 'f16', 'draft') runs;
+    -1 if unsupported."""
     return int(lib().pa_decode_kernel_for(ctypes.byref(shape), _FORMATS[fmt]))
 
 

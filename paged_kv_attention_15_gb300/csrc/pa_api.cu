@@ -167,16 +167,21 @@ SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL, int CW) {
 
 // Work-unit geometry: H2 kv heads per CTA unit, their M = H2 * G * T query
 // rows in MT m16 tiles, TS = 64 / H2 tokens per stage, TSL tokens per warp.
-// tcgen05 kernel (umma): M = N rows, TS = 128 / H2 tokens per stage.
+// Token-major tcgen05 kernel: M = N rows, TS = 128 / H2 tokens per stage.
+// Query-row-major tcgen05 kernel: M = 64 rows, TS = 64 / H2.
 struct Geom {
   int GT, H2, NHG, M, MT, TS, TSL, BR, lbr, TP, ilv;
-  bool umma;
+  int path;          // kernel: kPathWarp, kPathUmma or kPathQrow
+  int chunk_boxes;   // 1: one copy per page and 128-byte column chunk (query-row kernel)
   SplitKernel k;
 };
 
-// Which decode kernel a call may use: 0 automatic, 1 the warp-level MMA
-// kernel only, 2 the tcgen05 kernel wherever an instance exists.
-std::atomic<int> g_kernel_path{0};
+// Decode kernels (pa_decode_set_kernel_path / pa_decode_kernel_for).
+constexpr int kPathAuto = 0, kPathWarp = 1, kPathUmma = 2, kPathQrow = 3;
+
+// Which decode kernel a call may use: automatic, the warp-level MMA kernel
+// only, or one of the tcgen05 kernels wherever it has an instance.
+std::atomic<int> g_kernel_path{kPathAuto};
 
 int ilog2(int x) {
   int l = 0;
@@ -227,7 +232,8 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   g->H2 = H2;
   g->NHG = s->num_kv_heads / H2;
   g->M = M;
-  g->umma = false;
+  g->path = kPathWarp;
+  g->chunk_boxes = 0;
   g->MT = MT;
   g->TS = TS;
   g->TSL = TSL;
@@ -264,26 +270,59 @@ bool geom_umma(const pa_shape* s, Kind kind, Geom* g) {
     g->lbr = ilog2(g->BR);
     g->TP = TP;
     g->ilv = 1;
-    g->umma = true;
+    g->path = kPathUmma;
+    g->chunk_boxes = 0;
     g->k = k;
     return true;
   }
   return false;
 }
 
-// Automatic choice: the warp-level kernel (measured faster on every
-// workload so far); the tcgen05 kernel on request.
-bool want_umma(const pa_shape* s, Kind kind) {
-  (void)s;
-  (void)kind;
-  return g_kernel_path.load(std::memory_order_relaxed) == 2;
+// Query-row-major tcgen05 kernel geometry: 16-bit caches, D = 128, units of
+// 64 query rows (two kv heads of G * T = 32 rows, or one of 64); stages of
+// 64 key rows in page boxes of at least 16 rows; the draft scratch in one
+// box whose key rows fill whole 16-row MMA steps.
+bool geom_qrow(const pa_shape* s, Kind kind, Geom* g) {
+  if (kind == Kind::kFp8) return false;
+  const int G = s->num_q_heads / s->num_kv_heads, T = s->q_tokens, P = s->page_size, D = s->head_dim;
+  const int GT = G * T;
+  const int H2 = GT == 32 ? 2 : (GT == 64 ? 1 : 0);
+  if (H2 == 0 || s->num_kv_heads % H2) return false;
+  const int TS = 64 / H2, BR = P < TS ? P : TS;
+  if (BR < 16) return false;
+  int TP = (T + 15) / 16 * 16;
+  if (H2 == 2 && T <= 8) TP = 8;
+  if (kind == Kind::kTidar && TP * H2 > 64) return false;
+  const SplitKernel k = pa::qrow_kernel_16(D, kind == Kind::kF16, H2);
+  if (!k.fn) return false;
+  g->GT = GT;
+  g->H2 = H2;
+  g->NHG = s->num_kv_heads / H2;
+  g->M = 64;
+  g->MT = 0;
+  g->TS = TS;
+  g->TSL = 0;
+  g->BR = BR;
+  g->lbr = ilog2(BR);
+  g->TP = TP;
+  g->ilv = 1;
+  g->path = kPathQrow;
+  g->chunk_boxes = 1;
+  g->k = k;
+  return true;
 }
+
+// Automatic choice: the warp-level kernel (measured faster on every
+// workload so far); a tcgen05 kernel on request.
+int wanted_path() { return g_kernel_path.load(std::memory_order_relaxed); }
 
 // One kv head per unit, or more while a page's box stays under 16 KB: a
 // 16-row page of one head is a 4 KB copy, too small to keep enough bytes in
 // flight per SM.
 pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out) {
-  if (want_umma(s, kind) && geom_umma(s, kind, out)) return PA_OK;
+  const int want = wanted_path();
+  if (want == kPathUmma && geom_umma(s, kind, out)) return PA_OK;
+  if (want == kPathQrow && geom_qrow(s, kind, out)) return PA_OK;
   Geom best;
   if (!geom_for(s, kind, 1, &best)) return PA_ERR_UNSUPPORTED;
   const int e = kind == Kind::kFp8 ? 1 : 2;
@@ -424,13 +463,15 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   }
   // KV caches as 5-D (128-byte column chunk, slot, kv head, chunk index,
   // page): one box copies every chunk of BR rows of one page for the H2
-  // heads of a unit, landing in shared memory as [chunk][head][row][128 B].
+  // heads of a unit, landing in shared memory as [chunk][head][row][128 B]
+  // (or, for the query-row kernel, one chunk per box: [head][row][128 B]).
   const Geom& geo = plan.geo;
   const uint64_t nch = (uint64_t)D * e / 128;
+  const uint32_t box_ch = geo.chunk_boxes ? 1u : (uint32_t)nch;
   {
     const uint64_t dims[5] = {128 / e, (uint64_t)P, (uint64_t)Hkv, nch, (uint64_t)s.num_pages};
     const uint64_t str[4] = {(uint64_t)Hkv * D * e, (uint64_t)D * e, 128, (uint64_t)P * Hkv * D * e};
-    const uint32_t box[5] = {(uint32_t)(128 / e), (uint32_t)geo.BR, (uint32_t)geo.H2, (uint32_t)nch, 1u};
+    const uint32_t box[5] = {(uint32_t)(128 / e), (uint32_t)geo.BR, (uint32_t)geo.H2, box_ch, 1u};
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : (a.kind == Kind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
@@ -441,7 +482,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     // Rows T..TP-1 of the box fall outside the tensor and read as zeros.
     const uint64_t dims[5] = {64, (uint64_t)T, (uint64_t)Hkv, nch, (uint64_t)B};
     const uint64_t str[4] = {(uint64_t)Hkv * D * 2, (uint64_t)D * 2, 128, (uint64_t)T * Hkv * D * 2};
-    const uint32_t box[5] = {64u, (uint32_t)geo.TP, (uint32_t)geo.H2, (uint32_t)nch, 1u};
+    const uint32_t box[5] = {64u, (uint32_t)geo.TP, (uint32_t)geo.H2, box_ch, 1u};
     if (!make_map(&p.tm_ks, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k_scratch, dims, str, box) ||
         !make_map(&p.tm_vs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v_scratch, dims, str, box))
       return PA_ERR_INVALID_ARG;
@@ -725,7 +766,7 @@ pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
 }
 
 pa_status pa_decode_set_kernel_path(int32_t path) {
-  if (path < 0 || path > 2) return PA_ERR_INVALID_ARG;
+  if (path < kPathAuto || path > kPathQrow) return PA_ERR_INVALID_ARG;
   g_kernel_path.store(path, std::memory_order_relaxed);
   return PA_OK;
 }
@@ -736,7 +777,7 @@ int32_t pa_decode_kernel_for(const pa_shape* shape, int32_t format) {
   if (check_shape(shape, kind) != PA_OK) return -1;
   Geom g;
   if (pick_geometry(shape, kind, &g) != PA_OK) return -1;
-  return g.umma ? 2 : 1;
+  return g.path;
 }
 
 pa_status pa_decode_profile_events(void* start_event, void* split_done_event) {

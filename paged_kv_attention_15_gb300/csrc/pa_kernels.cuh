@@ -270,6 +270,136 @@ __device__ __forceinline__ void raise_abort(volatile int* s_abort, int* err_flag
   atomicOr(err_flags, kErrWaitTimeout);
 }
 
+// Shared-memory ring that a producer warp fills: NS stages of `stage` bytes
+// from sbase (each the K tile, then the V tile `tile` bytes further), and two
+// Q slots of `qslot` bytes from sbase + off_q, each QCH column chunks of
+// `qchunk` bytes. A stage tile is [page box][chunk][head][box row][128 B],
+// or, with chunk_stride != 0 (one copy per page and chunk),
+// [chunk][page box][head][box row][128 B] with chunks chunk_stride apart.
+struct RingGeom {
+  uint32_t sbase, off_q, qslot, qchunk, stage, tile;
+  int ns, qch, nch;
+  uint32_t row_bytes;     // bytes of one key row of all H2 heads
+  uint32_t chunk_stride;  // 0: a box holds every chunk of its rows
+};
+
+// The producer warp of the split kernels: walks this CTA's work items and,
+// per item, copies the Q rows of its H2 kv heads into a Q slot and every
+// stage's K and V page boxes into the ring (one box per page, or the
+// stage's rows of one page; the draft-token scratch as the last stage of
+// its sequence's last item), after the consumers released the slot. Raises
+// the abort flag on a timed-out wait and returns once every copy it issued
+// has landed.
+static __device__ __forceinline__ void produce_ring(const SplitParams& p, const int* s_ctx, const int* s_start,
+                                                 const RingGeom& g, uint32_t bar_full, uint32_t bar_empty,
+                                                 uint32_t bar_qfull, uint32_t bar_qempty, volatile int* s_abort,
+                                                 int lane) {
+  const uint32_t sbase = g.sbase;
+  const int P = p.P;
+  const int H2 = p.H2;
+  const int TS = p.TS;
+  const uint32_t row_bytes = g.row_bytes;
+  const uint64_t pol_kv = l2_policy_evict_first();
+  const uint64_t pol_q = l2_policy_evict_last();
+  if (lane == 0) {
+    prefetch_tensormap(&p.tm_q);
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+  }
+  Cursor cur;
+  cursor_init(p, s_start, cur);
+  Item it;
+  int stage = 0, qn = 0;
+  uint32_t filled = 0, fill_parity = 0;
+  bool ok = true;
+  while (ok && next_item(p, s_ctx, s_start, cur, it)) {
+    if (it.nst == 0) continue;
+    const int qs = qn & 1;
+    // Warp-uniform verdicts: the lanes leave the loops together.
+    if (qn >= 2) ok = __all_sync(0xffffffffu, mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort));
+    if (!ok) break;
+    if (lane == 0) {
+      // Rows of kv head hl occupy rows [hl*GT, (hl+1)*GT) of each chunk.
+      const uint32_t qdst = sbase + g.off_q + qs * g.qslot;
+      mbar_arrive_expect_tx(bar_qfull + 8 * qs, g.qch * p.M * 128);
+      for (int hl = 0; hl < H2; ++hl)
+#pragma unroll
+        for (int c = 0; c < g.qch; ++c)
+          tma_load_4d(qdst + c * g.qchunk + hl * p.GT * 128, &p.tm_q, bar_qfull + 8 * qs, c * 64,
+                      (it.hg * H2 + hl) * p.G, 0, it.b, pol_q);
+    }
+    ++qn;
+
+    const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
+    const int pbase = it.tok0 / P;
+    const int npages = it.tok_end > it.tok0 ? (it.tok_end - 1) / P + 1 - pbase : 0;
+    int ibase = 0;
+    int ids = lane < npages ? __ldg(bt_row + pbase + lane) : 0;
+    int ids_next = 32 + lane < npages ? __ldg(bt_row + pbase + 32 + lane) : 0;
+    for (int j = 0; j < it.nst; ++j, ++stage) {
+      const int slot = stage % g.ns;
+      if (stage >= g.ns) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * slot, ((stage / g.ns) - 1) & 1, kWaitLimitNs, s_abort));
+        if (!ok) break;
+      }
+      filled |= 1u << slot;
+      fill_parity = (fill_parity & ~(1u << slot)) | (uint32_t((stage / g.ns) & 1) << slot);
+      const uint32_t full = bar_full + 8 * slot;
+      const uint32_t kdst = sbase + slot * g.stage;
+      const uint32_t vdst = kdst + g.tile;
+      const int ncb = g.chunk_stride ? g.nch : 1;  // copies per box: one per chunk, or one
+      if (it.scratch && j == it.nst - 1) {
+        if (lane == 0) {  // rows T..TP-1 of the box are outside the tensor: zero filled
+          mbar_arrive_expect_tx(full, 2 * g.nch * H2 * p.TP * 128);
+          for (int c = 0; c < ncb; ++c) {
+            tma_load_5d(kdst + c * g.chunk_stride, &p.tm_ks, full, 0, 0, it.hg * H2, c, it.b, pol_kv);
+            tma_load_5d(vdst + c * g.chunk_stride, &p.tm_vs, full, 0, 0, it.hg * H2, c, it.b, pol_kv);
+          }
+        }
+        continue;
+      }
+      const int t_first = it.tok0 + j * TS;
+      const int valid = min(TS, it.tok_end - t_first);
+      const int pidx0 = t_first / P - pbase;  // page of the stage, relative to the item
+      while (pidx0 >= ibase + 32) {           // advance the block-table window
+        ibase += 32;
+        ids = ids_next;
+        ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
+      }
+      if (P < TS) {  // whole pages: one box each
+        const int npg = (valid + P - 1) / P;
+        if (lane == 0) mbar_arrive_expect_tx(full, 2 * npg * P * row_bytes);
+        for (int i = 0; i < npg; ++i) {
+          const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase + i);
+          if (lane == 0) {
+            const uint32_t boff = i * (g.chunk_stride ? 1 : g.nch) * H2 * P * 128;
+            for (int c = 0; c < ncb; ++c) {
+              tma_load_5d(kdst + c * g.chunk_stride + boff, &p.tm_k, full, 0, 0, it.hg * H2, c, page, pol_kv);
+              tma_load_5d(vdst + c * g.chunk_stride + boff, &p.tm_v, full, 0, 0, it.hg * H2, c, page, pol_kv);
+            }
+          }
+        }
+      } else {  // TS rows of one page
+        const int row0 = t_first % P;
+        const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, 2 * TS * row_bytes);
+          for (int c = 0; c < ncb; ++c) {
+            tma_load_5d(kdst + c * g.chunk_stride, &p.tm_k, full, 0, row0, it.hg * H2, c, page, pol_kv);
+            tma_load_5d(vdst + c * g.chunk_stride, &p.tm_v, full, 0, row0, it.hg * H2, c, page, pol_kv);
+          }
+        }
+      }
+    }
+  }
+  // Near the end of this CTA's work: the split-K reduce may be scheduled
+  // (it waits for this grid to complete before reading any partial).
+  launch_dependents();
+  if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
+  // Let every copy this warp issued land before the CTA can exit.
+  drain_copies(bar_full, bar_qfull, g.ns, filled, fill_parity, qn);
+}
+
 // ------------------------------------------------------------ split kernel
 // KV element kinds of the split kernel: bf16 (q, caches, out bf16), fp8
 // (e4m3fn caches with scales; q and out bf16), f16 (q, caches, out f16).
@@ -353,99 +483,9 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
       regs_dec<kSplitProducerRegs>();
       if (warp != CW) return;  // the idle warps of the producer's warpgroup
     }
-    // ================================================================ producer
-    const uint64_t pol_kv = l2_policy_evict_first();
-    const uint64_t pol_q = l2_policy_evict_last();
-    if (lane == 0) {
-      prefetch_tensormap(&p.tm_q);
-      prefetch_tensormap(&p.tm_k);
-      prefetch_tensormap(&p.tm_v);
-    }
-    Cursor cur;
-    cursor_init(p, s_start, cur);
-    Item it;
-    int stage = 0, qn = 0;
-    uint32_t filled = 0, fill_parity = 0;
-    bool ok = true;
-    while (ok && next_item(p, s_ctx, s_start, cur, it)) {
-      if (it.nst == 0) continue;
-      const int qs = qn & 1;
-      // Warp-uniform verdicts: the lanes leave the loops together.
-      if (qn >= 2) ok = __all_sync(0xffffffffu, mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort));
-      if (!ok) break;
-      if (lane == 0) {
-        // Rows of kv head hl occupy rows [hl*GT, (hl+1)*GT) of each chunk.
-        const uint32_t qdst = sbase + C::OFF_Q + qs * C::QSLOT;
-        mbar_arrive_expect_tx(bar_qfull + 8 * qs, C::QCH * p.M * 128);
-        for (int hl = 0; hl < H2; ++hl)
-#pragma unroll
-          for (int c = 0; c < C::QCH; ++c)
-            tma_load_4d(qdst + c * C::QCHUNK + hl * p.GT * 128, &p.tm_q, bar_qfull + 8 * qs, c * 64,
-                        (it.hg * H2 + hl) * p.G, 0, it.b, pol_q);
-      }
-      ++qn;
-
-      const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
-      const int pbase = it.tok0 / P;
-      const int npages = it.tok_end > it.tok0 ? (it.tok_end - 1) / P + 1 - pbase : 0;
-      int ibase = 0;
-      int ids = lane < npages ? __ldg(bt_row + pbase + lane) : 0;
-      int ids_next = 32 + lane < npages ? __ldg(bt_row + pbase + 32 + lane) : 0;
-      for (int j = 0; j < it.nst; ++j, ++stage) {
-        const int slot = stage % NS;
-        if (stage >= NS) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * slot, ((stage / NS) - 1) & 1, kWaitLimitNs, s_abort));
-          if (!ok) break;
-        }
-        filled |= 1u << slot;
-        fill_parity = (fill_parity & ~(1u << slot)) | (uint32_t((stage / NS) & 1) << slot);
-        const uint32_t full = bar_full + 8 * slot;
-        const uint32_t kdst = sbase + slot * C::STAGE;
-        const uint32_t vdst = kdst + C::TILE;
-        if (it.scratch && j == it.nst - 1) {
-          if (lane == 0) {  // rows T..TP-1 of the box are outside the tensor: zero filled
-            mbar_arrive_expect_tx(full, 2 * NCH * H2 * p.TP * 128);
-            tma_load_5d(kdst, &p.tm_ks, full, 0, 0, it.hg * H2, 0, it.b, pol_kv);
-            tma_load_5d(vdst, &p.tm_vs, full, 0, 0, it.hg * H2, 0, it.b, pol_kv);
-          }
-          continue;
-        }
-        const int t_first = it.tok0 + j * TS;
-        const int valid = min(TS, it.tok_end - t_first);
-        const int pidx0 = t_first / P - pbase;  // page of the stage, relative to the item
-        while (pidx0 >= ibase + 32) {           // advance the block-table window
-          ibase += 32;
-          ids = ids_next;
-          ids_next = ibase + 32 + lane < npages ? __ldg(bt_row + pbase + ibase + 32 + lane) : 0;
-        }
-        if (P < TS) {  // whole pages: one box each
-          const int npg = (valid + P - 1) / P;
-          if (lane == 0) mbar_arrive_expect_tx(full, 2 * npg * P * row_bytes);
-          for (int i = 0; i < npg; ++i) {
-            const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase + i);
-            if (lane == 0) {
-              const uint32_t boff = i * NCH * H2 * P * 128;
-              tma_load_5d(kdst + boff, &p.tm_k, full, 0, 0, it.hg * H2, 0, page, pol_kv);
-              tma_load_5d(vdst + boff, &p.tm_v, full, 0, 0, it.hg * H2, 0, page, pol_kv);
-            }
-          }
-        } else {  // TS rows of one page
-          const int row0 = t_first % P;
-          const int page = __shfl_sync(0xffffffffu, ids, pidx0 - ibase);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(full, 2 * TS * row_bytes);
-            tma_load_5d(kdst, &p.tm_k, full, 0, row0, it.hg * H2, 0, page, pol_kv);
-            tma_load_5d(vdst, &p.tm_v, full, 0, row0, it.hg * H2, 0, page, pol_kv);
-          }
-        }
-      }
-    }
-    // Near the end of this CTA's work: the split-K reduce may be scheduled
-    // (it waits for this grid to complete before reading any partial).
-    launch_dependents();
-    if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
-    // Let every copy this warp issued land before the CTA can exit.
-    drain_copies(bar_full, bar_qfull, NS, filled, fill_parity, qn);
+    const RingGeom g{sbase, (uint32_t)C::OFF_Q, (uint32_t)C::QSLOT, (uint32_t)C::QCHUNK, (uint32_t)C::STAGE,
+                     (uint32_t)C::TILE, NS, C::QCH, NCH, row_bytes, 0u};
+    produce_ring(p, s_ctx, s_start, g, bar_full, bar_empty, bar_qfull, bar_qempty, s_abort, lane);
     return;
   }
 

@@ -117,6 +117,38 @@ def test_choose_splits_rejects_bad_shapes(lib):
     assert lib.pa_decode_choose_splits(ctypes.byref(shape(q_tokens=0)), 0) == -1
 
 
+def test_kernel_choice_per_path(lib):
+    """Host-only kernel choice: the warp-level kernel by default; with a
+    tcgen05 path forced, the shapes that kernel covers run it and the others
+    keep the warp-level kernel; invalid paths are rejected."""
+    bf16, fp8, f16, draft = 0, 1, 2, 3
+    qrow_shapes = [  # (shape, format): 64 query rows per unit, D = 128, 16-bit
+        (shape(q_tokens=8, num_q_heads=32, num_kv_heads=8, num_pages=400, max_blocks_per_seq=100), draft),
+        (shape(q_tokens=16, num_q_heads=32, num_kv_heads=8, num_pages=400, max_blocks_per_seq=100), draft),
+        (shape(q_tokens=1, num_q_heads=64, num_kv_heads=2), bf16),
+        (shape(q_tokens=1, num_q_heads=64, num_kv_heads=1), f16),
+    ]
+    other = [
+        (shape(), bf16),                                              # G * T = 4
+        (shape(q_tokens=1, num_q_heads=64, num_kv_heads=2), fp8),     # fp8
+        (shape(q_tokens=1, num_q_heads=64, num_kv_heads=2, head_dim=64), bf16),   # D = 64
+        (shape(q_tokens=3, num_q_heads=16, num_kv_heads=1), draft),   # 48 rows per kv head
+        (shape(q_tokens=1, num_q_heads=32, num_kv_heads=1), bf16),    # G = 32 with one kv head: no pair
+    ]
+    try:
+        for s, fmt in qrow_shapes + other:
+            assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_MMA
+        pb.set_kernel_path(pb.KERNEL_TCGEN05_QROW)
+        for s, fmt in qrow_shapes:
+            assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_TCGEN05_QROW
+        for s, fmt in other:
+            assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_MMA
+        assert lib.pa_decode_set_kernel_path(4) == pb.PA_ERR_INVALID_ARG
+        assert lib.pa_decode_set_kernel_path(-1) == pb.PA_ERR_INVALID_ARG
+    finally:
+        pb.set_kernel_path(pb.KERNEL_AUTO)
+
+
 def test_append_validation(lib):
     def call(s, fp8=False, **kw):
         a = dict(kn=FAKE, vn=FAKE, bt=FAKE, cl=FAKE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE)

@@ -202,7 +202,8 @@ LONG_ROWS = [
 
 
 # Shapes whose units could hold 128 query rows (4 kv heads x 32 rows, 2 x 64):
-# the units stay at 64 rows (four tiles, one per warp)
+# the units stay at 64 rows (four tiles; measured faster per call than
+# 128-row units, whose larger page boxes leave more partials to combine)
 EIGHT_TILES = [
     (dict(draft_scratch=True, q_tokens=8, num_q_heads=16, num_kv_heads=4), None),
     (dict(draft_scratch=True, q_tokens=8, num_q_heads=16, num_kv_heads=4, context_lens=(0, 31, 260, 16)), 3),
@@ -210,6 +211,12 @@ EIGHT_TILES = [
     (dict(q_tokens=4, num_q_heads=32, num_kv_heads=4), None),
     (dict(draft_scratch=True, q_tokens=8, num_q_heads=32, num_kv_heads=8), 1),
     (dict(kv_format="f16", q_tokens=4, num_q_heads=32, num_kv_heads=4), None),
+    (dict(draft_scratch=True, q_tokens=16, num_q_heads=16, num_kv_heads=4), 4),      # 2 heads x 64 rows
+    (dict(draft_scratch=True, q_tokens=16, num_q_heads=16, num_kv_heads=4, page_size=32,
+          context_lens=(32, 33, 1, 500)), 4),
+    (dict(draft_scratch=True, q_tokens=8, num_q_heads=16, num_kv_heads=4, page_size=64,
+          context_lens=(64, 65, 2, 700)), 2),
+    (dict(q_tokens=1, num_q_heads=128, num_kv_heads=4, context_lens=(0, 7, 129, 1000)), None),  # G 32, no draft
 ]
 
 
