@@ -154,8 +154,10 @@ __global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_co
   combine_row(
       i1 - i0 + 1, D, [&](int k) { return po + ((size_t)(u + i0 + k) * M + rho) * D; },
       [&](int k) {
-        const long long i = i0 + k;  // a CTA whose share is empty wrote nothing
-        return (N * i / G64) < (N * (i + 1) / G64) ? __ldcg(pl + (size_t)(u + i) * M + rho) : NEG_INF;
+        // A CTA whose share is empty wrote nothing; with at least as many
+        // flattened pages as CTAs every share holds a page.
+        const long long i = i0 + k;
+        return (N >= G64 || (N * i / G64) < (N * (i + 1) / G64)) ? __ldcg(pl + (size_t)(u + i) * M + rho) : NEG_INF;
       },
       p.out + row * D, p.lse ? p.lse + row : nullptr, lane, p.out_f16 != 0);
 }
