@@ -105,8 +105,9 @@ typedef struct pa_shape {
 
 /* Bytes of workspace pa_decode* needs for this shape and num_splits (0 for
  * num_splits == 1). For num_splits == 0 the size is the largest over every
- * decode entry point (bf16, f16, fp8, draft block) and depends on the
- * current device's SM count: size it on the device that will run the call
+ * decode entry point (bf16, f16, fp8, draft block) and every kernel
+ * selection (pa_decode_set_kernel_path), and depends on the current
+ * device's SM count: size it on the device that will run the call
  * (another GPU model may need more and would return PA_ERR_WORKSPACE).
  * Returns 0 as well for an invalid shape. */
 size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits);
@@ -119,8 +120,9 @@ size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits);
  * S >= 1 it falls back to when the per-sequence table does not fit in
  * shared memory (S = ceil(2 * SMs / (B * kv head groups)), at most
  * max_blocks_per_seq). Returns -1 for an invalid or unsupported shape, or
- * when no CUDA device is usable. The split scheduler of the north-star
- * problem statement: the grid fills the SMs. */
+ * when no CUDA device is usable. This is the split scheduler behind
+ * num_splits = 0 (the MSLK pull request's review: "num_splits: int = 0"):
+ * the grid fills the SMs. */
 int32_t pa_decode_choose_splits(const pa_shape* shape, int32_t fp8_kv);
 
 /* Dense bf16 paged decode (the MSLK page's dense decode kernel).

@@ -319,8 +319,8 @@ int wanted_path() { return g_kernel_path.load(std::memory_order_relaxed); }
 // One kv head per unit, or more while a page's box stays under 16 KB: a
 // 16-row page of one head is a 4 KB copy, too small to keep enough bytes in
 // flight per SM.
-pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out) {
-  const int want = wanted_path();
+pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out, int path = -1) {
+  const int want = path >= 0 ? path : wanted_path();
   if (want == kPathUmma && geom_umma(s, kind, out)) return PA_OK;
   if (want == kPathQrow && geom_qrow(s, kind, out)) return PA_OK;
   Geom best;
@@ -347,9 +347,10 @@ struct Plan {
   size_t part_lse_off = 0;
 };
 
-pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d, Plan* plan) {
+// path: the kernel selection to plan for (-1: the current setting).
+pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d, Plan* plan, int path = -1) {
   Geom geo;
-  pa_status st = pick_geometry(s, kind, &geo);
+  pa_status st = pick_geometry(s, kind, &geo, path);
   if (st != PA_OK) return st;
   const SplitKernel k = geo.k;
   const int B = s->batch, T = s->q_tokens, Hq = s->num_q_heads, D = s->head_dim;
@@ -591,14 +592,18 @@ size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits) {
   }
   DeviceState* d = nullptr;
   if (device_state(&d) != PA_OK) return 0;
-  // The balanced plan depends on the kind through the instance's fixed
-  // shared memory and the draft block's extra page; take the largest plan
-  // over every decode entry point.
+  // The balanced plan depends on the kind and the kernel (through the
+  // instance's fixed shared memory, its rows per unit and the draft block's
+  // extra page); take the largest plan over every decode entry point and
+  // every kernel selection, so that the size holds whatever
+  // pa_decode_set_kernel_path chooses.
   size_t best = 0;
   for (Kind kind : {Kind::kBf16, Kind::kF16, Kind::kFp8, Kind::kTidar}) {
     if (check_shape(shape, kind) != PA_OK) continue;
-    Plan plan;
-    if (make_plan(shape, kind, 0, d, &plan) == PA_OK && plan.ws_bytes > best) best = plan.ws_bytes;
+    for (int path : {kPathWarp, kPathUmma, kPathQrow}) {
+      Plan plan;
+      if (make_plan(shape, kind, 0, d, &plan, path) == PA_OK && plan.ws_bytes > best) best = plan.ws_bytes;
+    }
   }
   return best;
 }

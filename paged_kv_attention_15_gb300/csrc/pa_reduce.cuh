@@ -9,33 +9,39 @@
 namespace pa {
 
 // ------------------------------------------------------------ row combine
+// Pieces whose loads a warp keeps in flight at once. Four rather than
+// eight keeps the kernels at most 64 registers (eight resident CTAs per SM):
+// a row has two or three pieces at the benchmark workloads, and a launch of
+// several thousand four-row CTAs then runs in one wave.
+constexpr int kCombineGroup = 4;
 // One warp combines the pieces k = 0..np-1 of one query row: M = max_k lse_k,
 // w_k = exp(lse_k - M), out = sum_k w_k o_k / sum_k w_k, lse = M + ln sum_k w_k,
 // in one online pass (running max, sums rescaled when it grows) that keeps
-// the loads of eight pieces in flight. Pieces with lse = -inf weigh 0; a row
+// the loads of KG pieces in flight. Pieces with lse = -inf weigh 0; a row
 // whose pieces are all empty gets out = 0, lse = -inf; a piece whose lse is
 // NaN (its work was cut short by a timed-out wait) makes the row NaN.
-// o_row(k) points at piece k's D (<= 256) floats in global memory, read
-// past L1 (other CTAs of the same grid may have written them); l_val(k) is
-// its lse. Lane l owns columns 4l..4l+3 and 128+4l..128+4l+3. Source: the
+// o_row(k) points at piece k's D (<= 256; <= 128 unless WIDE) floats in
+// global memory, read past L1 (other CTAs of the same grid may have written
+// them); l_val(k) is its lse. Lane l owns columns 4l..4l+3 and, if WIDE,
+// 128+4l..128+4l+3. Source: the
 // MSLK pull request "[ROCm] Add FlyDSL paged-attention decode backend (dense
 // + fp8) with benchmark" (Kernels: pa_decode_reduce, the split-K combine).
-template <typename ORow, typename LVal>
+template <int KG, bool WIDE, typename ORow, typename LVal>
 __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_val, __nv_bfloat16* out,
                                             float* lse_out, int lane, bool out_f16) {
   auto pack = [&](float lo, float hi) { return out_f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float LOG2E = 1.4426950408889634f;
   const int c0 = lane * 4, c1 = 128 + lane * 4;
-  const bool h0 = c0 < D, h1 = c1 < D;
+  const bool h0 = c0 < D, h1 = WIDE && c1 < D;
   float m = NEG_INF, L = 0.f;
   bool poisoned = false;
   float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-  for (int k0 = 0; k0 < np; k0 += 8) {
-    float lk[8];
-    float4 v0[8], v1[8];
+  for (int k0 = 0; k0 < np; k0 += KG) {
+    float lk[KG];
+    float4 v0[KG], v1[KG];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KG; ++j) {
       const bool in = k0 + j < np;
       lk[j] = in ? l_val(k0 + j) : NEG_INF;
       poisoned |= lk[j] != lk[j];
@@ -43,15 +49,16 @@ __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_va
       v0[j] = in && h0 ? __ldcg(reinterpret_cast<const float4*>(o + c0)) : make_float4(0.f, 0.f, 0.f, 0.f);
       v1[j] = in && h1 ? __ldcg(reinterpret_cast<const float4*>(o + c1)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float mc = fmaxf(fmaxf(fmaxf(m, fmaxf(lk[0], lk[1])), fmaxf(lk[2], lk[3])),
-                           fmaxf(fmaxf(lk[4], lk[5]), fmaxf(lk[6], lk[7])));
+    float mc = m;
+#pragma unroll
+    for (int j = 0; j < KG; ++j) mc = fmaxf(mc, lk[j]);
     if (mc == NEG_INF) continue;
     const float so = m == NEG_INF ? 0.f : ex2((m - mc) * LOG2E);
     a0.x *= so; a0.y *= so; a0.z *= so; a0.w *= so;
     a1.x *= so; a1.y *= so; a1.z *= so; a1.w *= so;
     L *= so;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KG; ++j) {
       if (lk[j] == NEG_INF) continue;
       const float w = ex2((lk[j] - mc) * LOG2E);
       a0.x += w * v0[j].x; a0.y += w * v0[j].y; a0.z += w * v0[j].z; a0.w += w * v0[j].w;
@@ -73,18 +80,22 @@ __device__ __forceinline__ void combine_row(int np, int D, ORow o_row, LVal l_va
 
 // combine_row over a row of any D (a multiple of 4): 256 columns at a time
 // (the weights are recomputed per chunk; they are the same every time).
-template <typename ORow, typename LVal>
+template <int KG, typename ORow, typename LVal>
 __device__ __forceinline__ void combine_row_any(int np, int D, ORow o_row, LVal l_val, __nv_bfloat16* out,
                                                 float* lse_out, int lane, bool out_f16) {
+  if (D <= 128) {
+    combine_row<KG, false>(np, D, o_row, l_val, out, lse_out, lane, out_f16);
+    return;
+  }
   for (int c = 0; c < D; c += 256)
-    combine_row(
+    combine_row<KG, true>(
         np, D - c < 256 ? D - c : 256, [&](int k) { return o_row(k) + c; }, l_val, out + c,
         c == 0 ? lse_out : nullptr, lane, out_f16);
 }
 
 
 // Explicit splits: grid covers B*T*Hq rows, 4 rows (warps) per CTA.
-__global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(128, 8) pa_reduce_splits_kernel(const __grid_constant__ ReduceParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row = (size_t)blockIdx.x * 4 + warp;
   const size_t rows = (size_t)p.B * p.T * p.Hq;
@@ -94,7 +105,7 @@ __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_cons
   const float* po = p.part_o + base * p.D;
   const float* pl = p.part_lse + base;
   const int D = p.D;
-  combine_row_any(
+  combine_row_any<kCombineGroup>(
       p.num_splits, D, [&](int k) { return po + (size_t)k * D; }, [&](int k) { return __ldcg(pl + k); },
       p.out + row * D, p.lse ? p.lse + row : nullptr, lane, p.out_f16 != 0);
 }
@@ -103,7 +114,7 @@ __global__ void __launch_bounds__(128) pa_reduce_splits_kernel(const __grid_cons
 // row 4y + w of unit u = b * NHG + hg from the pieces that the split CTAs
 // i0..i1 covering the unit wrote to slots u + i. Units wholly inside one
 // CTA's share, and sequences with no keys, were written by the split kernel.
-__global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(128, 8) pa_reduce_balanced_kernel(const __grid_constant__ ReduceParams p) {
   __shared__ long long s_sum[2][4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
@@ -151,7 +162,7 @@ __global__ void __launch_bounds__(128) pa_reduce_balanced_kernel(const __grid_co
   const float* pl = p.part_lse;
   const int M = p.M, D = p.D;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  combine_row(
+  combine_row_any<kCombineGroup>(
       i1 - i0 + 1, D, [&](int k) { return po + ((size_t)(u + i0 + k) * M + rho) * D; },
       [&](int k) {
         // A CTA whose share is empty wrote nothing; with at least as many

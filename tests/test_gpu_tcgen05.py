@@ -215,3 +215,23 @@ def test_graph_capture_replays_like_eager():
     eager = pb.decode_inputs(other.to("cuda"), num_splits=0)
     torch.cuda.synchronize()
     assert torch.equal(out, eager[0]) and torch.equal(lse, eager[1])
+
+
+def test_workspace_sized_under_the_default_selection_fits():
+    """pa_decode_workspace_size(shape, 0) is the largest plan over every
+    kernel selection: a workspace sized while the automatic choice is set
+    serves a call on this kernel."""
+    inp = gen.make_inputs(spec(**dict(batch=6, ctx_range=(1, 900), context_lens=None, pool_pages=500, max_blocks_per_seq=57)))
+    dev = inp.to("cuda")
+    shp = pb.make_shape(dev.q, dev.k_cache, dev.block_tables)
+    pb.set_kernel_path(pb.KERNEL_AUTO)
+    size = pb.workspace_size(shp, 0)
+    pb.set_kernel_path(pb.KERNEL_TCGEN05)
+    assert pb.kernel_for_inputs(dev) == pb.KERNEL_TCGEN05
+    assert pb.workspace_size(shp, 0) == size
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+    ref_out, ref_lse = oracle.decode(ora(inp), inp.scale)
+    out, lse = pb.decode_inputs(dev, workspace=ws)
+    torch.cuda.synchronize()
+    assert pb.device_error() == 0
+    check(out.float().cpu().double().numpy(), lse.cpu().double().numpy(), ref_out, ref_lse, tol_of(inp.spec))
