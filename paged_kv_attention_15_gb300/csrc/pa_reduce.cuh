@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(128, 8) pa_reduce_balanced_kernel(const __grid
   const int u = blockIdx.x;
   const int b = u / p.NHG, hg = u % p.NHG;
   const int cap = p.max_blocks * p.P;
+  int cb = __ldg(p.context_lens + b);  // (issued with the loop's loads: one round trip)
   long long before = 0, total = 0;
   for (int i = threadIdx.x; i < p.B; i += 128) {
     int c = __ldg(p.context_lens + i);
@@ -142,7 +143,6 @@ __global__ void __launch_bounds__(128, 8) pa_reduce_balanced_kernel(const __grid
   if (rho >= p.M) return;
   before = s_sum[0][0] + s_sum[0][1] + s_sum[0][2] + s_sum[0][3];
   total = s_sum[1][0] + s_sum[1][1] + s_sum[1][2] + s_sum[1][3];
-  int cb = __ldg(p.context_lens + b);
   cb = cb < 0 ? 0 : (cb > cap ? cap : cb);
   const long long nvb = (cb + p.P - 1) / p.P + p.tidar;
   if (nvb == 0) return;
