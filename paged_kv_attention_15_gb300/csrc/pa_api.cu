@@ -278,27 +278,34 @@ bool geom_umma(const pa_shape* s, Kind kind, Geom* g) {
   return false;
 }
 
-// Query-row-major tcgen05 kernel geometry: 16-bit caches, D = 128, units of
-// 64 query rows (two kv heads of G * T = 32 rows, or one of 64); stages of
-// 64 key rows in page boxes of at least 16 rows; the draft scratch in one
-// box whose key rows fill whole 16-row MMA steps.
+// Query-row-major tcgen05 kernel geometry: 16-bit caches, D = 128; units of
+// 128 query rows (four kv heads of G * T = 32 rows: one 16-token page box
+// of the four heads per 64-key-row stage) where the kv heads group by four,
+// else of 64 rows (two kv heads of 32 rows, or one of 64; stages of 64 key
+// rows copied per page and 128-byte chunk, page boxes of at least 16 rows);
+// the draft scratch in one box whose key rows fill whole 16-row MMA steps.
 bool geom_qrow(const pa_shape* s, Kind kind, Geom* g) {
   if (kind == Kind::kFp8) return false;
   const int G = s->num_q_heads / s->num_kv_heads, T = s->q_tokens, P = s->page_size, D = s->head_dim;
   const int GT = G * T;
-  const int H2 = GT == 32 ? 2 : (GT == 64 ? 1 : 0);
+  int H2 = GT == 32 ? 2 : (GT == 64 ? 1 : 0);
+  int M = 64;
+  if (GT == 32 && s->num_kv_heads % 4 == 0 && pa::qrow_kernel_16(D, kind == Kind::kF16, 4, 128).fn) {
+    H2 = 4;
+    M = 128;
+  }
   if (H2 == 0 || s->num_kv_heads % H2) return false;
   const int TS = 64 / H2, BR = P < TS ? P : TS;
   if (BR < 16) return false;
   int TP = (T + 15) / 16 * 16;
-  if (H2 == 2 && T <= 8) TP = 8;
+  if (H2 >= 2 && T <= 8) TP = 8;
   if (kind == Kind::kTidar && TP * H2 > 64) return false;
-  const SplitKernel k = pa::qrow_kernel_16(D, kind == Kind::kF16, H2);
+  const SplitKernel k = pa::qrow_kernel_16(D, kind == Kind::kF16, H2, M);
   if (!k.fn) return false;
   g->GT = GT;
   g->H2 = H2;
   g->NHG = s->num_kv_heads / H2;
-  g->M = 64;
+  g->M = M;
   g->MT = 0;
   g->TS = TS;
   g->TSL = 0;
@@ -307,7 +314,7 @@ bool geom_qrow(const pa_shape* s, Kind kind, Geom* g) {
   g->TP = TP;
   g->ilv = 1;
   g->path = kPathQrow;
-  g->chunk_boxes = 1;
+  g->chunk_boxes = M == 64 ? 1 : 0;
   g->k = k;
   return true;
 }

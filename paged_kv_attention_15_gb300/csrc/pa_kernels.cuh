@@ -254,15 +254,16 @@ __device__ __forceinline__ uint32_t swz(int row, int unit) {
 // Waits (bounded, ignoring the abort flag) for the last fill of every ring
 // slot and Q slot this producer issued, so that no copy is still in flight
 // when the CTA exits. `filled` has bit s set if slot s was ever filled, and
-// `parity` holds the phase parity of its last fill.
+// `parity` holds the phase parity of its last fill; Q loads went to nq
+// slots in turn.
 __device__ __forceinline__ void drain_copies(uint32_t bar_full, uint32_t bar_qfull, int ns, uint32_t filled,
-                                             uint32_t parity, int qloads) {
+                                             uint32_t parity, int qloads, int nq = 2) {
   const int zero = 0;
   const volatile int* no_abort = &zero;
   for (int s = 0; s < ns; ++s)
     if (filled >> s & 1) mbar_wait(bar_full + 8 * s, parity >> s & 1, kWaitLimitNs, no_abort);
-  for (int q = qloads - 2 > 0 ? qloads - 2 : 0; q < qloads; ++q)
-    mbar_wait(bar_qfull + 8 * (q & 1), (q >> 1) & 1, kWaitLimitNs, no_abort);
+  for (int q = qloads - nq > 0 ? qloads - nq : 0; q < qloads; ++q)
+    mbar_wait(bar_qfull + 8 * (q % nq), (q / nq) & 1, kWaitLimitNs, no_abort);
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* s_abort, int* err_flags) {
@@ -281,6 +282,7 @@ struct RingGeom {
   int ns, qch, nch;
   uint32_t row_bytes;     // bytes of one key row of all H2 heads
   uint32_t chunk_stride;  // 0: a box holds every chunk of its rows
+  int nq;                 // Q slots (2: double-buffered across work items; 1)
 };
 
 // The producer warp of the split kernels: walks this CTA's work items and,
@@ -314,9 +316,10 @@ static __device__ __forceinline__ void produce_ring(const SplitParams& p, const 
   bool ok = true;
   while (ok && next_item(p, s_ctx, s_start, cur, it)) {
     if (it.nst == 0) continue;
-    const int qs = qn & 1;
+    const int qs = qn % g.nq;
     // Warp-uniform verdicts: the lanes leave the loops together.
-    if (qn >= 2) ok = __all_sync(0xffffffffu, mbar_wait(bar_qempty + 8 * qs, ((qn >> 1) - 1) & 1, kWaitLimitNs, s_abort));
+    if (qn >= g.nq)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_qempty + 8 * qs, ((qn / g.nq) - 1) & 1, kWaitLimitNs, s_abort));
     if (!ok) break;
     if (lane == 0) {
       // Rows of kv head hl occupy rows [hl*GT, (hl+1)*GT) of each chunk.
@@ -397,7 +400,7 @@ static __device__ __forceinline__ void produce_ring(const SplitParams& p, const 
   launch_dependents();
   if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
   // Let every copy this warp issued land before the CTA can exit.
-  drain_copies(bar_full, bar_qfull, g.ns, filled, fill_parity, qn);
+  drain_copies(bar_full, bar_qfull, g.ns, filled, fill_parity, qn, g.nq);
 }
 
 // ------------------------------------------------------------ split kernel
@@ -484,7 +487,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
       if (warp != CW) return;  // the idle warps of the producer's warpgroup
     }
     const RingGeom g{sbase, (uint32_t)C::OFF_Q, (uint32_t)C::QSLOT, (uint32_t)C::QCHUNK, (uint32_t)C::STAGE,
-                     (uint32_t)C::TILE, NS, C::QCH, NCH, row_bytes, 0u};
+                     (uint32_t)C::TILE, NS, C::QCH, NCH, row_bytes, 0u, 2};
     produce_ring(p, s_ctx, s_start, g, bar_full, bar_empty, bar_qfull, bar_qempty, s_abort, lane);
     return;
   }

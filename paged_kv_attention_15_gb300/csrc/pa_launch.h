@@ -27,8 +27,9 @@ SplitKernel split_kernel_f16(int head_dim, int row_tiles, int slice, int consume
 SplitKernel umma_kernel_fp8(int head_dim, int GT, int N);
 SplitKernel umma_kernel_16(int head_dim, bool f16, int GT, int N);
 
-// Instance of the query-row-major tcgen05 kernel (16-bit caches, 64 query
-// rows per unit) for (head_dim, kv heads per unit); fn == nullptr if not built.
-SplitKernel qrow_kernel_16(int head_dim, bool f16, int h2);
+// Instance of the query-row-major tcgen05 kernel (16-bit caches) for
+// (head_dim, kv heads per unit, query rows per unit m = 64 or 128);
+// fn == nullptr if not built.
+SplitKernel qrow_kernel_16(int head_dim, bool f16, int h2, int m);
 
 }  // namespace pa

@@ -47,9 +47,16 @@ constexpr int kQThreads = 192;  // softmax warps 0-3, producer warp 4, MMA warp 
 constexpr int kQProducerWarp = 4;
 constexpr int kQMmaWarp = 5;
 
-template <int D>
+// M = 64: two kv heads of 32 query rows or one of 64, pages copied per
+// 128-byte chunk, two Q slots. M = 128: four kv heads of 32 rows, whose
+// 16-token page box already holds the stage's 64 key rows contiguously in
+// every chunk (one copy per page, a 16 KB box), one Q slot (the ring keeps
+// four stages).
+template <int D, int M_>
 struct QCfg {
-  static constexpr int M = 64;        // query rows of a unit: the MMA M
+  static constexpr int M = M_;        // query rows of a unit: the MMA M
+  static constexpr bool CB = M == 64; // one copy per page and chunk (else per page)
+  static constexpr int NQ = M == 128 ? 1 : 2;  // Q slots
   static constexpr int KR = 64;       // key rows (tokens x heads) of a stage
   static constexpr int NCH = D / 64;  // 128-byte column chunks of a 16-bit row
   static constexpr int TILE = KR * D * 2;  // [chunk][key row][128 B]
@@ -60,10 +67,10 @@ struct QCfg {
   static constexpr int PBUF = M * KR * 2;  // P of a stage: one 128-byte row (64 keys) per query row
   static constexpr int NPB = 2;
   static constexpr int BARS = 256;
-  static constexpr int FIXED = 2 * QSLOT + NPB * PBUF + BARS + 64;
+  static constexpr int FIXED = NQ * QSLOT + NPB * PBUF + BARS + 64;
   static constexpr int NS = clamp_int((kSmemBudget - FIXED) / STAGE, 2, 8);
   static constexpr int OFF_Q = NS * STAGE;
-  static constexpr int OFF_P = OFF_Q + 2 * QSLOT;
+  static constexpr int OFF_P = OFF_Q + NQ * QSLOT;
   static constexpr int OFF_BAR = OFF_P + NPB * PBUF;
   static constexpr int OFF_MISC = OFF_BAR + BARS;  // tensor-memory base, abort flag
   static constexpr int OFF_TABLE = OFF_MISC + 64;
@@ -72,6 +79,7 @@ struct QCfg {
   static constexpr int TM_O = 2 * KR;                  // [D] output columns
   static constexpr int TM_COLS = 2 * KR + D <= 256 ? 256 : 512;
   static_assert(D == 128 || D == 256, "head_dim");
+  static_assert(M == 64 || M == 128, "query rows per unit");
   static_assert(2 * NS + 16 <= BARS / 8, "barriers");
 };
 
@@ -115,9 +123,11 @@ __device__ __forceinline__ QStage q_stage(const SplitParams& p, const Item& it, 
   return g;
 }
 
-template <int D, int KV, int H2>
+template <int D, int KV, int H2, int M>
 __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_constant__ SplitParams p) {
-  using C = QCfg<D>;
+  using C = QCfg<D, M>;
+  constexpr int NQ = C::NQ;
+  constexpr int LH2 = H2 == 4 ? 2 : (H2 == 2 ? 1 : 0);  // log2 of H2
   constexpr bool F16 = KV == kKvF16;
   constexpr int NS = C::NS;
   constexpr int KR = C::KR;
@@ -159,9 +169,9 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
     *s_abort = 0;
     fence_mbar_init();
   }
-  {  // query rows past M read as zero: clear both Q slots once
+  {  // query rows past M read as zero: clear the Q slots once
     uint4* q4 = reinterpret_cast<uint4*>(smem + C::OFF_Q);
-    for (int i = tid; i < 2 * C::QSLOT / 16; i += kQThreads) q4[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < NQ * C::QSLOT / 16; i += kQThreads) q4[i] = make_uint4(0, 0, 0, 0);
   }
   if (warp == kQMmaWarp) tmem_alloc(sbase + C::OFF_MISC, C::TM_COLS);
   if (p.num_splits == 0) {
@@ -192,7 +202,8 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
   if (warp == kQProducerWarp) {
     // ================================================================ producer
     const RingGeom g{sbase, (uint32_t)C::OFF_Q, (uint32_t)C::QSLOT, (uint32_t)C::QCHUNK, (uint32_t)C::STAGE,
-                     (uint32_t)C::TILE, NS, C::NCH, C::NCH, (uint32_t)(H2 * D * 2), (uint32_t)C::CSTR};
+                     (uint32_t)C::TILE, NS, C::NCH, C::NCH, (uint32_t)(H2 * D * 2),
+                     C::CB ? (uint32_t)C::CSTR : 0u, NQ};
     produce_ring(p, s_ctx, s_start, g, bar_full, bar_empty, bar(kQbQFull), bar(kQbQEmpty), s_abort, lane);
   } else if (warp == kQMmaWarp) {
     // ================================================================ MMA issuer
@@ -205,8 +216,8 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
       bool ok = true;
       while (ok && next_item(p, s_ctx, s_start, cur, it)) {
         if (it.nst == 0) continue;
-        const int qs = qn & 1;
-        ok = mbar_wait(bar(kQbQFull + qs), (qn >> 1) & 1, kWaitLimitNs, s_abort);
+        const int qs = qn % NQ;
+        ok = mbar_wait(bar(kQbQFull + qs), (qn / NQ) & 1, kWaitLimitNs, s_abort);
         const uint32_t qbase = sbase + C::OFF_Q + qs * C::QSLOT;
         for (int j = 0; ok && j <= it.nst; ++j) {
           if (j < it.nst) {
@@ -218,13 +229,14 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
             tc_fence_after();
             const QStage g = q_stage(p, it, j);
             const int nkeys = g.nbox * H2 * g.brows;  // key rows of the stage (a multiple of 16)
+            const uint32_t cs = C::CB ? (uint32_t)C::CSTR : (uint32_t)nkeys * 128u;  // chunk stride
             const uint32_t id_s = idesc_f16(C::M, nkeys, !F16, false, false);
             const uint32_t kb = sbase + slot * C::STAGE;
             const uint32_t d_s = tm + (uint32_t)(C::TM_S + sb * KR);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
               const uint64_t a = smem_desc(qbase + (ks >> 2) * C::QCHUNK + (ks & 3) * 32, 16, 1024, kSwz128);
-              const uint64_t b = smem_desc(kb + (ks >> 2) * C::CSTR + (ks & 3) * 32, 16, 1024, kSwz128);
+              const uint64_t b = smem_desc(kb + (ks >> 2) * cs + (ks & 3) * 32, 16, 1024, kSwz128);
               umma_f16(d_s, a, b, id_s, ks > 0 ? 1u : 0u);
             }
             umma_commit(bar(kQbSFull + sb));
@@ -239,11 +251,12 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
             tc_fence_after();
             const QStage g = q_stage(p, it, jj);
             const int nkeys = g.nbox * H2 * g.brows;
+            const uint32_t cs = C::CB ? (uint32_t)C::CSTR : (uint32_t)nkeys * 128u;
             const uint32_t vb = sbase + slot * C::STAGE + C::TILE;
             const uint32_t pbuf = sbase + C::OFF_P + pb * C::PBUF;
             for (int key = 0; key < nkeys; key += 16) {  // P columns of the k-step
               const uint64_t a = smem_desc(pbuf + (key >> 4) * 32, 16, 1024, kSwz128);
-              const uint64_t b = smem_desc(vb + key * 128, C::CSTR, 1024, kSwz128);
+              const uint64_t b = smem_desc(vb + key * 128, cs, 1024, kSwz128);
               umma_f16(tm + C::TM_O, a, b, id_pv, (jj > 0 || key > 0) ? 1u : 0u);
             }
             umma_commit(bar_empty + 8 * slot);
@@ -266,9 +279,12 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
   } else {
     // ================================================================ softmax + epilogue
     const int GT = p.GT;
-    const bool act = lane < 16;
-    const int rho = 16 * warp + (lane & 15);  // this lane's query row (lanes >= 16 mirror 0-15)
-    const int hl = rho / GT;                  // its kv head in the unit (warp-uniform: GT >= 16)
+    // M = 64: row i in lane 32 (i / 16) + i % 16, so lane l < 16 of warp w
+    // owns row 16 w + l (lanes >= 16 mirror 0-15); M = 128: lane l of warp w
+    // owns row 32 w + l.
+    const bool act = M == 128 || lane < 16;
+    const int rho = M == 128 ? 32 * warp + lane : 16 * warp + (lane & 15);
+    const int hl = rho / GT;  // its kv head in the unit (warp-uniform: GT >= 16 / 32)
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const float sl = p.scale_log2;
     // Draft tokens the row's draft token sees in the scratch: all T, or the
@@ -306,7 +322,7 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
         tc_fence_after();
         const QStage g = q_stage(p, it, j);
         const int nrows = H2 * g.brows;     // key rows of a page box (all heads)
-        const int lbn = g.lb + (H2 == 2);   // log2 of nrows
+        const int lbn = g.lb + LH2;         // log2 of nrows
         const int nown = g.nbox * g.brows;  // own score columns written this stage
         // ---- this head's score columns, 16 at a time: own slot o = token
         // (paged: box o / brows, row o % brows; scratch: draft token o)
@@ -386,11 +402,12 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
               for (int u = 0; u < 8; ++u) v[u] = pk[kg * 8 + u];
             } else {
               // head of the group and own group index: boxes of nrows keys
-              // (paged: brows >= 16), or the scratch's 8 + 8 keys
+              // (paged: brows >= 16), or the scratch's 8-key heads (two per
+              // group)
               if (g.scr && g.brows == 8) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                  v[u] = (kg == 0 && (u >> 2) == hl) ? pk[u & 3] : 0u;
+                  v[u] = (kg == (hl >> 1) && (u >> 2) == (hl & 1)) ? pk[u & 3] : 0u;
               } else {
                 const int key = 16 * kg;
                 const int i = key >> lbn, w = key & (nrows - 1);
@@ -426,8 +443,8 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
             const int r = r_lo + rest % nr;
             const int hc = rest / nr;  // head + H2 * chunk
             const int h = hc % H2, c = hc / H2;
-            const uint32_t row_addr = vb + (uint32_t)c * (uint32_t)C::CSTR +
-                                      (uint32_t)(last * nrows + h * g.brows + r) * 128u;
+            const uint32_t cs = C::CB ? (uint32_t)C::CSTR : (uint32_t)(g.nbox * nrows) * 128u;
+            const uint32_t row_addr = vb + (uint32_t)c * cs + (uint32_t)(last * nrows + h * g.brows + r) * 128u;
             st_shared_v4(row_addr + (uint32_t)(unit << 4), make_uint4(0, 0, 0, 0));
           }
         }

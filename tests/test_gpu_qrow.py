@@ -93,6 +93,15 @@ CASES = [
     dict(draft_scratch=False, q_tokens=2, num_q_heads=32, num_kv_heads=2, kv_format="f16",
          page_size=32),
     dict(batch=9, ctx_range=(1, 2000), context_lens=None, pool_pages=1400),
+    # 128-row units: four kv heads of 32 rows, one 16-token page box per stage
+    dict(num_q_heads=16, num_kv_heads=4, context_lens=(15, 16, 17, 333)),
+    dict(num_q_heads=32, num_kv_heads=8, draft_block=1, context_lens=(0, 100, 31, 700)),
+    dict(num_q_heads=16, num_kv_heads=4, draft_block=3, page_size=32, context_lens=(33, 64, 1, 300)),
+    dict(num_q_heads=16, num_kv_heads=4, page_size=64, context_lens=(64, 65, 129, 2)),
+    dict(q_tokens=4, num_q_heads=32, num_kv_heads=4),                    # 4 draft tokens x 8 heads
+    dict(draft_scratch=False, q_tokens=1, num_q_heads=128, num_kv_heads=4, context_lens=(0, 9, 400, 1000)),
+    dict(draft_scratch=False, q_tokens=2, num_q_heads=64, num_kv_heads=4, kv_format="f16"),
+    dict(batch=7, num_q_heads=32, num_kv_heads=8, ctx_range=(1, 1500), context_lens=None, pool_pages=800),
 ]
 
 
@@ -115,7 +124,8 @@ def test_spread_scores_rescale_the_output(q_scale):
 def test_nan_poison_past_the_context():
     """Cache slots past every context end hold NaN: their scores are masked
     and their value rows are zeroed before the product reads them."""
-    for kw in (dict(), dict(q_tokens=16, draft_block=4), dict(draft_scratch=False, q_tokens=1, num_q_heads=64)):
+    for kw in (dict(), dict(q_tokens=16, draft_block=4), dict(draft_scratch=False, q_tokens=1, num_q_heads=64),
+               dict(num_q_heads=16, num_kv_heads=4)):
         inp = gen.make_inputs(spec(context_lens=(5, 17, 64, 99), **kw), poison=True)
         full(inp, 0)
         full(inp, 3)
@@ -136,7 +146,8 @@ def test_page_relabelling_is_bit_exact():
 
 def test_matches_the_warp_mma_kernel():
     """The query-row kernel and the warp-level kernel agree within rounding."""
-    for case in (dict(), dict(q_tokens=16, draft_block=4), dict(draft_scratch=False, q_tokens=1, num_q_heads=64)):
+    for case in (dict(), dict(q_tokens=16, draft_block=4), dict(draft_scratch=False, q_tokens=1, num_q_heads=64),
+                 dict(num_q_heads=32, num_kv_heads=8)):
         inp = gen.make_inputs(spec(**case))
         dev = inp.to("cuda")
         a = run(inp, 0, dev=dev)
