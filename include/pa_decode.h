@@ -278,6 +278,21 @@ pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
  * rounding. Returns PA_ERR_INVALID_ARG for any other value. */
 pa_status pa_decode_set_kernel_path(int32_t path);
 
+/* Split-K combine of the balanced schedule (num_splits == 0): mode 0 (the
+ * default) runs a separate combine kernel after the split kernel (launched
+ * with programmatic dependent launch); mode 1 fuses it into the warp-level
+ * split kernel: each CTA counts its finished piece of a (sequence, kv head
+ * group) unit in the workspace, and the last one to finish combines the
+ * unit's pieces (one memset of the counters per call replaces the combine
+ * launch; fp8 caches, the eight-warp draft-block instances and the
+ * tcgen05 kernels keep the separate combine).
+ * Measured slower than mode 0 on every benchmark workload. Source: the MSLK
+ * pull request "[ROCm] Add FlyDSL paged-attention decode backend (dense +
+ * fp8) with benchmark" (Kernels: the split-K partial combine). Results
+ * agree within rounding. Process-wide; PA_ERR_INVALID_ARG for other values.
+ * Host-only. */
+pa_status pa_decode_set_combine(int32_t mode);
+
 /* Which kernel (1, 2 or 3, as above) a decode of this shape would run under the
  * current setting; format: 0 bf16 (pa_decode), 1 fp8 (pa_decode_fp8), 2 f16
  * (pa_decode_f16), 3 draft block (pa_decode_tidar*). -1 for an unsupported

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "pa_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32)]),
     "pa_decode_profile_events": (ctypes.c_int, [_P, _P]),
     "pa_decode_set_kernel_path": (ctypes.c_int, [ctypes.c_int32]),
+    "pa_decode_set_combine": (ctypes.c_int, [ctypes.c_int32]),
     "pa_decode_kernel_for": (ctypes.c_int32, [ctypes.POINTER(PaShape), ctypes.c_int32]),
     "pa_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float, _P, _P,
                                          ctypes.c_int32, _P]),
@@ -293,6 +294,15 @@ def set_kernel_path(path: int) -> None:
     """Process-wide kernel choice: KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05
     or KERNEL_TCGEN05_QROW (see pa_decode_set_kernel_path)."""
     _check(lib().pa_decode_set_kernel_path(int(path)), "pa_decode_set_kernel_path")
+
+
+COMBINE_SEPARATE, COMBINE_FUSED = 0, 1
+
+
+def set_combine(mode: int) -> None:
+    """Process-wide split-K combine of the balanced schedule: COMBINE_SEPARATE
+    or COMBINE_FUSED (see pa_decode_set_combine)."""
+    _check(lib().pa_decode_set_combine(int(mode)), "pa_decode_set_combine")
 
 
 def kernel_for(shape: PaShape, fmt: str) -> int:

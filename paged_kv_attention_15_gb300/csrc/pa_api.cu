@@ -183,6 +183,11 @@ constexpr int kPathAuto = 0, kPathWarp = 1, kPathUmma = 2, kPathQrow = 3;
 // only, or one of the tcgen05 kernels wherever it has an instance.
 std::atomic<int> g_kernel_path{kPathAuto};
 
+// How the balanced schedule's pieces are combined: a separate reduce kernel
+// (0), or fused into the warp-level split kernel (1: its last CTA to finish a
+// unit's piece combines the unit).
+std::atomic<int> g_combine_mode{0};
+
 int ilog2(int x) {
   int l = 0;
   while ((1 << l) < x) ++l;
@@ -352,6 +357,7 @@ struct Plan {
   size_t smem = 0;
   size_t ws_bytes = 0;
   size_t part_lse_off = 0;
+  size_t count_off = 0;   // balanced mode: per-unit arrival counters of the fused combine
 };
 
 // path: the kernel selection to plan for (-1: the current setting).
@@ -375,7 +381,8 @@ pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d
       p.smem = smem;
       const size_t slots = (size_t)units + p.grid;
       p.part_lse_off = align256(slots * M * D * sizeof(float));
-      p.ws_bytes = p.part_lse_off + align256(slots * M * sizeof(float));
+      p.count_off = p.part_lse_off + align256(slots * M * sizeof(float));
+      p.ws_bytes = p.count_off + align256((size_t)units * sizeof(unsigned));
       *plan = p;
       return PA_OK;
     }
@@ -528,6 +535,15 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     p.part_o = static_cast<float*>(a.workspace);
     p.part_lse = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + plan.part_lse_off);
   }
+  // Fused combine: warp-level kernel, balanced schedule; the counters start
+  // at zero (one memset per call; the kernel leaves them zero as well).
+  const bool fused = plan.balanced && geo.path == kPathWarp && geo.k.fused &&
+                     g_combine_mode.load(std::memory_order_relaxed) == 1;
+  if (fused) {
+    p.unit_count = reinterpret_cast<unsigned*>(static_cast<char*>(a.workspace) + plan.count_off);
+    if (cudaMemsetAsync(p.unit_count, 0, (size_t)B * geo.NHG * sizeof(unsigned), a.stream) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
 
   const SplitKernel k = geo.k;
   if ((st = ensure_kernel_ready(d, k)) != PA_OK) return st;
@@ -538,7 +554,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     return PA_ERR_CUDA;
   if (ev_split && cudaEventRecord(ev_split, a.stream) != cudaSuccess) return PA_ERR_CUDA;
 
-  if (plan.balanced || plan.splits > 1) {
+  if ((plan.balanced && !fused) || plan.splits > 1) {
     ReduceParams r;
     std::memset(&r, 0, sizeof(r));
     r.part_o = p.part_o;
@@ -775,6 +791,12 @@ pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
   if (need > 0 && (st = noalloc_scratch(&ws)) != PA_OK) return st;
   return pa_decode(q, k_cache, v_cache, block_tables, context_lens, shape, scale, out, lse, num_splits, ws, need,
                    stream);
+}
+
+pa_status pa_decode_set_combine(int32_t mode) {
+  if (mode < 0 || mode > 1) return PA_ERR_INVALID_ARG;
+  g_combine_mode.store(mode, std::memory_order_relaxed);
+  return PA_OK;
 }
 
 pa_status pa_decode_set_kernel_path(int32_t path) {

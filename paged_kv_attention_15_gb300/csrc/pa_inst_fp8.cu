@@ -7,7 +7,7 @@ template <int D, int MT, int TSL, int CW = kConsumerWarps>
 static SplitKernel entry() {
   using C = Cfg<D, MT, true, TSL, CW>;
   return SplitKernel{reinterpret_cast<const void*>(&pa_split_kernel<D, MT, kKvFp8, TSL, CW>), C::SMEM_FIXED, C::NS,
-                     C::THREADS, C::REGSPLIT ? kSplitLaunchRegs : 0};
+                     C::THREADS, C::REGSPLIT ? kSplitLaunchRegs : 0, C::FUSED ? 1 : 0};
 }
 
 template <int D>

@@ -92,6 +92,7 @@ struct SplitParams {
   float* lse;
   float* part_o;
   float* part_lse;
+  unsigned* unit_count;  // balanced schedule, combine fused into this kernel: arrivals per unit (else nullptr)
   int* err_flags;
   int B, T, Hq, Hkv, G, M, P, max_blocks, num_pages;
   int H2;          // kv heads per work unit
@@ -159,7 +160,13 @@ struct Cfg {
   static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
   static_assert(MT == 1 || MT == 2 || MT == 4, "unsupported row tiles");
   static_assert(TSL == 16 || TSL == 32 || TSL == 64, "unsupported warp slice");
+  // Fused combine: built into the instances whose main loop it costs no
+  // spills (not fp8, not the register split); float4 column groups per
+  // consumer thread and pass.
+  static constexpr bool FUSED = !FP8 && !REGSPLIT;
+  static constexpr int FEPT = clamp_int((ROWS * (D / 4) + 32 * CW - 1) / (32 * CW), 1, 4);
   static_assert(CW == 4 || CW == 8, "unsupported consumer warps");
+  static_assert(2 * 8 + 6 <= BARS / 8, "barrier area: full/empty rings, Q slots, abort flag, fused-combine flag");
 };
 
 // ----------------------------------------------------------------- schedule
@@ -401,6 +408,129 @@ static __device__ __forceinline__ void produce_ring(const SplitParams& p, const 
   if (!ok && lane == 0) raise_abort(s_abort, p.err_flags);
   // Let every copy this warp issued land before the CTA can exit.
   drain_copies(bar_full, bar_qfull, g.ns, filled, fill_parity, qn, g.nq);
+}
+
+// ------------------------------------------------------- fused combine
+// Pieces i0..i1 of the balanced schedule's unit u (the units' shares of the
+// flattened pages meet inside it): CTA i wrote its piece to slot u + i,
+// M rows of D floats and M lse values; a CTA whose share is empty wrote
+// nothing. Source: the MSLK pull request "[ROCm] Add FlyDSL paged-attention
+// decode backend (dense + fp8) with benchmark" (Kernels: the split-K partial
+// combine), here run by the last CTA to finish a piece of the unit.
+struct UnitPieces {
+  int i0, i1;      // CTAs whose shares meet the unit
+  long long N;     // flattened pages of the launch (all units)
+};
+
+__device__ __forceinline__ UnitPieces unit_pieces(const SplitParams& p, const int* s_start, const Item& it) {
+  const long long nvb = s_start[it.b + 1] - s_start[it.b];
+  UnitPieces r;
+  r.N = (long long)p.NHG * s_start[p.B];
+  const long long us = (long long)p.NHG * s_start[it.b] + (long long)it.hg * nvb;
+  const long long ue = us + nvb;
+  const long long G64 = p.grid;
+  r.i0 = (int)(((us + 1) * G64 - 1) / r.N);
+  r.i1 = (int)((ue * G64 - 1) / r.N);
+  return r;
+}
+
+// Number of CTAs in [i0, i1] whose share holds at least one page.
+__device__ __forceinline__ int written_pieces(const SplitParams& p, const UnitPieces& up) {
+  const long long G64 = p.grid;
+  if (up.N >= G64) return up.i1 - up.i0 + 1;
+  int n = 0;
+  for (long long i = up.i0; i <= up.i1; ++i) n += (up.N * i / G64) < (up.N * (i + 1) / G64);
+  return n;
+}
+
+// Combines unit u's pieces into its final rows with nthr threads (index
+// t): each thread takes float4 column groups (row rho, columns 4c..4c+3)
+// of up to EPT of the unit's M x D/4 groups per pass and loads, for two
+// pieces at a time, their lse and their columns of every group before
+// combining (one online pass: running max, sums rescaled when it grows), so
+// that a pass costs about one L2 round trip. Writes out (bf16, or f16 when
+// F16) and, for column group 0 of a row, its lse; a NaN piece lse makes the
+// row NaN, pieces with lse = -inf weigh 0.
+// (Not inlined: its registers stay out of the split kernel's main loop.)
+template <int D, bool F16, int EPT>
+__device__ __noinline__ void fused_combine(const SplitParams& p, const Item& it, const UnitPieces& up, int t,
+                                           int nthr) {
+  constexpr int C4 = D / 4;
+  constexpr int KG = 2;  // pieces per load round (EPT x KG float4 in flight per thread)
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float NaN = __int_as_float(0x7fffffff);
+  const float LOG2E = 1.4426950408889634f;
+  const int M = p.M, GT = p.GT, G = p.G;
+  const int u = it.b * p.NHG + it.hg;
+  const long long G64 = p.grid;
+  const int np = up.i1 - up.i0 + 1;
+  const int total = M * C4;
+  for (int e0 = 0; e0 < total; e0 += EPT * nthr) {
+    float m[EPT], L[EPT];
+    float4 a[EPT];
+    bool bad[EPT];
+#pragma unroll
+    for (int q = 0; q < EPT; ++q) {
+      m[q] = NEG_INF;
+      L[q] = 0.f;
+      a[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      bad[q] = false;
+    }
+    for (int k0 = 0; k0 < np; k0 += KG) {
+      float lk[KG][EPT];
+      float4 v[KG][EPT];
+#pragma unroll
+      for (int j = 0; j < KG; ++j) {
+        const long long i = up.i0 + k0 + j;
+        const bool in = k0 + j < np && (up.N >= G64 || (up.N * i / G64) < (up.N * (i + 1) / G64));
+        const size_t slot = (size_t)(u + i);
+#pragma unroll
+        for (int q = 0; q < EPT; ++q) {
+          const int e = e0 + q * nthr + t;
+          const int rho = e / C4, c = e - rho * C4;
+          const bool ok = in && e < total;
+          lk[j][q] = ok ? __ldcg(p.part_lse + slot * M + rho) : NEG_INF;
+          v[j][q] = ok ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * M + rho) * D) + c)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < EPT; ++q) {
+        float mc = m[q];
+#pragma unroll
+        for (int j = 0; j < KG; ++j) {
+          bad[q] |= lk[j][q] != lk[j][q];
+          mc = fmaxf(mc, lk[j][q]);
+        }
+        if (mc == NEG_INF) continue;
+        const float so = m[q] == NEG_INF ? 0.f : ex2((m[q] - mc) * LOG2E);
+        a[q].x *= so; a[q].y *= so; a[q].z *= so; a[q].w *= so;
+        L[q] *= so;
+#pragma unroll
+        for (int j = 0; j < KG; ++j) {
+          if (lk[j][q] == NEG_INF) continue;
+          const float w = ex2((lk[j][q] - mc) * LOG2E);
+          a[q].x += w * v[j][q].x; a[q].y += w * v[j][q].y; a[q].z += w * v[j][q].z; a[q].w += w * v[j][q].w;
+          L[q] += w;
+        }
+        m[q] = mc;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < EPT; ++q) {
+      const int e = e0 + q * nthr + t;
+      if (e >= total) continue;
+      const int rho = e / C4, c = e - rho * C4;
+      // row rho = hl * GT + tq * G + j  ->  query head (hg * H2 + hl) * G + j
+      const int hl = rho / GT, rem = rho - hl * GT;
+      const int tq = rem / G;
+      const size_t row = ((size_t)it.b * p.T + tq) * p.Hq + (size_t)(it.hg * p.H2 + hl) * G + (rem - tq * G);
+      const float inv = bad[q] ? NaN : (L[q] > 0.f ? 1.f / L[q] : 0.f);
+      *reinterpret_cast<uint2*>(p.out + row * D + 4 * c) =
+          make_uint2(pack16<F16>(a[q].x * inv, a[q].y * inv), pack16<F16>(a[q].z * inv, a[q].w * inv));
+      if (c == 0 && p.lse) p.lse[row] = bad[q] ? NaN : (L[q] > 0.f ? m[q] + lg2(L[q]) * kLn2 : NEG_INF);
+    }
+  }
 }
 
 // ------------------------------------------------------------ split kernel
@@ -940,58 +1070,87 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
       merge_weights();
       merge_columns(0, NT8);
     }
-    if (gi != 0) continue;
+    // Combine fused into this kernel (balanced schedule; instances with
+    // C::FUSED): every warp takes part in the arrival below, the tile's
+    // first warp writes the piece.
+    const bool fused = C::FUSED && p.unit_count != nullptr && it.part >= 0;
+    if (gi != 0 && !fused) continue;
+    if (gi == 0) {
+      float lse0 = L0 > 0.f ? (M0 + lg2(L0)) * kLn2 : NEG_INF;
+      float lse1 = L1 > 0.f ? (M1 + lg2(L1)) * kLn2 : NEG_INF;
+      // An item cut short by a timed-out wait (in this warp or another role of
+      // the CTA) is written as NaN, so that no part of it passes as a result.
+      if (__any_sync(0xffffffffu, !ok || *s_abort)) {
+        const float NaN = __int_as_float(0x7fffffff);
+  #pragma unroll
+        for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = NaN;
+        lse0 = lse1 = NaN;
+      }
 
-    float lse0 = L0 > 0.f ? (M0 + lg2(L0)) * kLn2 : NEG_INF;
-    float lse1 = L1 > 0.f ? (M1 + lg2(L1)) * kLn2 : NEG_INF;
-    // An item cut short by a timed-out wait (in this warp or another role of
-    // the CTA) is written as NaN, so that no part of it passes as a result.
-    if (__any_sync(0xffffffffu, !ok || *s_abort)) {
-      const float NaN = __int_as_float(0x7fffffff);
-#pragma unroll
-      for (int i = 0; i < NT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = NaN;
-      lse0 = lse1 = NaN;
+  #pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int rho = h2 ? rho1 : rho0;
+        if (rho >= p.M) continue;
+        // row rho = hl * GT + t * G + j  ->  query head (hg * H2 + hl) * G + j
+        const int rhl = rho / GT, rem = rho - rhl * GT;
+        const int t = rem / p.G;
+        const int h = (it.hg * H2 + rhl) * p.G + (rem - t * p.G);
+        const size_t row = ((size_t)it.b * p.T + t) * p.Hq + h;
+        const float lsev = h2 ? lse1 : lse0;
+        if (it.part < 0) {
+          __nv_bfloat16* o = p.out + row * D;
+          if (!FP8) {
+  #pragma unroll
+            for (int i = 0; i < NT8; ++i)
+              *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * c4) = pack16<F16>(acc[i][2 * h2], acc[i][2 * h2 + 1]);
+          } else {
+  #pragma unroll
+            for (int u = 0; u < D / 16; ++u)
+              *reinterpret_cast<uint2*>(o + 16 * u + 4 * c4) =
+                  make_uint2(pack_bf16x2(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2]),
+                             pack_bf16x2(acc[2 * u][2 * h2 + 1], acc[2 * u + 1][2 * h2 + 1]));
+          }
+          if (c4 == 0 && p.lse) p.lse[row] = lsev;
+        } else {
+          const size_t prow = p.num_splits > 0 ? row * p.num_splits + it.part : (size_t)it.part * p.M + rho;
+          float* o = p.part_o + prow * D;
+          if (!FP8) {
+  #pragma unroll
+            for (int i = 0; i < NT8; ++i)
+              *reinterpret_cast<float2*>(o + i * 8 + 2 * c4) = make_float2(acc[i][2 * h2], acc[i][2 * h2 + 1]);
+          } else {
+  #pragma unroll
+            for (int u = 0; u < D / 16; ++u)
+              *reinterpret_cast<float4*>(o + 16 * u + 4 * c4) =
+                  make_float4(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2], acc[2 * u][2 * h2 + 1],
+                              acc[2 * u + 1][2 * h2 + 1]);
+          }
+          if (c4 == 0) p.part_lse[prow] = lsev;
+        }
+      }
     }
-
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int rho = h2 ? rho1 : rho0;
-      if (rho >= p.M) continue;
-      // row rho = hl * GT + t * G + j  ->  query head (hg * H2 + hl) * G + j
-      const int rhl = rho / GT, rem = rho - rhl * GT;
-      const int t = rem / p.G;
-      const int h = (it.hg * H2 + rhl) * p.G + (rem - t * p.G);
-      const size_t row = ((size_t)it.b * p.T + t) * p.Hq + h;
-      const float lsev = h2 ? lse1 : lse0;
-      if (it.part < 0) {
-        __nv_bfloat16* o = p.out + row * D;
-        if (!FP8) {
-#pragma unroll
-          for (int i = 0; i < NT8; ++i)
-            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * c4) = pack16<F16>(acc[i][2 * h2], acc[i][2 * h2 + 1]);
-        } else {
-#pragma unroll
-          for (int u = 0; u < D / 16; ++u)
-            *reinterpret_cast<uint2*>(o + 16 * u + 4 * c4) =
-                make_uint2(pack_bf16x2(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2]),
-                           pack_bf16x2(acc[2 * u][2 * h2 + 1], acc[2 * u + 1][2 * h2 + 1]));
+    if constexpr (C::FUSED) {
+      if (fused) {
+        // The last CTA to finish a piece of this unit combines all of them:
+        // each piece's rows are made visible device-wide before its CTA
+        // counts itself in (atomicInc wraps to 0 on the last arrival, so the
+        // counters are zero again after every unit), and the last CTA reads
+        // the other pieces only after its own arrival.
+        volatile unsigned* s_last = reinterpret_cast<volatile unsigned*>(bars + 2 * NS + 5);
+        __threadfence();
+        named_barrier_sync(1, 32 * CW);
+        const UnitPieces up = unit_pieces(p, s_start, it);
+        if (warp == 0 && lane == 0) {
+          const unsigned np = (unsigned)written_pieces(p, up);
+          const unsigned old = atomicInc(p.unit_count + it.b * p.NHG + it.hg, np - 1);
+          *s_last = old == np - 1 ? 1u : 0u;
         }
-        if (c4 == 0 && p.lse) p.lse[row] = lsev;
-      } else {
-        const size_t prow = p.num_splits > 0 ? row * p.num_splits + it.part : (size_t)it.part * p.M + rho;
-        float* o = p.part_o + prow * D;
-        if (!FP8) {
-#pragma unroll
-          for (int i = 0; i < NT8; ++i)
-            *reinterpret_cast<float2*>(o + i * 8 + 2 * c4) = make_float2(acc[i][2 * h2], acc[i][2 * h2 + 1]);
-        } else {
-#pragma unroll
-          for (int u = 0; u < D / 16; ++u)
-            *reinterpret_cast<float4*>(o + 16 * u + 4 * c4) =
-                make_float4(acc[2 * u][2 * h2], acc[2 * u + 1][2 * h2], acc[2 * u][2 * h2 + 1],
-                            acc[2 * u + 1][2 * h2 + 1]);
+        named_barrier_sync(1, 32 * CW);
+        if (*s_last) {
+          __threadfence();
+          fused_combine<D, F16, C::FEPT>(p, it, up, warp * 32 + lane, 32 * CW);
         }
-        if (c4 == 0) p.part_lse[prow] = lsev;
+        named_barrier_sync(1, 32 * CW);  // s_last is read before the next arrival rewrites it
       }
     }
   }

@@ -14,6 +14,7 @@ struct SplitKernel {
   int threads;      // block size: 32 * (consumer warps + 1), or whole warpgroups
   int launch_regs;  // kernels that move registers between warpgroups (setmaxnreg):
                     // the registers per thread their split needs at launch; 0 otherwise
+  int fused;        // 1: the balanced schedule's combine can be fused into this kernel
 };
 
 // Kernel instance for (head_dim, row tiles, tokens per warp slice,

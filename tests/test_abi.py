@@ -144,6 +144,8 @@ def test_kernel_choice_per_path(lib):
         for s, fmt in other:
             assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_MMA
         assert lib.pa_decode_set_kernel_path(4) == pb.PA_ERR_INVALID_ARG
+        assert lib.pa_decode_set_combine(2) == pb.PA_ERR_INVALID_ARG
+        assert lib.pa_decode_set_combine(-1) == pb.PA_ERR_INVALID_ARG
         assert lib.pa_decode_set_kernel_path(-1) == pb.PA_ERR_INVALID_ARG
     finally:
         pb.set_kernel_path(pb.KERNEL_AUTO)
