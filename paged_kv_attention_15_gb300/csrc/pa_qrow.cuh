@@ -1,6 +1,7 @@
 // Query-row-major tcgen05 decode kernel for 16-bit KV caches (bf16, f16)
-// and work units of 64 query rows: two kv heads of 32 query rows or one kv
-// head of 64 (grouped heads times draft tokens, the draft-block workloads).
+// and work units of M = 64 query rows (two kv heads of 32 query rows or one
+// kv head of 64: grouped heads times draft tokens, the draft-block
+// workloads) or M = 128 (four kv heads of 32).
 //
 // Sources: ROCm blog "Implementing a High-Performance Custom Diffusion
 // Attention Kernel with FlyDSL" (introduction items 1-3: head packing into
@@ -11,25 +12,28 @@
 // outputs as the warp-level split kernel (pa_kernels.cuh); the arithmetic is
 // laid out for the fifth-generation tensor cores:
 //
-//  - the producer copies each page once per 128-byte column chunk, so a
-//    stage tile is [chunk][key row][128 B] with the stage's 64 key rows
-//    (page box, head, row) contiguous in every chunk, 128-byte swizzled;
-//  - S = Q K^T per stage with M = the unit's 64 query rows (tcgen05.mma,
+//  - a stage tile is [chunk][key row][128 B] with the stage's 64 key rows
+//    (page box, head, row) contiguous in every chunk, 128-byte swizzled: for
+//    M = 64 the producer copies each page once per 128-byte column chunk;
+//    for M = 128 a stage is one 16-token page box of the four heads, which
+//    has that layout already and is copied whole;
+//  - S = Q K^T per stage with M = the unit's query rows (tcgen05.mma,
 //    kind::f16, fp32 accumulator in tensor memory), one MMA per 16-column
 //    k-step over all the stage's key rows (N = up to 64): the B descriptor
 //    points straight into the TMA-landed K tile, so K is never copied;
 //  - softmax in warps 0-3: with M = 64 the accumulator row i sits in tensor
 //    memory lane 32 (i / 16) + i % 16, so lane l < 16 of warp w owns query
-//    row 16 w + l and reads only its own kv head's score columns; the row
+//    row 16 w + l (M = 128: row i in lane i, lane l of warp w owns row
+//    32 w + l) and reads only its own kv head's score columns; the row
 //    max and sum are thread-local (no cross-thread reduction), the running
 //    max moves lazily (kMaxSlack), and the thread writes its row of P (16-bit,
 //    zeros in the other head's columns) into a 128-byte-swizzled K-major tile;
-//  - O += P V with M = 64, N = D, one MMA per 16 key rows: V is the B operand
+//  - O += P V with N = D, one MMA per 16 key rows: V is the B operand
 //    in its landed layout (MN-major: dims contiguous, LBO = the chunk stride,
 //    SBO = 8 key rows), O stays in tensor memory for the whole work item and
 //    is read once by the epilogue (O / l, and the log-sum-exp);
 //  - a producer warp fills the stage ring like the warp-level kernel
-//    (produce_ring, one copy per chunk), one MMA warp issues both products:
+//    (produce_ring), one MMA warp issues both products:
 //    S of stage j, then P V of stage j - 1, so the softmax of stage j
 //    overlaps P V of j - 1. (A tcgen05.mma has a fixed cost of tens of
 //    cycles however small its N: a stage takes D / 16 + 4 of them.)
