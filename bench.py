@@ -80,9 +80,10 @@ APPEND_METRIC = "KV-cache append µs/call and achieved HBM GB/s (fraction of 8 T
 SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh"]
 UMMA_KERNEL_SOURCES = ["pa_umma.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
 QROW_KERNEL_SOURCES = ["pa_qrow.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
-KERNEL_NAMES = {1: "pa_split_kernel", 2: "pa_umma_kernel", 3: "pa_qrow_kernel"}
+PAIR_KERNEL_SOURCES = ["pa_pair.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
+KERNEL_NAMES = {1: "pa_split_kernel", 2: "pa_umma_kernel", 3: "pa_qrow_kernel", 4: "pa_pair_kernel"}
 KERNEL_SOURCES = {"pa_split_kernel": SPLIT_KERNEL_SOURCES, "pa_umma_kernel": UMMA_KERNEL_SOURCES,
-                  "pa_qrow_kernel": QROW_KERNEL_SOURCES}
+                  "pa_qrow_kernel": QROW_KERNEL_SOURCES, "pa_pair_kernel": PAIR_KERNEL_SOURCES}
 APPEND_KERNEL_SOURCES = ["pa_append.cu", "pa_ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -478,7 +479,7 @@ def run_ours(args, world, rank, local):
     host = gen.make_inputs(spec)
     pb.lib()
     pb.set_kernel_path({"auto": pb.KERNEL_AUTO, "warp": pb.KERNEL_WARP_MMA, "tcgen05": pb.KERNEL_TCGEN05,
-                        "tcgen05-qrow": pb.KERNEL_TCGEN05_QROW}[args.kernel_path])
+                        "tcgen05-qrow": pb.KERNEL_TCGEN05_QROW, "warp-pair": pb.KERNEL_WARP_PAIR}[args.kernel_path])
     sets = [host.to(dev), host.to(dev)]  # alternated: each step reads KV not in L2
     kname = KERNEL_NAMES[pb.kernel_for_inputs(sets[0])]
     shape = pb.make_shape(sets[0].q, sets[0].k_cache, sets[0].block_tables)
@@ -928,7 +929,7 @@ def main(argv=None):
     ap.add_argument("--kernel-steps", type=int, default=300,
                     help="eager calls timed for the dominant kernel alone (independent of --steps)")
     ap.add_argument("--cpu-workers", type=int, default=0, help="oracle processes for the all-cores run (0: all)")
-    ap.add_argument("--kernel-path", default="auto", choices=["auto", "warp", "tcgen05", "tcgen05-qrow"],
+    ap.add_argument("--kernel-path", default="auto", choices=["auto", "warp", "tcgen05", "tcgen05-qrow", "warp-pair"],
                     help="split kernel: automatic choice, the warp-level MMA kernel, or one of the tcgen05 "
                          "kernels (token-major, query-row-major)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")

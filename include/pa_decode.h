@@ -262,19 +262,22 @@ pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
                             const pa_shape* shape, float scale, void* out, float* lse,
                             int32_t num_splits, pa_stream_t stream);
 
-/* Kernel selection. The decode entry points run one of three split kernels:
+/* Kernel selection. The decode entry points run one of four split kernels:
  * 1 = warp-level MMA kernel (mma.sync tiles of query rows, every shape the
  *     library supports),
  * 2 = token-major tcgen05 kernel (scores and output transposed in tensor
  *     memory; units of 16 or 32 query rows per kv head, D = 128, and fp8
- *     D = 256), or
+ *     D = 256),
  * 3 = query-row-major tcgen05 kernel (bf16 and f16 caches, D = 128, units of
  *     64 query rows: G * T = 32 with two kv heads per unit, or G * T = 64;
- *     pages of at least 16 tokens).
+ *     pages of at least 16 tokens), or
+ * 4 = warp-level MMA kernel with paired consumer roles (one warp computes
+ *     scores, softmax and the P operand, a second one P V and the output;
+ *     fp8 caches, up to 32 query rows per kv head).
  * pa_decode_set_kernel_path(0) (the default) picks per call the kernel
- * measured fastest for the shape; 1 forces the warp-level kernel; 2 and 3
- * use that tcgen05 kernel wherever it has an instance (else the warp-level
- * kernel). Process-wide, for tests and benchmarks; the results agree within
+ * measured fastest for the shape (4 for fp8 caches where it has an
+ * instance, else 1); 1 forces the warp-level kernel; 2, 3 and 4 use that
+ * kernel wherever it has an instance (else the warp-level kernel). Process-wide, for tests and benchmarks; the results agree within
  * rounding. Returns PA_ERR_INVALID_ARG for any other value. */
 pa_status pa_decode_set_kernel_path(int32_t path);
 
@@ -293,7 +296,7 @@ pa_status pa_decode_set_kernel_path(int32_t path);
  * Host-only. */
 pa_status pa_decode_set_combine(int32_t mode);
 
-/* Which kernel (1, 2 or 3, as above) a decode of this shape would run under the
+/* Which kernel (1 to 4, as above) a decode of this shape would run under the
  * current setting; format: 0 bf16 (pa_decode), 1 fp8 (pa_decode_fp8), 2 f16
  * (pa_decode_f16), 3 draft block (pa_decode_tidar*). -1 for an unsupported
  * shape. Host-only. */

@@ -286,13 +286,13 @@ def device_error() -> int:
 
 # Decode kernels: automatic, the warp-level MMA kernel, the token-major
 # tcgen05 kernel, the query-row-major tcgen05 kernel (16-bit, 64-row units).
-KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05, KERNEL_TCGEN05_QROW = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05, KERNEL_TCGEN05_QROW, KERNEL_WARP_PAIR = 0, 1, 2, 3, 4
 _FORMATS = {"bf16": 0, "fp8": 1, "f16": 2, "draft": 3}
 
 
 def set_kernel_path(path: int) -> None:
-    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05
-    or KERNEL_TCGEN05_QROW (see pa_decode_set_kernel_path)."""
+    """Process-wide kernel choice: KERNEL_AUTO, KERNEL_WARP_MMA, KERNEL_TCGEN05,
+    KERNEL_TCGEN05_QROW or KERNEL_WARP_PAIR (see pa_decode_set_kernel_path)."""
     _check(lib().pa_decode_set_kernel_path(int(path)), "pa_decode_set_kernel_path")
 
 
@@ -306,7 +306,7 @@ def set_combine(mode: int) -> None:
 
 
 def kernel_for(shape: PaShape, fmt: str) -> int:
-    """The kernel (KERNEL_WARP_MMA, KERNEL_TCGEN05 or KERNEL_TCGEN05_QROW) a
+    """The kernel (KERNEL_WARP_MMA, KERNEL_TCGEN05, KERNEL_TCGEN05_QROW or KERNEL_WARP_PAIR) a
     decode of this shape and format ('bf16', 'fp8', 'f16', 'draft') runs;
     -1 if unsupported."""
     return int(lib().pa_decode_kernel_for(ctypes.byref(shape), _FORMATS[fmt]))

@@ -21,9 +21,9 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpadecode.so")
 
 SOURCES = ["pa_api.cu", "pa_inst_bf16.cu", "pa_inst_f16.cu", "pa_inst_fp8.cu", "pa_inst_umma.cu",
-           "pa_inst_umma_fp8.cu", "pa_inst_qrow.cu", "pa_append.cu"]
+           "pa_inst_umma_fp8.cu", "pa_inst_qrow.cu", "pa_inst_pair.cu", "pa_append.cu"]
 HEADERS = ["pa_ptx.cuh", "pa_kernels.cuh", "pa_reduce.cuh", "pa_launch.h", "pa_inst_bf16.cu", "pa_tc.cuh",
-           "pa_umma.cuh", "pa_inst_umma.cu", "pa_qrow.cuh"]
+           "pa_umma.cuh", "pa_inst_umma.cu", "pa_qrow.cuh", "pa_pair.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -171,13 +171,13 @@ SplitKernel pick_kernel(Kind kind, int D, int MT, int TSL, int CW) {
 // Query-row-major tcgen05 kernel: M = 64 rows, TS = 64 / H2.
 struct Geom {
   int GT, H2, NHG, M, MT, TS, TSL, BR, lbr, TP, ilv;
-  int path;          // kernel: kPathWarp, kPathUmma or kPathQrow
+  int path;          // kernel: kPathWarp, kPathUmma, kPathQrow or kPathPair
   int chunk_boxes;   // 1: one copy per page and 128-byte column chunk (query-row kernel)
   SplitKernel k;
 };
 
 // Decode kernels (pa_decode_set_kernel_path / pa_decode_kernel_for).
-constexpr int kPathAuto = 0, kPathWarp = 1, kPathUmma = 2, kPathQrow = 3;
+constexpr int kPathAuto = 0, kPathWarp = 1, kPathUmma = 2, kPathQrow = 3, kPathPair = 4;
 
 // Which decode kernel a call may use: automatic, the warp-level MMA kernel
 // only, or one of the tcgen05 kernels wherever it has an instance.
@@ -194,7 +194,9 @@ int ilog2(int x) {
   return l;
 }
 
-bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
+// pair: the split kernel with paired consumer roles (four pairs, each an S
+// warp and a PV warp), laid out like four consumer warps.
+bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g, bool pair = false) {
   const int G = s->num_q_heads / s->num_kv_heads, T = s->q_tokens, P = s->page_size, D = s->head_dim;
   const int GT = G * T, M = H2 * GT;
   if (M > 64 || s->num_kv_heads % H2) return false;
@@ -209,7 +211,7 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
   SplitKernel k{nullptr, 0, 0, 0};
   int TS = 0, TSL = 0, ilv = 1;
-  for (int CW = 8; CW >= pa::kConsumerWarps && !k.fn; CW /= 2) {
+  for (int CW = pair ? pa::kConsumerWarps : 8; CW >= pa::kConsumerWarps && !k.fn; CW /= 2) {
     const int NGW = CW / MT;
     if (NGW < 1 || NGW % HT) continue;
     const int NSL = NGW / HT;
@@ -226,7 +228,8 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
         ilv = TSL / base;
         if (TSL != 16 && TSL != 32 && TSL != 64) continue;
         if (ilv > NSL || NSL % ilv) continue;
-        k = pick_kernel(kind, D, MT, TSL, CW);
+        k = pair ? (kind == Kind::kFp8 ? pa::pair_kernel_fp8(D, MT, TSL) : SplitKernel{nullptr, 0, 0, 0})
+                 : pick_kernel(kind, D, MT, TSL, CW);
         if (k.fn) break;
       }
     }
@@ -237,7 +240,7 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g) {
   g->H2 = H2;
   g->NHG = s->num_kv_heads / H2;
   g->M = M;
-  g->path = kPathWarp;
+  g->path = pair ? kPathPair : kPathWarp;
   g->chunk_boxes = 0;
   g->MT = MT;
   g->TS = TS;
@@ -324,8 +327,9 @@ bool geom_qrow(const pa_shape* s, Kind kind, Geom* g) {
   return true;
 }
 
-// Automatic choice: the warp-level kernel (measured faster on every
-// workload so far); a tcgen05 kernel on request.
+// Automatic choice: for fp8 caches the paired-role warp-level kernel
+// (measured faster on the fp8 workload), else the single-role one; a tcgen05
+// kernel on request.
 int wanted_path() { return g_kernel_path.load(std::memory_order_relaxed); }
 
 // One kv head per unit, or more while a page's box stays under 16 KB: a
@@ -335,13 +339,17 @@ pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out, int path = -1) 
   const int want = path >= 0 ? path : wanted_path();
   if (want == kPathUmma && geom_umma(s, kind, out)) return PA_OK;
   if (want == kPathQrow && geom_qrow(s, kind, out)) return PA_OK;
+  // The paired-role kernel where it has an instance for the shape, else the
+  // single-role warp-level kernel.
   Geom best;
-  if (!geom_for(s, kind, 1, &best)) return PA_ERR_UNSUPPORTED;
+  bool pair = want == kPathPair || (want == kPathAuto && kind == Kind::kFp8);
+  if (pair && !geom_for(s, kind, 1, &best, true)) pair = false;
+  if (!pair && !geom_for(s, kind, 1, &best)) return PA_ERR_UNSUPPORTED;
   const int e = kind == Kind::kFp8 ? 1 : 2;
   for (int cand = 2; cand <= 4; cand *= 2) {
     if ((long)best.BR * best.H2 * s->head_dim * e >= 16384) break;
     Geom g;
-    if (!geom_for(s, kind, cand, &g)) break;
+    if (!geom_for(s, kind, cand, &g, pair)) break;
     best = g;
   }
   *out = best;
@@ -623,7 +631,7 @@ size_t pa_decode_workspace_size(const pa_shape* shape, int32_t num_splits) {
   size_t best = 0;
   for (Kind kind : {Kind::kBf16, Kind::kF16, Kind::kFp8, Kind::kTidar}) {
     if (check_shape(shape, kind) != PA_OK) continue;
-    for (int path : {kPathWarp, kPathUmma, kPathQrow}) {
+    for (int path : {kPathWarp, kPathUmma, kPathQrow, kPathPair}) {
       Plan plan;
       if (make_plan(shape, kind, 0, d, &plan, path) == PA_OK && plan.ws_bytes > best) best = plan.ws_bytes;
     }
@@ -800,7 +808,7 @@ pa_status pa_decode_set_combine(int32_t mode) {
 }
 
 pa_status pa_decode_set_kernel_path(int32_t path) {
-  if (path < kPathAuto || path > kPathQrow) return PA_ERR_INVALID_ARG;
+  if (path < kPathAuto || path > kPathPair) return PA_ERR_INVALID_ARG;
   g_kernel_path.store(path, std::memory_order_relaxed);
   return PA_OK;
 }

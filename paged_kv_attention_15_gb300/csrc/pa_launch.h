@@ -23,6 +23,11 @@ SplitKernel split_kernel_bf16(int head_dim, int row_tiles, int slice, int consum
 SplitKernel split_kernel_fp8(int head_dim, int row_tiles, int slice, int consumer_warps);
 SplitKernel split_kernel_f16(int head_dim, int row_tiles, int slice, int consumer_warps);
 
+// Instance of the split kernel with paired consumer roles (per row tile and
+// slice group an S warp and two PV warps, four such pairs) for (head_dim,
+// row tiles, tokens per warp slice); fn == nullptr if not built.
+SplitKernel pair_kernel_fp8(int head_dim, int row_tiles, int slice);
+
 // Instance of the tcgen05 kernel for (head_dim, query rows per kv head GT,
 // rows per work unit N = kv heads per unit * GT); fn == nullptr if not built.
 SplitKernel umma_kernel_fp8(int head_dim, int GT, int N);

@@ -118,9 +118,10 @@ def test_choose_splits_rejects_bad_shapes(lib):
 
 
 def test_kernel_choice_per_path(lib):
-    """Host-only kernel choice: the warp-level kernel by default; with a
-    tcgen05 path forced, the shapes that kernel covers run it and the others
-    keep the warp-level kernel; invalid paths are rejected."""
+    """Host-only kernel choice: by default the paired-role kernel for fp8
+    caches and the warp-level kernel otherwise; with a path forced, the
+    shapes that kernel covers run it and the others keep the warp-level
+    kernel; invalid paths are rejected."""
     bf16, fp8, f16, draft = 0, 1, 2, 3
     qrow_shapes = [  # (shape, format): 64 query rows per unit, D = 128, 16-bit
         (shape(q_tokens=8, num_q_heads=32, num_kv_heads=8, num_pages=400, max_blocks_per_seq=100), draft),
@@ -136,6 +137,10 @@ def test_kernel_choice_per_path(lib):
         (shape(q_tokens=1, num_q_heads=32, num_kv_heads=1), bf16),    # G = 32 with one kv head: no pair
     ]
     try:
+        for s, fmt in qrow_shapes + other:  # automatic: fp8 caches on the paired-role kernel
+            want = pb.KERNEL_WARP_PAIR if fmt == fp8 else pb.KERNEL_WARP_MMA
+            assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == want
+        pb.set_kernel_path(pb.KERNEL_WARP_MMA)
         for s, fmt in qrow_shapes + other:
             assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_MMA
         pb.set_kernel_path(pb.KERNEL_TCGEN05_QROW)
@@ -143,7 +148,18 @@ def test_kernel_choice_per_path(lib):
             assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_TCGEN05_QROW
         for s, fmt in other:
             assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_MMA
-        assert lib.pa_decode_set_kernel_path(4) == pb.PA_ERR_INVALID_ARG
+        pb.set_kernel_path(pb.KERNEL_WARP_PAIR)
+        pair_shapes = [  # fp8, up to 32 query rows per kv head
+            (shape(q_tokens=1, num_q_heads=32, num_kv_heads=2, head_dim=256), fp8),
+            (shape(q_tokens=1, num_q_heads=16, num_kv_heads=1, head_dim=128), fp8),
+            (shape(), fp8),
+        ]
+        for s, fmt in pair_shapes:
+            assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_PAIR
+        for s, fmt in qrow_shapes + other:
+            if fmt != fp8:
+                assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_MMA
+        assert lib.pa_decode_set_kernel_path(5) == pb.PA_ERR_INVALID_ARG
         assert lib.pa_decode_set_combine(2) == pb.PA_ERR_INVALID_ARG
         assert lib.pa_decode_set_combine(-1) == pb.PA_ERR_INVALID_ARG
         assert lib.pa_decode_set_kernel_path(-1) == pb.PA_ERR_INVALID_ARG

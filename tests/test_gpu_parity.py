@@ -127,6 +127,42 @@ def test_fp8_sweep(case, num_splits):
     check_full(gen.make_inputs(spec(**case)), num_splits)
 
 
+FP8_SCALE_CASES = [
+    dict(),
+    dict(head_dim=256, num_q_heads=32, num_kv_heads=2, context_lens=(1, 40, 700, 2000)),
+    dict(num_q_heads=24, num_kv_heads=1, context_lens=(90, 1000, 3, 257)),
+]
+
+
+@pytest.mark.parametrize("case", FP8_SCALE_CASES, ids=[str(i) for i in range(len(FP8_SCALE_CASES))])
+@pytest.mark.parametrize("num_splits", [0, 1])
+def test_fp8_query_and_value_scale_ranges(case, num_splits):
+    """fp8 KV with query rows of very different magnitudes (each row times
+    2^k, k in [-12, 3]), value scales that grow along every sequence (times
+    2^(8 i / n), i the token, n the context length) and spread inside every
+    stage (times a random 2^[-3, 3]), and key scales times 2^[-2, 2]: the
+    scaled probabilities span far more than the e4m3 range, and every output
+    element still meets the bar (a P operand of fewer than f16's eleven
+    significant bits, or one whose range follows the stage's largest scale,
+    misses it on elements near zero in rows of large outputs)."""
+    inp = gen.make_inputs(spec(kv_format="fp8", **case))
+    rng = np.random.default_rng(99)
+    k = rng.integers(-12, 4, size=inp.q.shape[:-1])
+    inp.q = (inp.q.float() * torch.from_numpy(np.exp2(k)).float()[..., None]).to(torch.bfloat16)
+    bt = inp.block_tables.numpy()
+    lens = inp.context_lens.numpy()
+    P = inp.spec.page_size
+    vs = inp.v_scale.clone()
+    for b in range(bt.shape[0]):
+        for i in range(int(lens[b])):
+            page = int(bt[b, i // P])
+            vs[page, i % P] *= float(2.0 ** np.floor(8 * i / max(1, int(lens[b]))))
+    vs *= torch.from_numpy(np.exp2(rng.integers(-3, 4, size=vs.shape))).float()
+    inp.v_scale = vs
+    inp.k_scale = inp.k_scale * torch.from_numpy(np.exp2(rng.integers(-2, 3, size=inp.k_scale.shape))).float()
+    check_full(inp, num_splits)
+
+
 @pytest.mark.parametrize("q_scale", [4.0, 16.0])
 @pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
 def test_spread_scores_move_the_running_max(kv_format, q_scale):
