@@ -733,15 +733,10 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
       const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
       const int tok_l = it.tok0 + tb + (lane & (TSL - 1));  // this lane's token in stage 0
       const uint32_t ring = sbase + C::OFF_SRING + warp * (kScaleRing * 2 * 32 * 4);
-      // The page of this lane's token in stage jj (loaded one handled stage
-      // before its scale copy, off the copy's dependency chain).
-      auto page_of = [&](int jj) -> int {
-        const int tok = tok_l + jj * TS;
-        return tok < it.tok_end ? __ldg(bt_row + (tok >> lp)) : 0;
-      };
-      auto copy_scales = [&](int jj, int n, int pg) {  // stage jj, the warp's n-th handled stage; pg: page_of(jj)
+      auto copy_scales = [&](int jj, int n) {  // stage jj, the warp's n-th handled stage
         const int tok = tok_l + jj * TS;
         if (tok < it.tok_end) {
+          int pg = __ldg(bt_row + (tok >> lp));
           pg = (unsigned)pg < (unsigned)p.num_pages ? pg : 0;  // outside the pool: page 0's (finite) scales
           const size_t off = ((size_t)pg << lp | (tok & (P - 1))) * p.Hkv + g;
           const uint32_t dst = ring + (n % kScaleRing) * 256 + (lane & (TSL - 1)) * 4;
@@ -753,11 +748,9 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
         cp_async_commit();
       };
       int nh = 0;  // stages this warp handled in this item
-      int pg_next = 0;  // page_of() of the next scale copy
       if (FP8) {
 #pragma unroll
-        for (int a = 0; a < kScaleAhead; ++a) copy_scales(ph + a * p.ilv, a, page_of(ph + a * p.ilv));
-        pg_next = page_of(ph + kScaleAhead * p.ilv);
+        for (int a = 0; a < kScaleAhead; ++a) copy_scales(ph + a * p.ilv, a);
       }
 
       for (int j = 0; j < it.nst; ++j) {
@@ -789,8 +782,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
                              warp * (kScaleRing * 2 * 32) + (nh % kScaleRing) * 64;  // [token - tb]
           const float* vsc = ksc + 32;
           if (FP8) {
-            copy_scales(j + kScaleAhead * p.ilv, nh + kScaleAhead, pg_next);
-            pg_next = page_of(j + (kScaleAhead + 1) * p.ilv);
+            copy_scales(j + kScaleAhead * p.ilv, nh + kScaleAhead);
             cp_async_wait<kScaleAhead>();  // this stage's group has landed
             __syncwarp();                  // ... for every lane's copies
             ++nh;
