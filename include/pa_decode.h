@@ -272,11 +272,12 @@ pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
  *     64 query rows: G * T = 32 with two kv heads per unit, or G * T = 64;
  *     pages of at least 16 tokens), or
  * 4 = warp-level MMA kernel with paired consumer roles (one warp computes
- *     scores, softmax and the P operand, a second one P V and the output;
- *     fp8 caches, up to 32 query rows per kv head).
+ *     scores, softmax and the P operand, two more P V and the output; fp8
+ *     caches with up to 32 query rows per kv head, and 16-bit caches at
+ *     D = 128 with units of 33-64 query rows).
  * pa_decode_set_kernel_path(0) (the default) picks per call the kernel
  * measured fastest for the shape (4 for fp8 caches where it has an
- * instance, else 1); 1 forces the warp-level kernel; 2, 3 and 4 use that
+ * instance, else 1: the 16-bit units of kernel 4 measured slower); 1 forces the warp-level kernel; 2, 3 and 4 use that
  * kernel wherever it has an instance (else the warp-level kernel). Process-wide, for tests and benchmarks; the results agree within
  * rounding. Returns PA_ERR_INVALID_ARG for any other value. */
 pa_status pa_decode_set_kernel_path(int32_t path);

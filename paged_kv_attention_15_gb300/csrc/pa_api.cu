@@ -228,7 +228,8 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g, bool pair = false) 
         ilv = TSL / base;
         if (TSL != 16 && TSL != 32 && TSL != 64) continue;
         if (ilv > NSL || NSL % ilv) continue;
-        k = pair ? (kind == Kind::kFp8 ? pa::pair_kernel_fp8(D, MT, TSL) : SplitKernel{nullptr, 0, 0, 0})
+        k = pair ? (kind == Kind::kFp8 ? pa::pair_kernel_fp8(D, MT, TSL)
+                                       : pa::pair_kernel_16(D, kind == Kind::kF16, MT, TSL))
                  : pick_kernel(kind, D, MT, TSL, CW);
         if (k.fn) break;
       }
@@ -341,19 +342,27 @@ pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out, int path = -1) 
   if (want == kPathQrow && geom_qrow(s, kind, out)) return PA_OK;
   // The paired-role kernel where it has an instance for the shape, else the
   // single-role warp-level kernel.
-  Geom best;
-  bool pair = want == kPathPair || (want == kPathAuto && kind == Kind::kFp8);
-  if (pair && !geom_for(s, kind, 1, &best, true)) pair = false;
-  if (!pair && !geom_for(s, kind, 1, &best)) return PA_ERR_UNSUPPORTED;
+  // From the smallest unit with an instance (one kv head for the
+  // single-role kernel; the paired kernel's 16-bit instances start at 64
+  // query rows), grow it while its page box stays under 16 KB.
   const int e = kind == Kind::kFp8 ? 1 : 2;
-  for (int cand = 2; cand <= 4; cand *= 2) {
-    if ((long)best.BR * best.H2 * s->head_dim * e >= 16384) break;
-    Geom g;
-    if (!geom_for(s, kind, cand, &g, pair)) break;
-    best = g;
-  }
-  *out = best;
-  return PA_OK;
+  auto search = [&](bool pair, Geom* best) {
+    bool have = false;
+    for (int cand = 1; cand <= 4; cand *= 2) {
+      if (have && (long)best->BR * best->H2 * s->head_dim * e >= 16384) break;
+      Geom g;
+      if (!geom_for(s, kind, cand, &g, pair)) {
+        if (have) break;
+        continue;
+      }
+      *best = g;
+      have = true;
+    }
+    return have;
+  };
+  const bool pair = want == kPathPair || (want == kPathAuto && kind == Kind::kFp8);
+  if (pair && search(true, out)) return PA_OK;
+  return search(false, out) ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
 // The launch plan of a call: mode, grid and workspace.

@@ -25,4 +25,13 @@ SplitKernel pair_kernel_fp8(int head_dim, int row_tiles, int slice) {
   return SplitKernel{nullptr, 0, 0, 0};
 }
 
+// 16-bit caches: the draft-block geometry, four row tiles (64 query rows per
+// unit), every pair taking the whole stage (32 or 64 tokens).
+SplitKernel pair_kernel_16(int head_dim, bool f16, int row_tiles, int slice) {
+  if (head_dim != 128 || row_tiles != 4) return SplitKernel{nullptr, 0, 0, 0};
+  if (slice == 32) return f16 ? pair_entry<128, 4, kKvF16, 32>() : pair_entry<128, 4, kKvBf16, 32>();
+  if (slice == 64) return f16 ? pair_entry<128, 4, kKvF16, 64>() : pair_entry<128, 4, kKvBf16, 64>();
+  return SplitKernel{nullptr, 0, 0, 0};
+}
+
 }  // namespace pa

@@ -27,6 +27,7 @@ SplitKernel split_kernel_f16(int head_dim, int row_tiles, int slice, int consume
 // slice group an S warp and two PV warps, four such pairs) for (head_dim,
 // row tiles, tokens per warp slice); fn == nullptr if not built.
 SplitKernel pair_kernel_fp8(int head_dim, int row_tiles, int slice);
+SplitKernel pair_kernel_16(int head_dim, bool f16, int row_tiles, int slice);
 
 // Instance of the tcgen05 kernel for (head_dim, query rows per kv head GT,
 // rows per work unit N = kv heads per unit * GT); fn == nullptr if not built.

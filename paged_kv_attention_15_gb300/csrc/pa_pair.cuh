@@ -87,7 +87,7 @@ struct PCfg {
   static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;
   static_assert(D % 64 == 0 && (!FP8 || D >= 128), "unsupported head_dim");
   static_assert(MT == 1 || MT == 2 || MT == 4, "unsupported row tiles");
-  static_assert(TSL == 16 || TSL == 32, "unsupported warp slice");
+  static_assert(TSL == 16 || TSL == 32 || TSL == 64, "unsupported warp slice");
   static_assert(DH % CHW == 0, "merge rounds");
   static_assert((2 * 8 + 5 + 2 * PAIRS * NMSG) * 8 <= BARS, "barrier area");
 };

@@ -156,7 +156,12 @@ def test_kernel_choice_per_path(lib):
         ]
         for s, fmt in pair_shapes:
             assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_PAIR
-        for s, fmt in qrow_shapes + other:
+        # 16-bit: the paired kernel's units of four row tiles at D = 128
+        # (33-64 query rows), the warp-level kernel elsewhere.
+        pair16 = qrow_shapes + [other[3]]
+        for s, fmt in pair16:
+            assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_PAIR
+        for s, fmt in other[:3] + other[4:]:
             if fmt != fp8:
                 assert lib.pa_decode_kernel_for(ctypes.byref(s), fmt) == pb.KERNEL_WARP_MMA
         assert lib.pa_decode_set_kernel_path(5) == pb.PA_ERR_INVALID_ARG

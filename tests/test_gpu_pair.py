@@ -1,12 +1,12 @@
 """The split kernel with paired consumer roles (an S warp computing scores,
-softmax and the P operand, a PV warp holding the output; messages through
+softmax and the P operand, two PV warps holding the output; messages through
 shared memory) against the fp64 oracle, through the C ABI.
 
 Every case forces that kernel (pa_decode_set_kernel_path(4)) and checks that
 the library reports it for the shape, so a silent fall-back to another
-kernel cannot pass. The bar is the fp8 one of test_gpu_parity.py:
-|gpu - oracle| <= 2e-2 + 2e-2 |oracle| on out and |lse_gpu - lse_oracle| <=
-1e-3.
+kernel cannot pass. The bars are those of test_gpu_parity.py:
+|gpu - oracle| <= tol + tol |oracle| on out, tol = 2e-2 for fp8 KV and 1e-2
+for 16-bit KV, and |lse_gpu - lse_oracle| <= 1e-3.
 """
 
 import dataclasses
@@ -157,6 +157,73 @@ def test_full_size_fp8_workload():
     out, lse = run(inp, 0)
     ref_out, ref_lse = oracle.decode(ora(inp), inp.scale)
     check(out, lse, ref_out, ref_lse)
+
+
+def draft_spec(**kw):
+    # the TiDAR geometry: 8 draft tokens x 4 query heads = 32 rows per kv head
+    base = dict(batch=4, q_tokens=8, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                context_lens=(1, 100, 16, 333), kv_format="bf16", draft_scratch=True, seed=53)
+    base.update(kw)
+    return gen.custom_spec(**base)
+
+
+DRAFT_CASES = [
+    dict(),                                                              # two kv heads of 32 rows per unit
+    dict(draft_block=1),                                                 # causal draft
+    dict(draft_block=3, context_lens=(0, 17, 64, 200)),                  # block-masked draft, empty prefix
+    dict(context_lens=(15, 16, 17, 33)),                                 # partial last pages
+    dict(page_size=32, context_lens=(31, 32, 65, 300)),
+    dict(page_size=64, context_lens=(64, 1, 700, 65)),
+    dict(num_q_heads=16, num_kv_heads=4, batch=3, context_lens=(5, 400, 77)),  # two head groups
+    dict(q_tokens=16, num_q_heads=8, num_kv_heads=2, draft_block=4),     # 64 rows of one kv head, 64-token slices
+    dict(q_tokens=16, num_q_heads=8, num_kv_heads=2, draft_block=4, page_size=64, context_lens=(64, 129, 3, 500)),
+    dict(q_tokens=4, num_q_heads=16, num_kv_heads=2),                    # 4 draft tokens x 8 heads
+    dict(draft_scratch=False, q_tokens=1, num_q_heads=64, num_kv_heads=2),  # no draft: G = 32
+    dict(draft_scratch=False, q_tokens=1, num_q_heads=64, num_kv_heads=1, context_lens=(0, 1000, 64, 63)),
+    dict(draft_scratch=False, q_tokens=1, num_q_heads=64, num_kv_heads=2, kv_format="f16"),
+    dict(batch=9, ctx_range=(1, 2000), context_lens=None, pool_pages=1400),
+]
+
+
+def draft_full(inp, num_splits):
+    oi = ora(inp)
+    if inp.spec.draft_block is not None:
+        oi["draft_block"] = inp.spec.draft_block
+    ref_out, ref_lse = oracle.decode(oi, inp.scale)
+    tol = 1e-2
+    out, lse = run(inp, num_splits)
+    assert np.all(np.isfinite(out)), "non-finite output"
+    excess = np.abs(out - ref_out) - (tol + tol * np.abs(ref_out))
+    assert excess.max() <= 0, f"out: max excess {excess.max():.3g}"
+    inf = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), inf), "lse -inf pattern differs"
+    d = np.abs(lse[~inf] - ref_lse[~inf])
+    assert d.size == 0 or d.max() <= LSE_TOL, f"lse: {d.max():.3g}"
+
+
+@pytest.mark.parametrize("case", DRAFT_CASES, ids=[str(i) for i in range(len(DRAFT_CASES))])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_pair_16bit_draft_geometry(case, num_splits):
+    """16-bit caches on the paired-role kernel: units of 64 query rows (four
+    row tiles, one pair each), slices of the whole stage (32 or 64 tokens),
+    draft-block scratch and masks."""
+    draft_full(gen.make_inputs(draft_spec(**case)), num_splits)
+
+
+def test_pair_16bit_matches_the_single_role_kernel():
+    """The single-role kernel slices these stages differently (two warps per
+    row tile), so the two agree within rounding, not bit for bit."""
+    for case in (dict(), dict(q_tokens=16, draft_block=4), dict(draft_scratch=False, q_tokens=1, num_q_heads=64)):
+        inp = gen.make_inputs(draft_spec(**case))
+        dev = inp.to("cuda")
+        for ns in (0, 3):
+            a = run(inp, ns, dev=dev)
+            pb.set_kernel_path(pb.KERNEL_WARP_MMA)
+            out, lse = pb.decode_inputs(dev, num_splits=ns)
+            torch.cuda.synchronize()
+            pb.set_kernel_path(pb.KERNEL_WARP_PAIR)
+            assert np.abs(a[0] - out.float().cpu().double().numpy()).max() <= 2e-2
+            assert np.abs(a[1] - lse.cpu().double().numpy()).max() <= LSE_TOL
 
 
 def test_graph_capture_replays_like_eager():
