@@ -1,7 +1,8 @@
 // Split kernel with paired consumer roles (included by the instance units).
 //
 // Same operation, schedule, ring, partials and outputs as pa_split_kernel
-// (pa_kernels.cuh), with each consumer's per-stage chain cut in two. Sources:
+// (pa_kernels.cuh), with each consumer's per-stage chain split between
+// three warps. Sources:
 // the MSLK pull request "[ROCm] Add FlyDSL paged-attention decode backend
 // (dense + fp8) with benchmark" (Kernels: head-packed matrix-core decode,
 // native fp8 e4m3fn KV with symmetric per-token scale, split-K partials) and
@@ -17,8 +18,9 @@
 // computes the scores, the online max and sum and the P operand (fp8: times
 // the per-token V scale) and sends P with the rows' rescale factors to two
 // PV warps (warps 4-7: output columns [0, D/2); warps 8-11: [D/2, D))
-// through a two-slot message ring in shared memory (mbarriers; all lanes
-// arrive, every wait bounded); each PV warp holds its half of the output
+// through a message slot in shared memory (mbarriers; all lanes arrive,
+// every wait bounded; the S warp runs up to one slice ahead); each PV warp
+// holds its half of the output
 // accumulator, rescales it, runs P V on its half of the stage's value
 // columns and releases the stage. The three chains overlap across stages.
 // Closing a work item the S warp sends its running max and sum, and the PV
