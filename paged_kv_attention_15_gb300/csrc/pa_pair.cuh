@@ -432,7 +432,14 @@ __global__ void __launch_bounds__(PCfg<D, MT, KV == kKvFp8, TSL>::THREADS, 1)
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            constexpr float slack = FP8 ? 0.f : kMaxSlack;
+            // fp8: P~ = p * v_scale is f16, so the running max may lag by
+            // kMaxSlack (p <= 2^8) only while every v_scale of the slice is
+            // below 2^7 (P~ < 2^15); else it tracks the exact max.
+            float slack = kMaxSlack;
+            if (FP8) {
+              const uint32_t vb = (lane < TSL && tb + lane < valid) ? __float_as_uint(fabsf(vsc[lane])) : 0u;
+              slack = __reduce_max_sync(0xffffffffu, vb) < 0x43000000u ? kMaxSlack : 0.f;  // 128.0f
+            }
             const float mn0 = mx0 > m0 + slack ? mx0 : m0, mn1 = mx1 > m1 + slack ? mx1 : m1;
             const float mu0 = mn0 == NEG_INF ? 0.f : mn0;
             const float mu1 = mn1 == NEG_INF ? 0.f : mn1;

