@@ -756,9 +756,7 @@ def run_serving_step(args, host, dev, pb, nbytes, world):
     B, Hkv, D = spec.batch, spec.num_kv_heads, spec.head_dim
     devset = host.to(dev)
     gen_new = torch.Generator().manual_seed(spec.seed + 77)
-    dt = torch.float16 if spec.kv_format == "f16" else torch.bfloat16
-    if spec.kv_format == "f16":
-        return None  # the append takes bf16 rows
+    dt = torch.float16 if spec.kv_format == "f16" else torch.bfloat16  # (f16 rows into an f16 cache)
     k_new = torch.randn(B, 1, Hkv, D, generator=gen_new).to(dt).pin_memory()
     v_new = torch.randn(B, 1, Hkv, D, generator=gen_new).to(dt).pin_memory()
     per_step = {"q": host.q, "block_tables": host.block_tables, "context_lens": host.context_lens}

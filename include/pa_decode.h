@@ -210,6 +210,8 @@ pa_status pa_decode_reduce_f16(const float* part_out, const float* part_lse, int
  * k_cache[page][slot][g][:].
  *  - k_new, v_new: bf16 [B, T, Hkv, D], contiguous; k_cache, v_cache: bf16
  *    [num_pages, P, Hkv, D]. D in {64, 128, 256}; num_q_heads is not used.
+ *    The rows are copied bit for bit, so f16 rows into f16 caches (the
+ *    caches of pa_decode_f16) take the same call.
  *  - context_lens is read, not advanced: the caller adds T after the call.
  *  - Positions at or past max_blocks_per_seq * P, and page ids outside
  *    [0, num_pages), are skipped (nothing written, no fault).

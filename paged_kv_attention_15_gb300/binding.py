@@ -204,11 +204,15 @@ def decode_inputs(inp, **kw):
 def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
               k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor] = None,
               v_scale: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Appends k_new/v_new [B, T, Hkv, D] (bf16) at positions context_lens[b] + t
-    through pa_kv_append, or pa_kv_append_fp8 when the caches are uint8
-    (e4m3fn codes; k_scale/v_scale [num_pages, P, Hkv] fp32 are written)."""
+    """Appends k_new/v_new [B, T, Hkv, D] (bf16, or f16 into f16 caches) at
+    positions context_lens[b] + t through pa_kv_append, or pa_kv_append_fp8
+    when the caches are uint8 (e4m3fn codes; k_scale/v_scale [num_pages, P,
+    Hkv] fp32 are written)."""
     _need_contig(k_new=k_new, v_new=v_new, block_tables=block_tables, context_lens=context_lens,
                  k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale)
+    want = torch.bfloat16 if k_cache.dtype == torch.uint8 else k_cache.dtype
+    if k_new.dtype != want or v_new.dtype != want or v_cache.dtype != k_cache.dtype:
+        raise TypeError(f"kv_append: new rows must be {want} for a {k_cache.dtype} cache")
     B, T, Hkv, D = k_new.shape
     shape = PaShape(B, T, Hkv, Hkv, D, k_cache.shape[1], k_cache.shape[0], block_tables.shape[1])
     args = [_ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens), ctypes.byref(shape),

@@ -350,7 +350,8 @@ def custom_spec(name="custom", **kw) -> DecodeSpec:
 @dataclasses.dataclass(frozen=True)
 class AppendSpec:
     """Shape and value recipe of one KV-cache append: B sequences that cache
-    C_b tokens each receive T new tokens (K and V rows N(0,1) in bf16)."""
+    C_b tokens each receive T new tokens (K and V rows N(0,1) in bf16, or in
+    f16 for an f16 cache)."""
 
     name: str
     batch: int
@@ -419,10 +420,11 @@ def make_append_inputs(spec: AppendSpec) -> AppendInputs:
         page_size=spec.page_size, context_lens=tuple(int(c) + T for c in lens), kv_format=spec.kv_format,
         pool_pages=spec.pool_pages, max_blocks_per_seq=spec.max_blocks_per_seq, seed=spec.seed))
     rows = max(1, _CHUNK_ELEMS // (T * Hkv * D))
+    t16 = torch.float16 if spec.kv_format == "f16" else torch.bfloat16  # new rows: the cache's type (fp8: bf16)
     return AppendInputs(
         spec=spec,
-        k_new=_normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_KNEW, rows),
-        v_new=_normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_VNEW, rows),
+        k_new=_normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_KNEW, rows, t16),
+        v_new=_normal_bf16((B, T, Hkv, D), spec.seed, _STREAM_VNEW, rows, t16),
         block_tables=base.block_tables,
         context_lens=torch.from_numpy(np.asarray(lens, dtype=np.int32)),
         k_cache=base.k_cache, v_cache=base.v_cache, k_scale=base.k_scale, v_scale=base.v_scale)

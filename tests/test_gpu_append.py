@@ -1,7 +1,8 @@
 """GPU KV-cache append (pa_kv_append / pa_kv_append_fp8, through the C ABI)
 against the CPU oracle: the written caches (and fp8 scales) must equal the
-oracle's bit for bit, since the append copies bf16 rows and takes every
-fp8 rounding decision in float32 exactly as the oracle does."""
+oracle's bit for bit, since the append copies 16-bit rows (bf16, or f16 into
+f16 caches) and takes every fp8 rounding decision in float32 exactly as the
+oracle does."""
 
 import dataclasses
 
@@ -43,7 +44,7 @@ def oracle_append(inp, rows=None):
 
 def bits_of(t):
     t = t.cpu()
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16)
     if t.dtype == torch.float32:
         return t.numpy().view(np.uint32)
@@ -72,14 +73,14 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("kv_format", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_append_matches_oracle_bit_exact(case, kv_format):
     inp = gen.make_append_inputs(spec(kv_format=kv_format, **case))
     assert_caches_equal(gpu_append(inp), oracle_append(inp))
 
 
-@pytest.mark.parametrize("kv_format", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
 def test_positions_past_capacity_and_bad_pages_are_skipped(kv_format):
     inp = gen.make_append_inputs(spec(kv_format=kv_format, new_tokens=6, context_lens=(40, 42, 0, 3),
                                       max_blocks_per_seq=3))
@@ -145,7 +146,7 @@ def test_fp8_quantiser_stress_bit_exact(head_dim):
     assert_caches_equal(gpu_append(inp), oracle_append(inp))
 
 
-@pytest.mark.parametrize("kv_format", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
 def test_decode_after_append_matches_oracle(kv_format):
     """Append T tokens on the GPU, then decode over C_b + T tokens: the result
     equals the oracle's decode of the oracle-appended cache."""
@@ -155,7 +156,8 @@ def test_decode_after_append_matches_oracle(kv_format):
     ref = oracle_append(inp)
     B, T, Hkv, D = inp.k_new.shape
     Hq = 4 * Hkv
-    q = torch.randn(B, 1, Hq, D, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    q = torch.randn(B, 1, Hq, D, generator=torch.Generator().manual_seed(3)).to(
+        torch.float16 if kv_format == "f16" else torch.bfloat16)
     ctx = inp.context_lens + T
     out, lse = pb.decode(q.cuda(), dev.k_cache, dev.v_cache, dev.block_tables, ctx.cuda(), D ** -0.5,
                          k_scale=dev.k_scale, v_scale=dev.v_scale)
