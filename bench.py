@@ -512,6 +512,17 @@ def run_ours(args, world, rank, local):
                 pb.decode_inputs(sets[j], out=outs[j], lse=lses[j], workspace=wss[j], num_splits=args.num_splits)
             graphs.append(g)
     torch.cuda.synchronize(dev)
+    # Not an empty graph: a replay rewrites the output, NaN-filled first
+    # (every output row is written, zeros for a sequence with no keys).
+    for j in range(2):
+        outs[j].fill_(float("nan"))
+    with torch.cuda.stream(cap_stream):
+        for j in range(2):
+            graphs[j].replay()
+    torch.cuda.synchronize(dev)
+    for j in range(2):
+        if not bool(torch.isfinite(outs[j]).all()):
+            raise RuntimeError("a captured decode graph did not write its output")
     with torch.cuda.stream(cap_stream):
         for i in range(args.warmup):
             graphs[i & 1].replay()
@@ -658,6 +669,18 @@ def run_append(args, world, rank, local):
             with torch.cuda.graph(g, stream=cap_stream):
                 call(sets[j], cap_stream)
             graphs.append(g)
+    torch.cuda.synchronize(dev)
+    # Not an empty graph: a replay writes the new rows into caches cleared first.
+    for j in range(2):
+        sets[j].k_cache.zero_()
+    with torch.cuda.stream(cap_stream):
+        for j in range(2):
+            graphs[j].replay()
+    torch.cuda.synchronize(dev)
+    for j in range(2):
+        if not bool(sets[j].k_cache.view(torch.uint8).any()):
+            raise RuntimeError("a captured append graph did not write the cache")
+    with torch.cuda.stream(cap_stream):
         for i in range(args.warmup):
             graphs[i & 1].replay()
     torch.cuda.synchronize(dev)
