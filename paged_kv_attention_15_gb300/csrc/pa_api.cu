@@ -178,6 +178,7 @@ struct Geom {
 
 // Decode kernels (pa_decode_set_kernel_path / pa_decode_kernel_for).
 constexpr int kPathAuto = 0, kPathWarp = 1, kPathUmma = 2, kPathQrow = 3, kPathPair = 4;
+constexpr int kPairItemPages = 8, kItemPages = 4;  // Plan::item_w of the paired-role kernel, of the others
 
 // Which decode kernel a call may use: automatic, the warp-level MMA kernel
 // only, or one of the tcgen05 kernels wherever it has an instance.
@@ -375,6 +376,7 @@ struct Plan {
   size_t ws_bytes = 0;
   size_t part_lse_off = 0;
   size_t count_off = 0;   // balanced mode: per-unit arrival counters of the fused combine
+  int item_w = 0;         // balanced mode: virtual pages charged per work item (SplitParams::item_w)
 };
 
 // path: the kernel selection to plan for (-1: the current setting).
@@ -387,13 +389,20 @@ pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d
   const int M = geo.M, units = B * geo.NHG;
   Plan p;
   p.geo = geo;
+  // The fixed cost of a work item (Q load and conversion, merge, partial
+  // write) in pages of the balanced schedule: on the paired-role kernel's fp8
+  // workload a CTA's extra item cost about 3.3 us, some seven pages' worth
+  // (8: split kernel 121.5 -> 118.8 us); 4 for the other kernels (gqa_d64
+  // 63.5 -> 61.5 us, the other workloads unchanged).
+  p.item_w = geo.path == kPathPair ? kPairItemPages : kItemPages;
   if (num_splits == 0) {
     const size_t smem = (size_t)k.smem_fixed + (size_t)(2 * B + 1) * 4;
     if (smem <= (size_t)d->smem_optin) {
       p.balanced = true;
       // One CTA per SM, but no more CTAs than the flattened pages can fill
       // (more would only add empty shares for the reduce to skip).
-      const long long most = (long long)units * (s->max_blocks_per_seq + (kind == Kind::kTidar ? 1 : 0));
+      const long long most =
+          (long long)units * (s->max_blocks_per_seq + (kind == Kind::kTidar ? 1 : 0) + p.item_w);
       p.grid = most < d->sms ? (int)(most < 1 ? 1 : most) : d->sms;
       p.smem = smem;
       const size_t slots = (size_t)units + p.grid;
@@ -547,6 +556,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
   p.tidar = a.kind == Kind::kTidar ? 1 : 0;
   p.draft_block = a.draft_block > 0 && a.draft_block < T ? a.draft_block : T;
   p.grid = plan.grid;
+  p.item_w = plan.balanced ? plan.item_w : 0;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
   if (plan.ws_bytes) {
     p.part_o = static_cast<float*>(a.workspace);
@@ -591,6 +601,7 @@ pa_status run_decode_impl(const CallArgs& a, cudaEvent_t ev_start, cudaEvent_t e
     r.P = P;
     r.max_blocks = s.max_blocks_per_seq;
     r.tidar = p.tidar;
+    r.item_w = p.item_w;
     r.num_splits = plan.balanced ? 0 : plan.splits;
     r.out_f16 = a.kind == Kind::kF16 ? 1 : 0;
     r.grid = plan.grid;

@@ -106,6 +106,7 @@ struct SplitParams {
   int tidar;       // 1: each sequence also attends to its T scratch tokens
   int draft_block; // draft token t sees scratch tokens [0, min(T, (t / draft_block + 1) * draft_block))
   int grid;        // CTAs of a balanced launch
+  int item_w;      // balanced schedule: virtual pages charged for starting a work item on a unit
   float scale_log2;
 };
 
@@ -119,6 +120,7 @@ struct ReduceParams {
   int H2, NHG, GT;
   int num_splits;  // >= 1: explicit layout [B][T][Hq][S]; 0: balanced-launch slots
   int grid;        // CTAs of the balanced split launch
+  int item_w;      // the split launch's item_w
   int out_f16;     // 1: out holds f16 (else bf16)
 };
 
@@ -188,6 +190,15 @@ __device__ __forceinline__ int clamp_ctx(const SplitParams& p, int c) {
   return c < 0 ? 0 : (c > cap ? cap : c);
 }
 
+// Virtual pages of a (sequence, head group) unit in the balanced schedule:
+// its pages and the draft-block scratch, plus item_w for the fixed cost of a
+// work item on it (Q load, merge, partial write), so that a CTA whose share
+// starts a unit takes that many fewer pages; none for a unit with no work.
+__device__ __forceinline__ int unit_vpages(int ctx, int P, int tidar, int item_w) {
+  const int v = (ctx + P - 1) / P + tidar;
+  return v > 0 ? v + item_w : 0;
+}
+
 __device__ __forceinline__ void cursor_init(const SplitParams& p, const int* s_start, Cursor& cur) {
   cur.done = 0;
   if (p.num_splits == 0) {
@@ -240,10 +251,12 @@ __device__ __forceinline__ bool next_item(const SplitParams& p, const int* s_ctx
     const int vp1 = (int)(end - us);
     const int ctx = s_ctx[b];
     const int n = (ctx + P - 1) / P;
+    // virtual pages [0, item_w) of the unit carry no keys; its pages follow
+    const int rp0 = max(vp0 - p.item_w, 0), rp1 = max(vp1 - p.item_w, 0);
     it.b = b;
     it.hg = hg;
-    it.tok0 = vp0 * P;
-    it.tok_end = max(it.tok0, min(min(vp1, n) * P, ctx));
+    it.tok0 = rp0 * P;
+    it.tok_end = max(it.tok0, min(min(rp1, n) * P, ctx));
     it.scratch = (p.tidar && vp1 == nv) ? 1 : 0;  // the scratch is the unit's last virtual page
     it.part = (us >= cur.f0 && ue <= cur.f1) ? -1 : (b * NHG + hg + (int)blockIdx.x);
     cur.f = end;
@@ -592,7 +605,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
       if (lane == 0) s_start[0] = 0;
       for (int base = 0; base < p.B; base += 32) {
         const int i = base + lane;
-        int v = i < p.B ? (s_ctx[i] + p.P - 1) / p.P + p.tidar : 0;
+        int v = i < p.B ? unit_vpages(s_ctx[i], p.P, p.tidar, p.item_w) : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int n = __shfl_up_sync(0xffffffffu, v, o);

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
       if (lane == 0) s_start[0] = 0;
       for (int base = 0; base < p.B; base += 32) {
         const int i = base + lane;
-        int v = i < p.B ? (s_ctx[i] + p.P - 1) / p.P + p.tidar : 0;
+        int v = i < p.B ? unit_vpages(s_ctx[i], p.P, p.tidar, p.item_w) : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int n = __shfl_up_sync(0xffffffffu, v, o);

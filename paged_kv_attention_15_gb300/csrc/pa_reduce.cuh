@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(128, 8) pa_reduce_balanced_kernel(const __grid
   for (int i = threadIdx.x; i < p.B; i += 128) {
     int c = __ldg(p.context_lens + i);
     c = c < 0 ? 0 : (c > cap ? cap : c);
-    const long long nv = (c + p.P - 1) / p.P + p.tidar;
+    const long long nv = unit_vpages(c, p.P, p.tidar, p.item_w);
     total += nv;
     if (i < b) before += nv;
   }
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(128, 8) pa_reduce_balanced_kernel(const __grid
   before = s_sum[0][0] + s_sum[0][1] + s_sum[0][2] + s_sum[0][3];
   total = s_sum[1][0] + s_sum[1][1] + s_sum[1][2] + s_sum[1][3];
   cb = cb < 0 ? 0 : (cb > cap ? cap : cb);
-  const long long nvb = (cb + p.P - 1) / p.P + p.tidar;
+  const long long nvb = unit_vpages(cb, p.P, p.tidar, p.item_w);
   if (nvb == 0) return;
   const long long N = total * p.NHG;
   const long long us = before * p.NHG + (long long)hg * nvb;
