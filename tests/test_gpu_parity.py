@@ -127,6 +127,29 @@ def test_fp8_sweep(case, num_splits):
     check_full(gen.make_inputs(spec(**case)), num_splits)
 
 
+ITEM_WEIGHT_CASES = [
+    dict(batch=40, ctx_range=(1, 48), context_lens=None, pool_pages=200),                 # 1-3 pages each
+    dict(batch=40, ctx_range=(1, 48), context_lens=None, pool_pages=200, kv_format="fp8"),  # paired kernel
+    dict(batch=24, ctx_range=(0, 40), context_lens=None, pool_pages=120, q_tokens=8, draft_scratch=True),
+    dict(batch=7, context_lens=(1, 0, 17, 2, 33, 0, 5), num_q_heads=16, num_kv_heads=8),
+]
+
+
+@pytest.mark.parametrize("case", ITEM_WEIGHT_CASES, ids=[str(i) for i in range(len(ITEM_WEIGHT_CASES))])
+@pytest.mark.parametrize("combine", [pb.COMBINE_SEPARATE, pb.COMBINE_FUSED])
+def test_balanced_schedule_item_weights(case, combine):
+    """The balanced schedule charges each (sequence, head group) unit a few
+    virtual pages ahead of its keys: with many short sequences, CTA shares
+    start, end or lie wholly inside those pages (empty pieces), and the
+    combined rows still match the oracle."""
+    inp = gen.make_inputs(spec(**case))
+    pb.set_combine(combine)
+    try:
+        check_full(inp, 0)
+    finally:
+        pb.set_combine(pb.COMBINE_SEPARATE)
+
+
 FP8_SCALE_CASES = [
     dict(),
     dict(head_dim=256, num_q_heads=32, num_kv_heads=2, context_lens=(1, 40, 700, 2000)),
