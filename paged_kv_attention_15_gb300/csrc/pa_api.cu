@@ -395,6 +395,9 @@ pa_status make_plan(const pa_shape* s, Kind kind, int num_splits, DeviceState* d
   // (8: split kernel 121.5 -> 118.8 us); 4 for the other kernels (gqa_d64
   // 63.5 -> 61.5 us, the other workloads unchanged).
   p.item_w = geo.path == kPathPair ? kPairItemPages : kItemPages;
+  // A call too small to give every SM several pages gains nothing from the
+  // weights, only more CTAs with empty shares.
+  if ((long long)units * s->max_blocks_per_seq < 4LL * d->sms) p.item_w = 0;
   if (num_splits == 0) {
     const size_t smem = (size_t)k.smem_fixed + (size_t)(2 * B + 1) * 4;
     if (smem <= (size_t)d->smem_optin) {

@@ -127,11 +127,16 @@ def test_fp8_sweep(case, num_splits):
     check_full(gen.make_inputs(spec(**case)), num_splits)
 
 
+# Block tables 64 pages wide: the host charges the weights only to calls
+# whose page bound gives every SM several pages.
 ITEM_WEIGHT_CASES = [
-    dict(batch=40, ctx_range=(1, 48), context_lens=None, pool_pages=200),                 # 1-3 pages each
-    dict(batch=40, ctx_range=(1, 48), context_lens=None, pool_pages=200, kv_format="fp8"),  # paired kernel
-    dict(batch=24, ctx_range=(0, 40), context_lens=None, pool_pages=120, q_tokens=8, draft_scratch=True),
-    dict(batch=7, context_lens=(1, 0, 17, 2, 33, 0, 5), num_q_heads=16, num_kv_heads=8),
+    dict(batch=40, ctx_range=(1, 48), context_lens=None, pool_pages=200, max_blocks_per_seq=64),  # 1-3 pages each
+    dict(batch=40, ctx_range=(1, 48), context_lens=None, pool_pages=200, max_blocks_per_seq=64,
+         kv_format="fp8"),                                                                       # paired kernel
+    dict(batch=24, ctx_range=(0, 40), context_lens=None, pool_pages=120, max_blocks_per_seq=64, q_tokens=8,
+         draft_scratch=True),
+    dict(batch=7, context_lens=(1, 0, 17, 2, 33, 0, 5), num_q_heads=16, num_kv_heads=8, pool_pages=40,
+         max_blocks_per_seq=400),
 ]
 
 
