@@ -349,7 +349,7 @@ pa_status pick_geometry(const pa_shape* s, Kind kind, Geom* out, int path = -1) 
   const int e = kind == Kind::kFp8 ? 1 : 2;
   auto search = [&](bool pair, Geom* best) {
     bool have = false;
-    for (int cand = 1; cand <= 4; cand *= 2) {
+    for (int cand = 1; cand <= 8; cand *= 2) {
       if (have && (long)best->BR * best->H2 * s->head_dim * e >= 16384) break;
       Geom g;
       if (!geom_for(s, kind, cand, &g, pair)) {

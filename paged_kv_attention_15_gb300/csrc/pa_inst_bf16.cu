@@ -29,6 +29,15 @@ static SplitKernel by_tiles(int row_tiles, int slice, int cw) {
       return SplitKernel{nullptr, 0, 0, 0};
     }
   }
+  if constexpr (D == 64) {
+    // eight consumer warps, four per row tile, one kv head each: GQA units
+    // of eight kv heads (G T = 4), whose page box of 16 rows x 8 heads x
+    // 128 B is 16 KB
+    if (cw == 8) {
+      if (row_tiles == 2 && slice == 16) return entry<D, 2, 16, 8>();
+      return SplitKernel{nullptr, 0, 0, 0};
+    }
+  }
   if (cw != kConsumerWarps) return SplitKernel{nullptr, 0, 0, 0};
   if (row_tiles == 1 && slice == 16) return entry<D, 1, 16>();
   if constexpr (D == 64) {  // 128-row stages: 32 tokens per warp with one row tile
