@@ -299,21 +299,27 @@ cudaError_t launch_t(const AppendParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Tasks per warp step and slots per task. 16-bit rows: all rounds of four
-// tasks (one round each), of two (two rounds each), else four rounds of one
-// task at a time. fp8 (whose quantiser holds more registers per piece): two
-// one-round tasks, else two rounds of one task at a time (four tasks per
-// step measured slower: the registers halve the resident warps).
+// Tasks per warp step and slots per task. When the call has at least as
+// many tasks as a wave of resident warps: 16-bit rows take all rounds of
+// four tasks (one round each), of two (two rounds each), else four rounds
+// of one task at a time; fp8 rows (whose quantiser holds more registers per
+// piece) two one-round tasks, else two rounds of one task (more tasks per
+// step measured slower: the registers cut the resident warps). Calls with
+// fewer tasks (a decode step's append) keep one task per warp step, so that
+// every task has a warp of its own.
 template <bool FP8, int D>
 cudaError_t launch_d(const AppendParams& p, cudaStream_t stream) {
   constexpr int E = FP8 ? 16 : 8;
   const long long rounds = ((long long)p.Hkv * (D / E) + 31) / 32;
+  const long long wave =
+      (long long)(sm_count() > 0 ? sm_count() : 1) * blocks_per_sm<FP8, D, 1, FP8 ? 2 : 4>() * 8;
+  const bool few = p.tasks < wave;
   if constexpr (FP8) {
-    if (rounds == 1) return launch_t<FP8, D, 2, 1>(p, stream);
+    if (rounds == 1) return few ? launch_t<FP8, D, 1, 1>(p, stream) : launch_t<FP8, D, 2, 1>(p, stream);
     return launch_t<FP8, D, 1, 2>(p, stream);
   } else {
-    if (rounds == 1) return launch_t<FP8, D, 4, 1>(p, stream);
-    if (rounds == 2) return launch_t<FP8, D, 2, 2>(p, stream);
+    if (rounds == 1) return few ? launch_t<FP8, D, 1, 1>(p, stream) : launch_t<FP8, D, 4, 1>(p, stream);
+    if (rounds == 2) return few ? launch_t<FP8, D, 1, 2>(p, stream) : launch_t<FP8, D, 2, 2>(p, stream);
     return launch_t<FP8, D, 1, 4>(p, stream);
   }
 }

@@ -80,6 +80,25 @@ def test_append_matches_oracle_bit_exact(case, kv_format):
     assert_caches_equal(gpu_append(inp), oracle_append(inp))
 
 
+# Calls with at least a wave of resident warps' worth of tasks (2 B T of
+# them): 16-bit rows of one or two 32-piece rounds take several tasks per
+# warp step, whose payload loads all go out before their slot lookups.
+MANY_TASKS = [
+    dict(batch=16, new_tokens=256, num_kv_heads=2, head_dim=128, context_lens=None, ctx_range=(0, 300)),
+    dict(batch=16, new_tokens=256, num_kv_heads=4, head_dim=128, context_lens=None, ctx_range=(0, 300)),
+    dict(batch=16, new_tokens=256, num_kv_heads=3, head_dim=64, page_size=32, context_lens=None,
+         ctx_range=(0, 300)),
+    dict(batch=16, new_tokens=256, num_kv_heads=1, head_dim=256, context_lens=None, ctx_range=(0, 300)),
+]
+
+
+@pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
+@pytest.mark.parametrize("case", MANY_TASKS, ids=[str(i) for i in range(len(MANY_TASKS))])
+def test_append_of_many_tasks_bit_exact(case, kv_format):
+    inp = gen.make_append_inputs(spec(kv_format=kv_format, **case))
+    assert_caches_equal(gpu_append(inp), oracle_append(inp))
+
+
 @pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
 def test_positions_past_capacity_and_bad_pages_are_skipped(kv_format):
     inp = gen.make_append_inputs(spec(kv_format=kv_format, new_tokens=6, context_lens=(40, 42, 0, 3),
