@@ -305,6 +305,12 @@ pa_status pa_decode_set_combine(int32_t mode);
  * shape. Host-only. */
 int32_t pa_decode_kernel_for(const pa_shape* shape, int32_t format);
 
+/* How many kv heads one work unit of that decode takes (the query rows of
+ * those heads share each page's copy: 1, 2, 4 or 8, dividing num_kv_heads),
+ * under the current setting; format as for pa_decode_kernel_for. -1 for an
+ * unsupported shape. Host-only. */
+int32_t pa_decode_heads_per_unit(const pa_shape* shape, int32_t format);
+
 /* A static description of a status code (never NULL). */
 const char* pa_status_string(pa_status status);
 

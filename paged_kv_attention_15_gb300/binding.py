@@ -64,6 +64,7 @@ _SIGNATURES = {
     "pa_decode_set_kernel_path": (ctypes.c_int, [ctypes.c_int32]),
     "pa_decode_set_combine": (ctypes.c_int, [ctypes.c_int32]),
     "pa_decode_kernel_for": (ctypes.c_int32, [ctypes.POINTER(PaShape), ctypes.c_int32]),
+    "pa_decode_heads_per_unit": (ctypes.c_int32, [ctypes.POINTER(PaShape), ctypes.c_int32]),
     "pa_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.POINTER(PaShape), ctypes.c_float, _P, _P,
                                          ctypes.c_int32, _P]),
 }
@@ -321,3 +322,16 @@ def kernel_for_inputs(inp) -> int:
     s = inp.spec
     fmt = "draft" if s.draft_scratch else s.kv_format
     return kernel_for(make_shape(inp.q, inp.k_cache, inp.block_tables), fmt)
+
+
+def heads_per_unit(shape: PaShape, fmt: str) -> int:
+    """kv heads per work unit of a decode of this shape and format ('bf16',
+    'fp8', 'f16', 'draft'); -1 if unsupported."""
+    return int(lib().pa_decode_heads_per_unit(ctypes.byref(shape), _FORMATS[fmt]))
+
+
+def heads_per_unit_inputs(inp) -> int:
+    """heads_per_unit() of a DecodeInputs bundle."""
+    s = inp.spec
+    fmt = "draft" if s.draft_scratch else s.kv_format
+    return heads_per_unit(make_shape(inp.q, inp.k_cache, inp.block_tables), fmt)

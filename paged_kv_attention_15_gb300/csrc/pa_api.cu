@@ -845,6 +845,15 @@ int32_t pa_decode_kernel_for(const pa_shape* shape, int32_t format) {
   return g.path;
 }
 
+int32_t pa_decode_heads_per_unit(const pa_shape* shape, int32_t format) {
+  if (format < 0 || format > 3) return -1;
+  const Kind kind = format == 1 ? Kind::kFp8 : format == 2 ? Kind::kF16 : format == 3 ? Kind::kTidar : Kind::kBf16;
+  if (check_shape(shape, kind) != PA_OK) return -1;
+  Geom g;
+  if (pick_geometry(shape, kind, &g) != PA_OK) return -1;
+  return g.H2;
+}
+
 pa_status pa_decode_profile_events(void* start_event, void* split_done_event) {
   t_ev_start = static_cast<cudaEvent_t>(start_event);
   t_ev_split = static_cast<cudaEvent_t>(split_done_event);

@@ -172,6 +172,33 @@ def test_kernel_choice_per_path(lib):
         pb.set_kernel_path(pb.KERNEL_AUTO)
 
 
+def test_heads_per_unit(lib):
+    """Host-only unit geometry: a unit grows from one kv head while its page
+    box (16 rows x heads x row bytes) stays under 16 KB and an instance
+    covers its rows: four heads for the D = 128 GQA shape, eight at D = 64
+    (16-bit; fp8 has no such instance), and fewer where the group shape or
+    the head count stops it."""
+    bf16, fp8, f16 = 0, 1, 2
+    cases = [
+        (shape(num_q_heads=32, num_kv_heads=8), bf16, 4),                    # gqa: 16 x 4 x 256 B
+        (shape(num_q_heads=32, num_kv_heads=8, head_dim=64), bf16, 8),       # gqa_d64: 16 x 8 x 128 B
+        (shape(num_q_heads=32, num_kv_heads=8, head_dim=64), f16, 8),
+        (shape(num_q_heads=64, num_kv_heads=16, head_dim=64), bf16, 8),
+        (shape(num_q_heads=16, num_kv_heads=4, head_dim=64), bf16, 4),       # only four kv heads
+        (shape(num_q_heads=64, num_kv_heads=8, head_dim=64), bf16, 4),       # G 8: 64 rows at 8 heads
+        (shape(num_q_heads=32, num_kv_heads=8, head_dim=256), bf16, 2),      # 16 x 2 x 512 B
+        (shape(num_q_heads=32, num_kv_heads=2, head_dim=256), fp8, 2),       # the fp8 workload's units
+        (shape(num_q_heads=32, num_kv_heads=8, page_size=64), bf16, 1),      # a 64-row box of one head: 16 KB
+        (shape(num_q_heads=32, num_kv_heads=8, head_dim=64, page_size=64), bf16, 2),   # 64 x 2 x 128 B
+        (shape(num_q_heads=32, num_kv_heads=8, head_dim=64, page_size=256), bf16, 1),  # 128-row stage
+        (shape(q_tokens=4, num_q_heads=8, num_kv_heads=8, head_dim=64), bf16, 8),      # G 1 x T 4
+    ]
+    for s, fmt, want in cases:
+        assert lib.pa_decode_heads_per_unit(ctypes.byref(s), fmt) == want, (s.num_kv_heads, s.head_dim, fmt)
+    assert lib.pa_decode_heads_per_unit(ctypes.byref(shape(head_dim=96)), bf16) == -1
+    assert lib.pa_decode_heads_per_unit(ctypes.byref(shape()), 7) == -1
+
+
 def test_append_validation(lib):
     def call(s, fp8=False, **kw):
         a = dict(kn=FAKE, vn=FAKE, bt=FAKE, cl=FAKE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE)
@@ -222,7 +249,8 @@ int main(void) {
       (any_fn)pa_decode_workspace_size, (any_fn)pa_decode_choose_splits, (any_fn)pa_decode,
       (any_fn)pa_decode_fp8, (any_fn)pa_decode_f16, (any_fn)pa_decode_tidar, (any_fn)pa_decode_tidar_masked,
       (any_fn)pa_decode_reduce, (any_fn)pa_kv_append, (any_fn)pa_kv_append_fp8, (any_fn)pa_decode_noalloc,
-      (any_fn)pa_status_string, (any_fn)pa_decode_profile_events, (any_fn)pa_decode_device_error};
+      (any_fn)pa_status_string, (any_fn)pa_decode_profile_events, (any_fn)pa_decode_device_error,
+      (any_fn)pa_decode_heads_per_unit};
   for (unsigned i = 0; i < sizeof entries / sizeof entries[0]; ++i)
     if (!entries[i]) return 10;
   if (!pa_status_string(PA_OK)[0] || !pa_status_string((pa_status)99)[0]) return 1;
