@@ -77,10 +77,15 @@ WORKLOADS = {
 }
 APPEND_CONFIGS = ("append", "append_fp8", "append_step")
 APPEND_METRIC = "KV-cache append µs/call and achieved HBM GB/s (fraction of 8 TB/s) on 1 GB300"
-SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh"]
-UMMA_KERNEL_SOURCES = ["pa_umma.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
-QROW_KERNEL_SOURCES = ["pa_qrow.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
-PAIR_KERNEL_SOURCES = ["pa_pair.cuh", "pa_kernels.cuh", "pa_ptx.cuh"]
+# Sources of each decode kernel: its device code, the file that builds its
+# instances, and the host code that picks the instance, unit geometry and
+# launch plan for a shape (a change to any of them can change its traffic).
+SPLIT_KERNEL_SOURCES = ["pa_kernels.cuh", "pa_ptx.cuh", "pa_inst_bf16.cu", "pa_inst_f16.cu", "pa_inst_fp8.cu",
+                        "pa_api.cu"]
+UMMA_KERNEL_SOURCES = ["pa_umma.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh", "pa_inst_umma.cu",
+                       "pa_inst_umma_fp8.cu", "pa_api.cu"]
+QROW_KERNEL_SOURCES = ["pa_qrow.cuh", "pa_tc.cuh", "pa_kernels.cuh", "pa_ptx.cuh", "pa_inst_qrow.cu", "pa_api.cu"]
+PAIR_KERNEL_SOURCES = ["pa_pair.cuh", "pa_kernels.cuh", "pa_ptx.cuh", "pa_inst_pair.cu", "pa_api.cu"]
 KERNEL_NAMES = {1: "pa_split_kernel", 2: "pa_umma_kernel", 3: "pa_qrow_kernel", 4: "pa_pair_kernel"}
 KERNEL_SOURCES = {"pa_split_kernel": SPLIT_KERNEL_SOURCES, "pa_umma_kernel": UMMA_KERNEL_SOURCES,
                   "pa_qrow_kernel": QROW_KERNEL_SOURCES, "pa_pair_kernel": PAIR_KERNEL_SOURCES}
