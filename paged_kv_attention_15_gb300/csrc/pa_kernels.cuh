@@ -199,12 +199,19 @@ __device__ __forceinline__ int unit_vpages(int ctx, int P, int tidar, int item_w
   return v > 0 ? v + item_w : 0;
 }
 
+// a / b for a >= 0, b > 0: one 32-bit division while a fits in 32 bits (the
+// usual case; the 64-bit division is a long software sequence on the path to
+// a CTA's first page copy), the same quotient either way.
+__device__ __forceinline__ long long div_nonneg(long long a, int b) {
+  return a < (1LL << 32) ? (long long)((unsigned)a / (unsigned)b) : a / b;
+}
+
 __device__ __forceinline__ void cursor_init(const SplitParams& p, const int* s_start, Cursor& cur) {
   cur.done = 0;
   if (p.num_splits == 0) {
     const long long N = (long long)p.NHG * s_start[p.B];
-    cur.f0 = N * blockIdx.x / p.grid;
-    cur.f1 = N * (blockIdx.x + 1) / p.grid;
+    cur.f0 = div_nonneg(N * blockIdx.x, p.grid);
+    cur.f1 = div_nonneg(N * (blockIdx.x + 1), p.grid);
     cur.f = cur.f0;
   }
 }
@@ -243,7 +250,7 @@ __device__ __forceinline__ bool next_item(const SplitParams& p, const int* s_ctx
     const int b = lo;
     const int nv = s_start[b + 1] - s_start[b];
     const long long ub = (long long)NHG * s_start[b];
-    const int hg = (int)((f - ub) / nv);
+    const int hg = (int)div_nonneg(f - ub, nv);
     const long long us = ub + (long long)hg * nv;
     const long long ue = us + nv;
     const long long end = ue < cur.f1 ? ue : cur.f1;
@@ -312,6 +319,19 @@ struct RingGeom {
 // its sequence's last item), after the consumers released the slot. Raises
 // the abort flag on a timed-out wait and returns once every copy it issued
 // has landed.
+// The tensor maps a launch copies through, fetched while the CTA's prologue
+// (context lengths, prefix sums) runs, so that its first copies do not wait
+// for their descriptors.
+__device__ __forceinline__ void prefetch_maps(const SplitParams& p) {
+  prefetch_tensormap(&p.tm_q);
+  prefetch_tensormap(&p.tm_k);
+  prefetch_tensormap(&p.tm_v);
+  if (p.tidar) {
+    prefetch_tensormap(&p.tm_ks);
+    prefetch_tensormap(&p.tm_vs);
+  }
+}
+
 static __device__ __forceinline__ void produce_ring(const SplitParams& p, const int* s_ctx, const int* s_start,
                                                  const RingGeom& g, uint32_t bar_full, uint32_t bar_empty,
                                                  uint32_t bar_qfull, uint32_t bar_qempty, volatile int* s_abort,
@@ -323,11 +343,6 @@ static __device__ __forceinline__ void produce_ring(const SplitParams& p, const 
   const uint32_t row_bytes = g.row_bytes;
   const uint64_t pol_kv = l2_policy_evict_first();
   const uint64_t pol_q = l2_policy_evict_last();
-  if (lane == 0) {
-    prefetch_tensormap(&p.tm_q);
-    prefetch_tensormap(&p.tm_k);
-    prefetch_tensormap(&p.tm_v);
-  }
   Cursor cur;
   cursor_init(p, s_start, cur);
   Item it;
@@ -336,6 +351,14 @@ static __device__ __forceinline__ void produce_ring(const SplitParams& p, const 
   bool ok = true;
   while (ok && next_item(p, s_ctx, s_start, cur, it)) {
     if (it.nst == 0) continue;
+    // The item's block-table window is read first: the Q copies below
+    // overlap its latency.
+    const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
+    const int pbase = it.tok0 / P;
+    const int npages = it.tok_end > it.tok0 ? (it.tok_end - 1) / P + 1 - pbase : 0;
+    int ibase = 0;
+    int ids = lane < npages ? __ldg(bt_row + pbase + lane) : 0;
+    int ids_next = 32 + lane < npages ? __ldg(bt_row + pbase + 32 + lane) : 0;
     const int qs = qn % g.nq;
     // Warp-uniform verdicts: the lanes leave the loops together.
     if (qn >= g.nq)
@@ -353,12 +376,6 @@ static __device__ __forceinline__ void produce_ring(const SplitParams& p, const 
     }
     ++qn;
 
-    const int32_t* bt_row = p.block_tables + (size_t)it.b * p.max_blocks;
-    const int pbase = it.tok0 / P;
-    const int npages = it.tok_end > it.tok0 ? (it.tok_end - 1) / P + 1 - pbase : 0;
-    int ibase = 0;
-    int ids = lane < npages ? __ldg(bt_row + pbase + lane) : 0;
-    int ids_next = 32 + lane < npages ? __ldg(bt_row + pbase + 32 + lane) : 0;
     for (int j = 0; j < it.nst; ++j, ++stage) {
       const int slot = stage % g.ns;
       if (stage >= g.ns) {
@@ -580,6 +597,7 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
   int* s_ctx = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
   int* s_start = s_ctx + (p.num_splits == 0 ? p.B : 0);
 
+  if (tid == 32 * CW) prefetch_maps(p);  // the producer's lane 0
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);

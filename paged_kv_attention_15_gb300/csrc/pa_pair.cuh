@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(PCfg<D, MT, KV == kKvFp8, TSL>::THREADS, 1)
   int* s_ctx = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
   int* s_start = s_ctx + (p.num_splits == 0 ? p.B : 0);
 
+  if (tid == 32 * 3 * PAIRS) prefetch_maps(p);  // the producer's lane 0
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kQThreads, 1) pa_qrow_kernel(const __grid_cons
   int* s_start = s_ctx + (p.num_splits == 0 ? p.B : 0);
   const float NEG_INF = -__int_as_float(0x7f800000);
 
+  if (tid == 32 * kQProducerWarp) prefetch_maps(p);  // the producer's lane 0
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);

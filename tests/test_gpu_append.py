@@ -100,6 +100,28 @@ def test_append_of_many_tasks_bit_exact(case, kv_format):
 
 
 @pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
+def test_many_task_calls_skip_bad_slots(kv_format):
+    """Several tasks per warp step, some of them skipped: tokens past the
+    block table's capacity (two sequences whose lengths leave room for only
+    10 and 1 of their 256 new tokens) and page ids outside the pool
+    (negative, or past its end)."""
+    inp = gen.make_append_inputs(spec(kv_format=kv_format, batch=16, new_tokens=256, num_kv_heads=2,
+                                      context_lens=None, ctx_range=(0, 300)))
+    bt = inp.block_tables.clone()
+    n, cap = inp.k_cache.shape[0], bt.shape[1] * 16
+    bt[1, 3] = n + 11
+    bt[5, 0] = -1
+    bt[9, 7:12] = -7
+    bt[14, bt.shape[1] - 1] = n
+    lens = inp.context_lens.clone()
+    lens[3] = cap - 10
+    lens[8] = cap - 1
+    inp = dataclasses.replace(inp, block_tables=bt, context_lens=lens)
+    before = inp.clone()
+    assert_caches_equal(gpu_append(inp), oracle_append(before))
+
+
+@pytest.mark.parametrize("kv_format", ["bf16", "f16", "fp8"])
 def test_positions_past_capacity_and_bad_pages_are_skipped(kv_format):
     inp = gen.make_append_inputs(spec(kv_format=kv_format, new_tokens=6, context_lens=(40, 42, 0, 3),
                                       max_blocks_per_seq=3))
