@@ -679,6 +679,9 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
     return min(p.T, (t / p.draft_block + 1) * p.draft_block);
   };
   const int vis0 = visible(rho0), vis1 = visible(rho1);
+  // Every row of this warp's tile is its own (draft units: G T >= 16): a
+  // stage wholly inside the context then needs no score mask.
+  const bool own_rows = __all_sync(0xffffffffu, rok0 && rok1);
   const int lp = 31 - __clz(p.P);  // log2 of the page size (a power of two)
   const uint64_t pol_scale = l2_policy_evict_first();
   const float NEG_INF = -__int_as_float(0x7f800000);
@@ -889,15 +892,25 @@ __global__ void __launch_bounds__(Cfg<D, MT, KV == kKvFp8, TSL, CW>::THREADS, 1)
 
           // ---- scale (and per-token K scale), mask, online softmax in base 2
           const float sl = p.scale_log2;
+          if (!FP8 && own_rows && !scr && valid >= tb + TSL) {
 #pragma unroll
-          for (int i = 0; i < NTS; ++i) {
+            for (int i = 0; i < NTS; ++i) {
+              s[i][0] *= sl;
+              s[i][1] *= sl;
+              s[i][2] *= sl;
+              s[i][3] *= sl;
+            }
+          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = tb + i * 8 + 2 * c4 + (e & 1);
-              float f = s[i][e] * sl;
-              if (FP8) f *= ksc[tok - tb];
-              const int lim = scr ? (e < 2 ? vis0 : vis1) : valid;
-              s[i][e] = (tok < lim && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
+            for (int i = 0; i < NTS; ++i) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int tok = tb + i * 8 + 2 * c4 + (e & 1);
+                float f = s[i][e] * sl;
+                if (FP8) f *= ksc[tok - tb];
+                const int lim = scr ? (e < 2 ? vis0 : vis1) : valid;
+                s[i][e] = (tok < lim && (e < 2 ? rok0 : rok1)) ? f : NEG_INF;
+              }
             }
           }
           float mx0 = NEG_INF, mx1 = NEG_INF;
