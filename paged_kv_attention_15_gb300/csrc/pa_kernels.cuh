@@ -312,13 +312,6 @@ struct RingGeom {
   int nq;                 // Q slots (2: double-buffered across work items; 1)
 };
 
-// The producer warp of the split kernels: walks this CTA's work items and,
-// per item, copies the Q rows of its H2 kv heads into a Q slot and every
-// stage's K and V page boxes into the ring (one box per page, or the
-// stage's rows of one page; the draft-token scratch as the last stage of
-// its sequence's last item), after the consumers released the slot. Raises
-// the abort flag on a timed-out wait and returns once every copy it issued
-// has landed.
 // The tensor maps a launch copies through, fetched while the CTA's prologue
 // (context lengths, prefix sums) runs, so that its first copies do not wait
 // for their descriptors.
@@ -332,6 +325,13 @@ __device__ __forceinline__ void prefetch_maps(const SplitParams& p) {
   }
 }
 
+// The producer warp of the split kernels: walks this CTA's work items and,
+// per item, copies the Q rows of its H2 kv heads into a Q slot and every
+// stage's K and V page boxes into the ring (one box per page, or the
+// stage's rows of one page; the draft-token scratch as the last stage of
+// its sequence's last item), after the consumers released the slot. Raises
+// the abort flag on a timed-out wait and returns once every copy it issued
+// has landed.
 static __device__ __forceinline__ void produce_ring(const SplitParams& p, const int* s_ctx, const int* s_start,
                                                  const RingGeom& g, uint32_t bar_full, uint32_t bar_empty,
                                                  uint32_t bar_qfull, uint32_t bar_qempty, volatile int* s_abort,
