@@ -218,7 +218,7 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g, bool pair = false) 
     const int NSL = NGW / HT;
     // Stage rows: the instance's capacity when a warp's token slice allows
     // it, else 64.
-    for (int rows = cap_rows; rows >= 64 && !k.fn; rows /= 2) {
+    for (int rows = cap_rows; rows >= (cap_rows < 64 ? cap_rows : 64) && !k.fn; rows /= 2) {
       TS = rows / H2;
       if (TS % NSL) continue;
       const int base = TS / NSL;  // tokens per warp if every slice group took every stage

@@ -46,10 +46,14 @@ namespace pa {
 
 constexpr int kConsumerWarps = 4;  // consumer warps of most instances (one per SM sub-partition)
 // Capacity in key rows (tokens x heads) of a pipeline stage: 64, or 128
-// for the 128-byte rows of 16-bit D = 64, so that a stage's K tile can be
-// 16 KB and the per-stage waits and arrivals spread over as many bytes.
+// for the 128-byte rows of 16-bit D = 64 and 32 for the 512-byte rows of
+// 16-bit D = 256, so that a stage's K tile is 16 KB: the per-stage waits and
+// arrivals spread over as many bytes, and D = 256 keeps five stages in the
+// ring instead of two of 64 KB.
 // The host picks the rows a launch actually uses per stage (p.TS * H2).
-constexpr int stage_rows(int row_bytes, bool fp8) { return !fp8 && row_bytes <= 128 ? 128 : 64; }
+constexpr int stage_rows(int row_bytes, bool fp8) {
+  return fp8 ? 64 : (row_bytes <= 128 ? 128 : (row_bytes >= 512 ? 32 : 64));
+}
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kErrWaitTimeout = 1;
