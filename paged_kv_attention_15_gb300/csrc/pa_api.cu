@@ -209,6 +209,9 @@ bool geom_for(const pa_shape* s, Kind kind, int H2, Geom* g, bool pair = false) 
   // such an instance is built, else four.
   const bool fp8 = kind == Kind::kFp8;
   const int cap_rows = pa::stage_rows(D * (fp8 ? 1 : 2), fp8);
+  // The draft block's scratch stage lands TP rows of each of the unit's
+  // heads in one stage tile.
+  if (kind == Kind::kTidar && (T + 7) / 8 * 8 * H2 > cap_rows) return false;
   const int HT = GT >= 16 ? 1 : (16 / GT < H2 ? 16 / GT : H2);  // heads in a row tile
   SplitKernel k{nullptr, 0, 0, 0};
   int TS = 0, TSL = 0, ilv = 1;

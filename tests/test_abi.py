@@ -193,6 +193,13 @@ def test_heads_per_unit(lib):
         (shape(num_q_heads=32, num_kv_heads=8, head_dim=64, page_size=256), bf16, 1),  # 128-row stage
         (shape(q_tokens=4, num_q_heads=8, num_kv_heads=8, head_dim=64), bf16, 8),      # G 1 x T 4
     ]
+    draft = 3
+    cases += [  # draft blocks: the scratch stage's T (rounded up to 8) rows per head fit one stage tile
+        (shape(q_tokens=8, num_q_heads=32, num_kv_heads=8), draft, 2),                   # TiDAR: 2 x 32 rows
+        (shape(q_tokens=16, num_q_heads=32, num_kv_heads=8), draft, 1),                  # the long draft
+        (shape(q_tokens=4, num_q_heads=16, num_kv_heads=4, head_dim=256), draft, 2),     # 2 x 8 of 32 rows
+        (shape(q_tokens=32, num_q_heads=4, num_kv_heads=4, head_dim=256), draft, 1),     # 32 of 32 rows
+    ]
     for s, fmt, want in cases:
         assert lib.pa_decode_heads_per_unit(ctypes.byref(s), fmt) == want, (s.num_kv_heads, s.head_dim, fmt)
     assert lib.pa_decode_heads_per_unit(ctypes.byref(shape(head_dim=96)), bf16) == -1
